@@ -1,0 +1,177 @@
+"""CPU oracle for the single-token KV-cache decode step (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline arm of ``bench.py``
+may import this package.  The product path (the CUDA library and its binding) never
+does: the two share no code.  The arithmetic lives in ``kvc_oracle.c`` (plain C,
+double precision); this module builds it with gcc and marshals numpy arrays.
+
+bf16 tensors are passed as their raw ``uint16`` bit patterns; fp32 as ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvc_oracle.c")
+_SO = os.path.join(_HERE, "libkvc_oracle.so")
+
+BF16, F32 = 0, 1
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when the compiler has it).  Returns the .so path."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        P, I, U64, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64
+        L.oracle_kv_bytes.restype = U64
+        L.oracle_kv_bytes.argtypes = [I64] * 6
+        L.oracle_kv_bytes_ragged.restype = U64
+        L.oracle_kv_bytes_ragged.argtypes = [I64, I64, I64, I64, P, I]
+        L.oracle_append.restype = I
+        L.oracle_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
+        L.oracle_prefill_write.restype = I
+        L.oracle_prefill_write.argtypes = [P, P, P, P, I, P, I, I, I, I, I]
+        L.oracle_decode_attn.restype = I
+        L.oracle_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+        L.oracle_layer_full.restype = None
+        L.oracle_layer_full.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P]
+        L.oracle_layer_incremental.restype = None
+        L.oracle_layer_incremental.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+        L.oracle_set_fault.restype = None
+        L.oracle_set_fault.argtypes = [I]
+        L.oracle_get_fault.restype = I
+        L.oracle_set_threads.restype = I
+        L.oracle_set_threads.argtypes = [I]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return F32
+    raise TypeError(f"oracle takes bf16 bits (uint16) or float32, got {a.dtype}")
+
+
+def kv_bytes(L, B, H_kv, D, T, s) -> int:
+    return int(lib().oracle_kv_bytes(L, B, H_kv, D, T, s))
+
+
+def kv_bytes_ragged(L, H_kv, D, s, T_i) -> int:
+    t = np.ascontiguousarray(np.asarray(T_i, dtype=np.int32))
+    return int(lib().oracle_kv_bytes_ragged(L, H_kv, D, s, _ptr(t), t.size))
+
+
+def append(Kc, Vc, k_new, v_new, lens) -> int:
+    """In place: writes k_new/v_new [B,H_kv,D] into slot lens[b]-1 of Kc/Vc [B,H_kv,T_max,D]."""
+    B, H_kv, T_max, D = Kc.shape
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_append(_ptr(Kc), _ptr(Vc), _ptr(k_new), _ptr(v_new), _ptr(lens),
+                               B, H_kv, T_max, D, _dtype_code(Kc))
+
+
+def prefill_write(Kc, Vc, K, V, lens) -> int:
+    """In place: copies K/V [B,H_kv,T_in,D] slots [0, lens[b]) into Kc/Vc."""
+    B, H_kv, T_max, D = Kc.shape
+    T_in = K.shape[2]
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_prefill_write(_ptr(Kc), _ptr(Vc), _ptr(K), _ptr(V), T_in, _ptr(lens),
+                                      B, H_kv, T_max, D, _dtype_code(Kc))
+
+
+def decode_attn(q, Kc, Vc, lens, return_bad: bool = False):
+    """out[B,H_q,D] (float64) = softmax(q K^T / sqrt(D)) V over slots [0, lens[b])."""
+    B, H_q, D = q.shape
+    _, H_kv, T_max, D2 = Kc.shape
+    assert D == D2 and Kc.shape == Vc.shape and q.dtype == Kc.dtype == Vc.dtype
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros((B, H_q, D), dtype=np.float64)
+    bad = lib().oracle_decode_attn(_ptr(q), _ptr(Kc), _ptr(Vc), _ptr(lens), B, H_q, H_kv, T_max,
+                                   D, _dtype_code(q), _ptr(out))
+    return (out, bad) if return_bad else out
+
+
+def layer_full(x, WQ, WK, WV, WO, H_q, H_kv, D):
+    """Path A (dense causal layer).  Returns (out[B,T,hidden], K[B,H_kv,T,D], V[...])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    B, T, hidden = x.shape
+    Ws = [np.ascontiguousarray(w, dtype=np.float64) for w in (WQ, WK, WV, WO)]
+    out = np.zeros((B, T, hidden))
+    K = np.zeros((B, H_kv, T, D))
+    V = np.zeros((B, H_kv, T, D))
+    lib().oracle_layer_full(_ptr(x), B, T, hidden, H_q, H_kv, D, *[_ptr(w) for w in Ws],
+                            _ptr(out), _ptr(K), _ptr(V))
+    return out, K, V
+
+
+def layer_incremental(x, T_p, WQ, WK, WV, WO, H_q, H_kv, D):
+    """Path B (prefill T_p, then one token at a time through the cache).
+    Returns (decode outputs [B, T-T_p, hidden], final K cache, final V cache)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    B, T, hidden = x.shape
+    Ws = [np.ascontiguousarray(w, dtype=np.float64) for w in (WQ, WK, WV, WO)]
+    out = np.zeros((B, T - T_p, hidden))
+    Kc = np.zeros((B, H_kv, T, D))
+    Vc = np.zeros((B, H_kv, T, D))
+    lib().oracle_layer_incremental(_ptr(x), B, T_p, T, hidden, H_q, H_kv, D,
+                                   *[_ptr(w) for w in Ws], _ptr(out), _ptr(Kc), _ptr(Vc))
+    return out, Kc, Vc
+
+
+class planted_fault:
+    """Context manager that plants a known mistake in the oracle (tests only).
+
+    1 = interleaved GQA map (j mod H_kv), 2 = score scale 1/D, 3 = append one slot late,
+    4 = the new token left out of the attention."""
+
+    def __init__(self, which: int):
+        self.which = which
+
+    def __enter__(self):
+        lib().oracle_set_fault(self.which)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_fault(0)
+        return False
+
+
+def set_threads(n: int) -> int:
+    """Host threads for decode_attn (OpenMP over rows); returns the count in effect."""
+    return int(lib().oracle_set_threads(int(n)))
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))

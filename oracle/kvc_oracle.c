@@ -1,0 +1,361 @@
+/*
+ * kvc_oracle.c -- plain, slow CPU oracle for the single-token KV-cache decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call this file:
+ * only the tests, the package's smoke check and the benchmark's CPU-baseline arm use it.
+ * It shares no code, header, table or constant with the CUDA library; it includes only
+ * the C standard library.
+ *
+ * Every floating-point reduction is done in double precision, in the order the
+ * definition is written, with no blocking, fusion or reordering.
+ *
+ * Sources (web pages on the KV cache; page title, then section):
+ *   [KVG]  "KV 缓存" (llm-glossary, terms/kv-cache): "两条数学等价的 decode 路径",
+ *          "可直接运行的对照实验", "容量公式：先算逻辑 payload，再谈 allocator".
+ *   [W1D4] "第 1 周 · Day 4：KV Cache 与 MQA / GQA" (CME295 notes): §1.2, §1.3, §1.4,
+ *          §2.3, §3.1, §3.3, §3.4.
+ *   [M11]  "11.7 KV Cache：形状、显存与带宽" (Linear-Algebra-to-LLM): §2.2, §2.3, §4.2-§5.4.
+ *
+ * Readings taken where the pages are silent or garbled (listed in the design notes too):
+ *   - score scale is 1/sqrt(D): [M11] §2.2 prints "/d_k" (the square root was lost in
+ *     extraction); the teaching code in [KVG] divides by math.sqrt(head_dim).
+ *   - the new token attends to itself: append first, then attend over all L slots
+ *     ([W1D4] §1.3: "q 对缓存里全部 t+1 个 key 做注意力").
+ *   - lens[b] is the valid length AFTER the call's write; append writes slot lens[b]-1.
+ *   - query head j reads KV head floor(j / (H_q/H_kv))  ([W1D4] §3.4, repeat_interleave).
+ *   - a row with lens[b] < 1 or lens[b] > T_max is invalid: its output is zero and it is
+ *     counted in the return value.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_BF16 0
+#define OR_F32 1
+
+/* Planted-mistake switch for the tests that show the pins have teeth.  0 = correct. */
+static int g_fault = 0;
+void oracle_set_fault(int which) { g_fault = which; }
+int oracle_get_fault(void) { return g_fault; }
+
+static int g_threads = 1;
+/* Number of host threads the decode routine may use (1 = plain single-threaded loop). */
+int oracle_set_threads(int n) {
+    g_threads = n < 1 ? 1 : n;
+#ifdef _OPENMP
+    return g_threads;
+#else
+    g_threads = 1;
+    return 1;
+#endif
+}
+
+/* One stored element as a double.  bf16 is the top half of an IEEE binary32, so widening
+ * it is exact; fp32 widens exactly too. */
+static double load_elem(const void* base, int dtype, size_t idx) {
+    if (dtype == OR_F32) return (double)((const float*)base)[idx];
+    uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static int elem_bytes_of(int dtype) { return dtype == OR_F32 ? 4 : 2; }
+
+/* ---------------------------------------------------------------------------------------
+ * Capacity: [KVG] 容量公式 and [W1D4] §1.4: bytes = 2 * L * H_kv * D * (B * T) * s, the 2
+ * counting K and V.  The ragged form ([KVG], same section) replaces B*T by sum_i T_i.
+ * ------------------------------------------------------------------------------------- */
+uint64_t oracle_kv_bytes(int64_t L, int64_t B, int64_t H_kv, int64_t D, int64_t T, int64_t s) {
+    return (uint64_t)2 * (uint64_t)L * (uint64_t)H_kv * (uint64_t)D * ((uint64_t)B * (uint64_t)T) *
+           (uint64_t)s;
+}
+
+uint64_t oracle_kv_bytes_ragged(int64_t L, int64_t H_kv, int64_t D, int64_t s, const int32_t* T_i,
+                                int n) {
+    uint64_t sum = 0;
+    for (int i = 0; i < n; ++i) sum += (uint64_t)T_i[i];
+    return (uint64_t)2 * (uint64_t)L * (uint64_t)H_kv * (uint64_t)D * (uint64_t)s * sum;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Cache writes.  [W1D4] §3.1: the cache is preallocated to max_len and the new rows are
+ * written in place at [pos, pos+T); [KVG] "从教学代码到生产实现还差什么" item 1.
+ * Layout [B, H_kv, T_max, D], row = one token's D-vector.
+ * ------------------------------------------------------------------------------------- */
+
+/* Writes k_new[b,h,:] / v_new[b,h,:] (layout [B,H_kv,D]) into slot lens[b]-1.
+ * Returns the number of batch rows skipped because lens[b] is out of [1, T_max]. */
+int oracle_append(void* Kc, void* Vc, const void* k_new, const void* v_new, const int32_t* lens,
+                  int B, int H_kv, int T_max, int D, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 1 || L > T_max) {
+            ++bad;
+            continue;
+        }
+        int slot = L - 1;
+        if (g_fault == 3) slot = L; /* planted: off-by-one slot */
+        if (slot >= T_max) continue;
+        for (int h = 0; h < H_kv; ++h) {
+            size_t dst = (((size_t)b * H_kv + h) * T_max + slot) * row;
+            size_t src = ((size_t)b * H_kv + h) * row;
+            memcpy((char*)Kc + dst, (const char*)k_new + src, row);
+            memcpy((char*)Vc + dst, (const char*)v_new + src, row);
+        }
+    }
+    return bad;
+}
+
+/* Writes K[b,h,0:lens[b],:] (layout [B,H_kv,T_in,D]) into cache slots [0, lens[b]).
+ * Returns the number of rows skipped because lens[b] is out of [0, min(T_in, T_max)]. */
+int oracle_prefill_write(void* Kc, void* Vc, const void* K, const void* V, int T_in,
+                         const int32_t* lens, int B, int H_kv, int T_max, int D, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 0 || L > T_in || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h)
+            for (int t = 0; t < L; ++t) {
+                size_t dst = (((size_t)b * H_kv + h) * T_max + t) * row;
+                size_t src = (((size_t)b * H_kv + h) * T_in + t) * row;
+                memcpy((char*)Kc + dst, (const char*)K + src, row);
+                memcpy((char*)Vc + dst, (const char*)V + src, row);
+            }
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Decode attention for one query row, in double.  [M11] §2.2:
+ *   s_t = q . k_t / sqrt(D),   o = softmax(s) V
+ * over t in [0, L).  The softmax subtracts the row maximum before exponentiating (the same
+ * value mathematically; it keeps exp finite).
+ * q: D doubles; K, V: L rows of D doubles at stride `ld`; o: D doubles.
+ * ------------------------------------------------------------------------------------- */
+static void decode_row_f64(const double* q, const double* K, const double* V, int L, int D,
+                           size_t ld, double* o, double* s /* scratch, L doubles */) {
+    double scale = 1.0 / sqrt((double)D);
+    if (g_fault == 2) scale = 1.0 / (double)D; /* planted: the garbled "/d_k" reading */
+    int Lr = (g_fault == 4) ? L - 1 : L;       /* planted: new token left out */
+    if (Lr < 1) Lr = 1;
+    for (int t = 0; t < Lr; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += q[d] * K[(size_t)t * ld + d];
+        s[t] = acc * scale;
+    }
+    double m = s[0];
+    for (int t = 1; t < Lr; ++t)
+        if (s[t] > m) m = s[t];
+    double Z = 0.0;
+    for (int t = 0; t < Lr; ++t) {
+        s[t] = exp(s[t] - m);
+        Z += s[t];
+    }
+    for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t < Lr; ++t) acc += s[t] * V[(size_t)t * ld + d];
+        o[d] = acc / Z;
+    }
+}
+
+/* KV head read by query head j: [W1D4] §3.4, floor(j / (H_q / H_kv)). */
+static int kv_head_of(int j, int H_q, int H_kv) {
+    int g = H_q / H_kv;
+    if (g_fault == 1) return j % H_kv; /* planted: interleaved ("repeat") grouping */
+    return j / g;
+}
+
+/* Decode attention over the cache.
+ *   q     [B, H_q, D]           (dtype)
+ *   Kc,Vc [B, H_kv, T_max, D]   (dtype)
+ *   lens  [B]                   valid length of each sequence (the new token included)
+ *   out   [B, H_q, D]           double
+ * Returns the number of invalid rows (lens out of [1, T_max]); their output is zero. */
+int oracle_decode_attn(const void* q, const void* Kc, const void* Vc, const int32_t* lens, int B,
+                       int H_q, int H_kv, int T_max, int D, int dtype, double* out) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        if (lens[b] < 1 || lens[b] > T_max) ++bad;
+    const int rows = B * H_q;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) if (g_threads > 1)
+#endif
+    for (int r = 0; r < rows; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (L < 1 || L > T_max) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        size_t base = ((size_t)b * H_kv + h) * (size_t)T_max * D;
+        for (size_t i = 0; i < (size_t)L * D; ++i) {
+            Kd[i] = load_elem(Kc, dtype, base + i);
+            Vd[i] = load_elem(Vc, dtype, base + i);
+        }
+        decode_row_f64(qd, Kd, Vd, L, D, (size_t)D, o, s);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(s);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * One attention layer, two ways ([KVG] "两条数学等价的 decode 路径"; [W1D4] §1.3).
+ * x: [B, T, hidden]; W_Q [hidden, H_q*D], W_K / W_V [hidden, H_kv*D], W_O [H_q*D, hidden],
+ * all double, row-major.  No RoPE, no norm: the pages' single-layer teaching setting.
+ * ------------------------------------------------------------------------------------- */
+
+/* y[T, n] = x[T, k] @ W[k, n] */
+static void matmul(const double* x, const double* W, double* y, int T, int k, int n) {
+    for (int t = 0; t < T; ++t)
+        for (int c = 0; c < n; ++c) {
+            double acc = 0.0;
+            for (int i = 0; i < k; ++i) acc += x[(size_t)t * k + i] * W[(size_t)i * n + c];
+            y[(size_t)t * n + c] = acc;
+        }
+}
+
+/* Path A: dense causal attention over all T positions (the prefill of the pages): every
+ * query position i sees keys 0..i (the triu(-inf) mask).  Writes out[B,T,hidden] and, when
+ * Kout/Vout are non-null, the projected K/V in cache layout [B, H_kv, T, D]. */
+void oracle_layer_full(const double* x, int B, int T, int hidden, int H_q, int H_kv, int D,
+                       const double* WQ, const double* WK, const double* WV, const double* WO,
+                       double* out, double* Kout, double* Vout) {
+    const int nq = H_q * D, nkv = H_kv * D;
+    double* Q = (double*)malloc(sizeof(double) * (size_t)T * nq);
+    double* K = (double*)malloc(sizeof(double) * (size_t)T * nkv);
+    double* V = (double*)malloc(sizeof(double) * (size_t)T * nkv);
+    double* ctx = (double*)malloc(sizeof(double) * (size_t)T * nq);
+    double* s = (double*)malloc(sizeof(double) * (size_t)T);
+    const double scale = 1.0 / sqrt((double)D);
+    for (int b = 0; b < B; ++b) {
+        const double* xb = x + (size_t)b * T * hidden;
+        matmul(xb, WQ, Q, T, hidden, nq);
+        matmul(xb, WK, K, T, hidden, nkv);
+        matmul(xb, WV, V, T, hidden, nkv);
+        for (int j = 0; j < H_q; ++j) {
+            int h = j / (H_q / H_kv);
+            for (int i = 0; i < T; ++i) {
+                /* full score row with the causal mask: positions > i get -inf */
+                for (int t = 0; t < T; ++t) {
+                    if (t > i) {
+                        s[t] = -INFINITY;
+                        continue;
+                    }
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += Q[(size_t)i * nq + j * D + d] * K[(size_t)t * nkv + h * D + d];
+                    s[t] = acc * scale;
+                }
+                double m = -INFINITY;
+                for (int t = 0; t < T; ++t)
+                    if (s[t] > m) m = s[t];
+                double Z = 0.0;
+                for (int t = 0; t < T; ++t) {
+                    s[t] = exp(s[t] - m); /* exp(-inf) = 0 for masked positions */
+                    Z += s[t];
+                }
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int t = 0; t < T; ++t) acc += s[t] * V[(size_t)t * nkv + h * D + d];
+                    ctx[(size_t)i * nq + j * D + d] = acc / Z;
+                }
+            }
+        }
+        matmul(ctx, WO, out + (size_t)b * T * hidden, T, nq, hidden);
+        if (Kout && Vout)
+            for (int h = 0; h < H_kv; ++h)
+                for (int t = 0; t < T; ++t)
+                    for (int d = 0; d < D; ++d) {
+                        size_t c = (((size_t)b * H_kv + h) * T + t) * D + d;
+                        Kout[c] = K[(size_t)t * nkv + h * D + d];
+                        Vout[c] = V[(size_t)t * nkv + h * D + d];
+                    }
+    }
+    free(Q);
+    free(K);
+    free(V);
+    free(ctx);
+    free(s);
+}
+
+/* Path B: prefill the first T_p positions once (path A on the prompt, keeping its K/V in a
+ * preallocated cache of T_total slots), then for each later position project only that
+ * token, write its k/v at the next slot, and attend with the decode routine over all slots
+ * written so far.  out[B, T_total - T_p, hidden] holds the decode outputs; Kc/Vc
+ * [B, H_kv, T_total, D] hold the final cache. */
+void oracle_layer_incremental(const double* x, int B, int T_p, int T_total, int hidden, int H_q,
+                              int H_kv, int D, const double* WQ, const double* WK,
+                              const double* WV, const double* WO, double* out, double* Kc,
+                              double* Vc) {
+    const int nq = H_q * D, nkv = H_kv * D;
+    double* pre_out = (double*)malloc(sizeof(double) * (size_t)T_p * hidden);
+    double* Kp = (double*)malloc(sizeof(double) * (size_t)H_kv * T_p * D);
+    double* Vp = (double*)malloc(sizeof(double) * (size_t)H_kv * T_p * D);
+    double* q = (double*)malloc(sizeof(double) * nq);
+    double* k = (double*)malloc(sizeof(double) * nkv);
+    double* v = (double*)malloc(sizeof(double) * nkv);
+    double* ctx = (double*)malloc(sizeof(double) * nq);
+    double* s = (double*)malloc(sizeof(double) * (size_t)T_total);
+    for (int b = 0; b < B; ++b) {
+        const double* xb = x + (size_t)b * T_total * hidden;
+        double* Kb = Kc + (size_t)b * H_kv * T_total * D;
+        double* Vb = Vc + (size_t)b * H_kv * T_total * D;
+        memset(Kb, 0, sizeof(double) * (size_t)H_kv * T_total * D);
+        memset(Vb, 0, sizeof(double) * (size_t)H_kv * T_total * D);
+        oracle_layer_full(xb, 1, T_p, hidden, H_q, H_kv, D, WQ, WK, WV, WO, pre_out, Kp, Vp);
+        for (int h = 0; h < H_kv; ++h)
+            for (int t = 0; t < T_p; ++t)
+                for (int d = 0; d < D; ++d) {
+                    Kb[((size_t)h * T_total + t) * D + d] = Kp[((size_t)h * T_p + t) * D + d];
+                    Vb[((size_t)h * T_total + t) * D + d] = Vp[((size_t)h * T_p + t) * D + d];
+                }
+        for (int pos = T_p; pos < T_total; ++pos) {
+            const double* xt = xb + (size_t)pos * hidden;
+            matmul(xt, WQ, q, 1, hidden, nq);
+            matmul(xt, WK, k, 1, hidden, nkv);
+            matmul(xt, WV, v, 1, hidden, nkv);
+            for (int h = 0; h < H_kv; ++h)
+                for (int d = 0; d < D; ++d) {
+                    Kb[((size_t)h * T_total + pos) * D + d] = k[h * D + d];
+                    Vb[((size_t)h * T_total + pos) * D + d] = v[h * D + d];
+                }
+            const int L = pos + 1;
+            for (int j = 0; j < H_q; ++j) {
+                int h = kv_head_of(j, H_q, H_kv);
+                decode_row_f64(q + j * D, Kb + (size_t)h * T_total * D,
+                               Vb + (size_t)h * T_total * D, L, D, (size_t)D, ctx + j * D, s);
+            }
+            matmul(ctx, WO, out + ((size_t)b * (T_total - T_p) + (pos - T_p)) * hidden, 1, nq,
+                   hidden);
+        }
+    }
+    free(pre_out);
+    free(Kp);
+    free(Vp);
+    free(q);
+    free(k);
+    free(v);
+    free(ctx);
+    free(s);
+}
