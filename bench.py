@@ -1,0 +1,416 @@
+"""Benchmark of the single-token KV-cache decode step (append + decode attention, every layer).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-graph]
+
+Prints ONE JSON line on rank 0.  A step = one decode step of the whole model: for each of the
+workload's layers one fused kvc_decode_step (append the new token, attend over the history).
+The metric is the decode-attention KV-read bandwidth, 2 * H_kv * D * s * sum_b L_b bytes per
+layer, divided by the step time.  Inputs are synthetic (counter-based generator), resident in
+HBM, and larger than L2 (every layer has its own cache).
+
+--impl reference times the CPU oracle (the plain C, fp64 restatement of the pages) on the
+host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-read GB/s (% of GB300 HBM peak) and µs/step, 8B-GQA B=24"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(w, budget_s: float, threads: int, max_layers: int | None = None):
+    """Times the oracle on whole layers of the workload until budget_s is used (at least one
+    layer).  Returns (GB/s of algorithmic KV read, layers done, seconds, threads used)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from kv_cache_decode_kvc_gb300 import synth
+
+    used = oracle.set_threads(threads)
+    lens = w.lens()
+    lens_np = lens.numpy()
+    done, secs, nbytes = 0, 0.0, 0
+    layers = w.layers if max_layers is None else min(w.layers, max_layers)
+    for layer in range(layers):
+        # the post-append cache of this layer is the generator's rows [0, L_b) of each stream
+        T_max = int(lens.max())
+        K = synth.bf16_bits(synth.block(w.seed, layer, "K", 0, w.B, w.H_kv, 0, T_max, w.D, w.B))
+        V = synth.bf16_bits(synth.block(w.seed, layer, "V", 0, w.B, w.H_kv, 0, T_max, w.D, w.B))
+        q = synth.bf16_bits(synth.queries(w.seed, layer, w.B, w.H_q, w.D))
+        t0 = time.perf_counter()
+        oracle.decode_attn(q, K, V, lens_np)
+        secs += time.perf_counter() - t0
+        nbytes += w.kv_read_bytes_per_layer()
+        done += 1
+        if secs >= budget_s:
+            break
+    return nbytes / secs / 1e9, done, secs, used
+
+
+def run_reference(args, w):
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        gbs, layers, secs, used = oracle_sample(w, budget_s=0.0, threads=threads, max_layers=1)
+        if i >= args.warmup:
+            per_step.append((gbs, secs))
+    gbs = statistics.median(g for g, _ in per_step)
+    sample = f"layer 0 of {w.name} (all {w.B} sequences x {w.H_q} query heads) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(s for _, s in per_step), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+def traffic_from_profiles(kernel_src_hash: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_gqa8b_b24.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path, encoding="utf-8"):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_decode_kvc_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_decode_kvc_gb300 import kvc
+    from kv_cache_decode_kvc_gb300.workloads import fill_layer, step_inputs
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    kvc.load()  # fails loudly without the CUDA library
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    seed = w.seed + 7919 * rank  # each replica decodes its own batch (weak scaling)
+    L = w.layers
+    cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
+    t_fill = time.perf_counter()
+    for layer in range(L):
+        fill_layer(cache, layer, w, seed=seed)
+    ins = [step_inputs(w, layer, seed=seed) for layer in range(L)]
+    outs = [torch.empty(w.B, w.H_q, w.D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    lens_d = w.lens().to(dev)
+    torch.cuda.synchronize()
+    t_fill = time.perf_counter() - t_fill
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+
+    def step():
+        for layer in range(L):
+            q, kn, vn = ins[layer]
+            kvc.kvc_decode_step(cache.h, layer, q, kn, vn, outs[layer], lens_d, sptr)
+
+    # the automatic merge path adds a combine kernel per layer when streams are few and long
+    # (same rule as the library: segments per stream x group outputs above 64 KB)
+    P, U = kvc.kvc_get_ctas(cache.h), w.B * w.H_kv
+    nseg = (P + U - 1) // U + 1
+    launches_per_step = 2 * L if nseg * w.G * w.D * 4 > 65536 else L
+
+    graph = None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+        stream.synchronize()
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            for _ in range(args.warmup):
+                graph.replay()
+        stream.synchronize()
+    st, detail = cache.last_error(sptr)
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"device error during warm-up: status {st} detail {detail:#x}")
+
+    run = graph.replay if graph is not None else step
+
+    # ---- timed region: K steps, barrier + synchronize on both sides, CUDA events on `stream`
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(vis.split(",")[local] if vis else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st, detail = cache.last_error(sptr)
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
+
+    kv_bytes_step = L * w.kv_read_bytes_per_layer()
+    gbs = world * kv_bytes_step / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # ---- per-launch durations of the decode kernel (events around each launch, same stream)
+    per_launch = []
+    with torch.cuda.stream(stream):
+        evs = []
+        for _ in range(max(1, min(args.steps, 5))):
+            for layer in range(L):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                q, kn, vn = ins[layer]
+                kvc.kvc_decode_step(cache.h, layer, q, kn, vn, outs[layer], lens_d, sptr)
+                b.record(stream)
+                evs.append((a, b))
+    torch.cuda.synchronize()
+    per_launch = [a.elapsed_time(b) for a, b in evs]
+    launch_ms = statistics.mean(per_launch)
+    B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
+    alg_bytes_launch = (w.kv_read_bytes_per_layer() + 2 * B * Hq * D * s  # q read, out written
+                        + 4 * B * Hkv * D * s + 4 * B)                    # k/v new read + written, lens
+    achieved = alg_bytes_launch / (launch_ms * 1e-3) / 1e9
+    traffic = traffic_from_profiles(kernel_source_hash())
+
+    # ---- end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
+    h_q = [i[0].cpu().pin_memory() for i in ins]
+    h_kn = [i[1].cpu().pin_memory() for i in ins]
+    h_vn = [i[2].cpu().pin_memory() for i in ins]
+    h_lens = w.lens().pin_memory()
+    h_out = [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    d_q = [torch.empty_like(i[0]) for i in ins]
+    d_kn = [torch.empty_like(i[1]) for i in ins]
+    d_vn = [torch.empty_like(i[2]) for i in ins]
+    d_lens = torch.empty_like(lens_d)
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_kn + h_vn) + h_lens.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        d_lens.copy_(h_lens, non_blocking=True)
+        for layer in range(L):
+            d_q[layer].copy_(h_q[layer], non_blocking=True)
+            d_kn[layer].copy_(h_kn[layer], non_blocking=True)
+            d_vn[layer].copy_(h_vn[layer], non_blocking=True)
+            kvc.kvc_decode_step(cache.h, layer, d_q[layer], d_kn[layer], d_vn[layer], outs[layer], d_lens, sptr)
+            h_out[layer].copy_(outs[layer], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_gbs = world * kv_bytes_step / (e2e_ms * 1e-3) / 1e9
+    st, detail = cache.last_error(sptr)
+    if st != kvc.KVC_OK:
+        raise RuntimeError(f"device error in the e2e region: status {st} detail {detail:#x}")
+
+    # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        cgbs, layers_done, secs, used = oracle_sample(w, budget_s=args.cpu_budget, threads=threads)
+        cpu = {"value": round(cgbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+               "sample": f"{layers_done} whole layer(s) of {w.name} ({secs:.1f} s of oracle time, "
+                         f"{used} threads)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "us_per_step": round(ms * 1e3, 1), "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
+            "pct_of_nominal_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+            "attn_tokens_per_s": round(world * w.B / (ms * 1e-3), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (counter-based generator, bf16)",
+            "config": {"workload": w.name, "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
+                       "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
+                       "kv_bytes_per_step": kv_bytes_step,
+                       "l2": "inputs larger than L2 (each layer has its own cache; "
+                             f"{kv_bytes_step / 1e9:.1f} GB read per step)",
+                       "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                         "kernel": "decode_kernel<bf16,128,4>", "launch_us": round(launch_ms * 1e3, 2),
+                         "alg_bytes_per_launch": alg_bytes_launch},
+            "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clock_info,
+            "cpu_baseline": cpu,
+            "setup_s": round(t_fill, 1),
+        }
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

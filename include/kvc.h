@@ -1,0 +1,145 @@
+/*
+ * kvc.h -- C ABI of the GB300 (sm_103a) single-token KV-cache decode step.
+ *
+ * What it computes (sources are web pages on the KV cache, cited by title and section):
+ *   - a per-layer cache K, V in layout [B, H_kv, T_max, D], preallocated once and written
+ *     in place ("第 1 周 · Day 4：KV Cache 与 MQA / GQA" §3.1; "KV 缓存" glossary page,
+ *     "从教学代码到生产实现还差什么" item 1);
+ *   - append: the new token's k_t, v_t go to slot lens[b]-1 of every KV head
+ *     ("KV 缓存", "两条数学等价的 decode 路径", path B);
+ *   - decode attention: for every query head j of sequence b,
+ *         o[b,j,:] = softmax_t( q[b,j,:] . K[b,h,t,:] / sqrt(D) ) V[b,h,t,:],  t in [0, lens[b]),
+ *     with h = floor(j / (H_q/H_kv))  ("11.7 KV Cache：形状、显存与带宽" §2.2 single-step
+ *     decode; "第 1 周 · Day 4" §3.4 for the grouped-query head map);
+ *   - capacity: bytes = 2 * L * H_kv * D * B * T * s  ("第 1 周 · Day 4" §1.4; "KV 缓存",
+ *     容量公式, whose ragged form replaces B*T by sum_i T_i).
+ *
+ * Conventions used by every call:
+ *   - lens (int32 [B], DEVICE memory) is the valid length of each sequence AFTER the call's
+ *     own write.  One decode step is: lens += 1; kvc_append(...lens); kvc_decode_attn(...lens),
+ *     or the fused kvc_decode_step(...lens).  The new token attends to itself.
+ *   - All tensor pointers are DEVICE pointers, dense row-major, in the cache dtype
+ *     (bf16 bit patterns or fp32), 16-byte aligned.  The caller owns them.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).  Every call
+ *     that launches work is asynchronous on that stream and never synchronises, except
+ *     kvc_last_error and kvc_destroy.  All calls on one handle must come from one host thread
+ *     at a time.
+ *   - Errors: a problem visible on the host (null pointer, bad layer index, unsupported
+ *     shape, CUDA launch failure) returns a nonzero status and launches nothing.  lens lives
+ *     on the device, so an out-of-range lens[b] is found by the kernels: they skip that row
+ *     (append writes nothing, attention writes a zero output row), never read or write out of
+ *     bounds, and set the handle's device error word, which kvc_last_error reports.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvc_cache* kvc_t;
+
+/* Cache element types. */
+#define KVC_BF16 0
+#define KVC_F32 1
+
+/* Status codes. */
+#define KVC_OK 0
+#define KVC_EINVAL 1       /* bad argument (null pointer, negative size, layer out of range) */
+#define KVC_ENOMEM 2       /* device allocation failed or would exceed free memory */
+#define KVC_ECUDA 3        /* a CUDA runtime call or kernel launch failed */
+#define KVC_ERANGE 4       /* a size is out of the supported range (T_in > T_max, B > 1024) */
+#define KVC_EDEVICE 5      /* a kernel found bad input on the device (see kvc_last_error) */
+#define KVC_EUNSUPPORTED 6 /* shape or device not supported (D, group size, not sm_103) */
+
+/* Bits of the device error word returned through kvc_last_error's `detail`. */
+#define KVC_DEV_BAD_LENS 1u     /* some lens[b] < 1 (or < 0 for prefill) or > T_max */
+#define KVC_DEV_WAIT_TIMEOUT 2u /* an in-kernel wait gave up (internal error; output invalid) */
+
+/* Create a cache of `layers` layers, each holding K and V of shape [B, H_kv, T_max, D].
+ * Supported: dtype KVC_BF16 with D in {64, 128, 256}; KVC_F32 with D in {4, 64, 128, 256};
+ * H_q % H_kv == 0 with H_q/H_kv in {1, 2, 4, 8, 16, 32}; 1 <= B <= 1024; T_max >= 1.
+ * The cache (kvc_bytes(h) bytes, one device allocation) is zero-filled, like a preallocated
+ * torch.zeros cache.  Workspace for split sequences and a device error word are allocated
+ * here too, so no later call allocates.  Uses the current CUDA device.
+ * Returns KVC_OK and *out, or an error status and *out = NULL. */
+int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype);
+
+/* Synchronise the device, free everything the handle owns.  NULL is a no-op. */
+int kvc_destroy(kvc_t h);
+
+/* Prefill write: copy K, V ([B, H_kv, T_in, D], device) slots [0, lens[b]) into the cache of
+ * `layer`.  Requires 1 <= T_in <= T_max; a lens[b] outside [0, T_in] skips row b and sets
+ * KVC_DEV_BAD_LENS.  Slots >= lens[b] are not touched. */
+int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in,
+                      const int32_t* lens, void* stream);
+
+/* Append: write k_new[b,h,:], v_new[b,h,:] ([B, H_kv, D], device) into slot lens[b]-1 of every
+ * KV head h of `layer`.  Every other slot keeps its exact bytes.  A lens[b] outside
+ * [1, T_max] skips row b and sets KVC_DEV_BAD_LENS. */
+int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const int32_t* lens,
+               void* stream);
+
+/* Decode attention over the cache of `layer`: q, out are [B, H_q, D] (device, cache dtype);
+ * out[b,j,:] as in the header comment, fp32 softmax and accumulation, rounded to the cache
+ * dtype (nearest-even for bf16).  Reads slots [0, lens[b]).  A lens[b] outside [1, T_max]
+ * gives a zero row and sets KVC_DEV_BAD_LENS.  Long sequences are split across CTAs
+ * (split-T) and their partial softmax states merged on the device. */
+int kvc_decode_attn(kvc_t h, int layer, const void* q, void* out, const int32_t* lens,
+                    void* stream);
+
+/* Fused decode step = kvc_append followed by kvc_decode_attn, in one launch: the new token's
+ * k/v are read from k_new/v_new for the attention and written to slot lens[b]-1 of the cache.
+ * Same results as the two calls in sequence. */
+int kvc_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                    void* out, const int32_t* lens, void* stream);
+
+/* Allocated payload of the handle: 2 * layers * H_kv * D * B * T_max * elem_bytes. */
+uint64_t kvc_bytes(kvc_t h);
+
+/* The closed form 2 * L * H_kv * D * (B * T) * elem_bytes (no allocation, host only).
+ * Returns 0 if any argument is negative or the product overflows 64 bits. */
+uint64_t kvc_bytes_formula(int64_t L, int64_t B, int64_t H_kv, int64_t D, int64_t T,
+                           int64_t elem_bytes);
+
+/* Ragged payload 2 * layers * H_kv * D * elem_bytes * sum_b lens_host[b] (lens in HOST memory,
+ * B entries). */
+uint64_t kvc_payload_bytes(kvc_t h, const int32_t* lens_host);
+
+/* Device pointers of layer `layer`'s K and V caches ([B, H_kv, T_max, D], owned by h). */
+int kvc_layer_ptrs(kvc_t h, int layer, void** K, void** V);
+
+/* Synchronise `stream`, read and clear the device error word.  Returns KVC_OK if it was zero,
+ * else KVC_EDEVICE with the KVC_DEV_* bits in *detail (detail may be NULL). */
+int kvc_last_error(kvc_t h, void* stream, uint32_t* detail);
+
+/* Number of CTAs the attention kernel splits the work over (0 restores the default: one per
+ * SM).  1 <= ctas <= 4 * SMs.  Changes only the split, never the result beyond rounding. */
+int kvc_set_ctas(kvc_t h, int ctas);
+int kvc_get_ctas(kvc_t h);
+
+/* How streams cut across CTAs are merged: -1 automatic (default), 0 by the last CTA to finish
+ * the stream (arrival counter; no CTA ever waits on another), 1 by a separate combine kernel
+ * launched right after on the same stream.  Changes nothing beyond rounding. */
+int kvc_set_combine_mode(kvc_t h, int mode);
+
+/* Shape query: writes layers, B, H_q, H_kv, D, T_max, dtype (any pointer may be NULL). */
+int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
+                  int* dtype);
+
+/* Split-T partition used by the attention kernel (host copy of the device arithmetic, for
+ * tests).  The B*H_kv (sequence, KV head) streams are laid end to end, stream u = b*H_kv + h
+ * holding lens[b] tokens; with W tokens in total, CTA i of P takes positions
+ * [floor(i*W/P), floor((i+1)*W/P)).  Returns the CTA that owns position x (0 <= x < W). */
+int kvc_plan_cta_of(int64_t x, int64_t W, int P);
+
+/* Human-readable name of a status code. */
+const char* kvc_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,86 @@
+// kvc_copy.cu -- cache writes (bit-exact byte moves) and the split-T combine launcher.
+//
+// append: the new token's k_t, v_t go to slot lens[b]-1 of every KV head, in place in the
+// preallocated cache ("第 1 周 · Day 4：KV Cache 与 MQA / GQA" §3.1; "KV 缓存" glossary page,
+// "两条数学等价的 decode 路径", path B).  The write costs 2*B*H_kv*D*s bytes whatever the
+// history length ("11.7 KV Cache：形状、显存与带宽" §1.1: constant-cost append).
+// prefill write: the prompt's T_p rows per (b, h) go to slots [0, lens[b]).
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+// One warp per (b, h) row pair; 16-byte vectors.
+__global__ void append_kernel(const CopyParams p) {
+    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.B * p.H_kv) return;
+    const int b = gw / p.H_kv, h = gw - b * p.H_kv;
+    const int L = p.lens[b];
+    if (L < 1 || L > p.T_max) {
+        if (h == 0 && lane == 0) atomicOr(p.err, DEV_BAD_LENS);
+        return;
+    }
+    const size_t dst = ((size_t)gw * p.T_max + (size_t)(L - 1)) * p.row_bytes;
+    const size_t src = (size_t)gw * p.row_bytes;
+    const int nvec = p.row_bytes >> 4;
+    for (int v = lane; v < nvec; v += 32) {
+        const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + src) + v);
+        const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + src) + v);
+        reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + dst)[v] = kx;
+        reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + dst)[v] = vx;
+    }
+}
+
+// Grid-stride over the 16-byte vectors of all [B, H_kv, T_in] source rows.
+__global__ void prefill_kernel(const CopyParams p) {
+    const int nvec = p.row_bytes >> 4;
+    const size_t rows = (size_t)p.B * p.H_kv * p.T_in;
+    const size_t total = rows * nvec;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / nvec;
+        const int v = (int)(i - row * nvec);
+        const size_t bh = row / p.T_in;
+        const int t = (int)(row - bh * p.T_in);
+        const int b = (int)(bh / p.H_kv);
+        const int L = p.lens[b];
+        if (L < 0 || L > p.T_in) {
+            if (t == 0 && v == 0 && bh % p.H_kv == 0) atomicOr(p.err, DEV_BAD_LENS);
+            continue;
+        }
+        if (t >= L) continue;
+        const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + row * p.row_bytes) + v);
+        const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + row * p.row_bytes) + v);
+        const size_t drow = bh * p.T_max + t;
+        reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + drow * p.row_bytes)[v] = kx;
+        reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + drow * p.row_bytes)[v] = vx;
+    }
+}
+
+int launch_append(const CopyParams& p, cudaStream_t s) {
+    const int warps = p.B * p.H_kv;
+    const int threads = 256;
+    const int blocks = (warps * 32 + threads - 1) / threads;
+    append_kernel<<<blocks, threads, 0, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+int launch_prefill(const CopyParams& p, cudaStream_t s) {
+    const size_t total = (size_t)p.B * p.H_kv * p.T_in * (p.row_bytes >> 4);
+    const int threads = 256;
+    size_t blocks = (total + threads - 1) / threads;
+    if (blocks > 65536) blocks = 65536;
+    if (blocks == 0) blocks = 1;
+    prefill_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
+    return (int)cudaGetLastError();
+}
+
+int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s) {
+    const int blocks = p.B * p.H_kv * G;
+    const int threads = D < 128 ? (D < 32 ? 32 : D) : 128;
+    if (dtype == 0) combine_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(p, D, G);
+    else combine_kernel<float><<<blocks, threads, 0, s>>>(p, D, G);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace kvc

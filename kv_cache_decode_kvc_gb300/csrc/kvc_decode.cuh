@@ -1,0 +1,659 @@
+// kvc_decode.cuh -- decode attention over a [B, H_kv, T_max, D] cache (CUDA cores, fp32 math).
+//
+// Computes, for every sequence b and query head j (KV head h = j / G):
+//     o[b,j,:] = softmax_t(q[b,j,:] . K[b,h,t,:] / sqrt(D)) V[b,h,t,:],   t < lens[b]
+// ("11.7 KV Cache：形状、显存与带宽" §2.2 single-step decode; head map from
+// "第 1 周 · Day 4：KV Cache 与 MQA / GQA" §3.4).  Decode reads every cached byte once and does
+// about G FLOP per byte, far below any tensor-core ridge (same pages, §1.5 / §1.1), so this
+// kernel is built around the HBM stream:
+//
+// * Work split (split-T): the B*H_kv (b, h) streams are laid end to end and cut into P equal
+//   contiguous ranges, one per CTA (cta_begin); a CTA may finish one stream and start the next.
+//   A stream cut across several CTAs leaves per-CTA partial softmax states (running max m,
+//   denominator l, unnormalised output) that are merged afterwards -- by the last CTA to finish
+//   that stream (an arrival counter, no waiting) or by a separate combine kernel.
+// * Data movement: K and V tiles of TT tokens are streamed by bulk (TMA engine) copies into an
+//   NST-deep shared-memory ring guarded by mbarriers; every (b, h) row is a contiguous run of
+//   lens[b]*D elements, so a tile is one copy per tensor.  There is no producer warp: the last
+//   warp to finish with a stage (a shared-memory arrival counter) issues the copy of the tile
+//   NST ahead into it.  The first tile of each stream segment also brings the group's q rows.
+//   Each K/V byte comes from HBM once and serves all G query heads of its group.
+// * Math: NW warps.  A token row is spread over LPT lanes (E elements each); the q.k partial
+//   dots of TPI tokens x HS heads are reduced with a transposing butterfly so each lane ends
+//   with one full score; the softmax is online with a lazily raised reference max (rescale only
+//   when a score exceeds it by TAU in log2 units); p is gathered back to the LPT lanes for the
+//   p.V accumulation.  Groups of more than 8 heads are split into slices served by separate
+//   warps reading the same shared tile.
+#pragma once
+
+#include <math.h>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+template <typename T, int D_, int G_>
+struct DecodeCfg {
+    static constexpr int D = D_;
+    static constexpr int G = G_;
+    static constexpr int ES = Elem<T>::BYTES;
+    static constexpr int VEC = Elem<T>::VEC;
+    static constexpr int ROWB = D * ES;
+    static constexpr int NVR = ROWB / 16;                   // 16-byte vectors per row
+    static constexpr int HS = G < 8 ? G : 8;                // heads per slice
+    static constexpr int NS = G / HS;                       // head slices
+    static constexpr int LPT_A = 2 * HS > 4 ? 2 * HS : 4;
+    static constexpr int LPT_B = (D * HS) / 64;             // keeps HS*E <= 64 registers
+    static constexpr int LPT_T = LPT_A > LPT_B ? LPT_A : LPT_B;
+    static constexpr int LPT_C = LPT_T > 32 ? 32 : LPT_T;
+    static constexpr int LPT = NVR < LPT_C ? NVR : LPT_C;   // lanes per token
+    static constexpr int NV = NVR / LPT;                    // vectors per lane per row
+    static constexpr int E = NV * VEC;                      // elements per lane per row
+    static constexpr int NGRP = 32 / LPT;                   // token groups per warp
+    static constexpr int TPI = LPT >= HS ? LPT / HS : 1;    // tokens per group per iteration
+    static constexpr int R = (TPI * HS) / LPT;              // scores per lane after reduction
+    static constexpr int TPW = NGRP * TPI;                  // tokens per warp iteration
+    static constexpr int NWT_MAX = 8 / NS;                  // token warps per slice (<= 8 warps)
+    // Tile: 16 KB of each tensor, grown up to 32 KB when that is what 8 warps need, and never
+    // smaller than one warp iteration.
+    static constexpr int TT_16K = 16384 / ROWB > 0 ? 16384 / ROWB : 1;
+    static constexpr int TT_32K = 32768 / ROWB > 0 ? 32768 / ROWB : 1;
+    static constexpr int TT_WANT = NWT_MAX * TPW;
+    static constexpr int TT_A = TT_WANT < TT_16K ? TT_16K : (TT_WANT < TT_32K ? TT_WANT : TT_32K);
+    static constexpr int TT_B = TT_A > 512 ? 512 : TT_A;
+    static constexpr int TT = TT_B < TPW ? TPW : TT_B;      // tokens per tile
+    static constexpr int NWT = TT / TPW < NWT_MAX ? TT / TPW : NWT_MAX;
+    static constexpr int NW = NS * NWT;                     // warps
+    static constexpr int NTHREADS = NW * 32;
+    static constexpr int ITERS = TT / (NWT * TPW);          // warp iterations per tile
+    // Lanes of a quarter warp that read different rows at the same column would hit the
+    // same banks (rows are multiples of 128 B); rotating the column order by group removes it.
+    static constexpr int ROT = (LPT < 8 && NVR >= 8) ? 8 / LPT : 1;
+    static constexpr int TILE_BYTES = TT * ROWB;
+    static constexpr int Q_BYTES = (G * ROWB + 127) / 128 * 128;  // the group's q rows
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + Q_BYTES;
+    static constexpr int MERGE_FLOATS = NW * HS * (D + 2);
+    static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
+    static constexpr int MISC_BYTES = 256;
+    static constexpr int BUDGET = 230400;
+    static constexpr int NST_A =
+        (BUDGET - MERGE_FLOATS * 4 - PREFIX_BYTES - MISC_BYTES) / STAGE_BYTES;
+    static constexpr int NST = NST_A > 8 ? 8 : NST_A;       // ring depth
+    static constexpr int SMEM = NST * STAGE_BYTES + MERGE_FLOATS * 4 + PREFIX_BYTES + MISC_BYTES;
+    static_assert(ROWB % 16 == 0, "rows must be whole 16-byte vectors");
+    static_assert(R == 1 || LPT == 1, "lane mapping");
+    static_assert(NST >= 2, "shared-memory ring too shallow");
+    static_assert(TT % (NWT * TPW) == 0, "tile must split evenly over warps");
+    static_assert(HS * E <= 64, "register budget");
+};
+
+constexpr float TAU = 8.0f;  // lazy-rescale threshold, log2 units (p <= 2^8 between rescales)
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+// Walks the (b, h) streams a CTA's range [r0, r1) touches, in order.
+struct SegIter {
+    const int64_t* prefix;  // prefix[b] = sum_{b' < b} L_b' (invalid lengths count as 0)
+    int B, H_kv;
+    int64_t r1;
+    int b, h, L;
+    int64_t ustart;  // position of token 0 of stream (b, h)
+    int t0, t1;      // this segment: tokens [t0, t1) of the stream
+    bool valid;
+
+    __device__ void init(const int64_t* pre, int B_, int H_kv_, int64_t r0, int64_t r1_) {
+        prefix = pre; B = B_; H_kv = H_kv_; r1 = r1_;
+        int lo = 0, hi = B - 1;  // largest b with H_kv * prefix[b] <= r0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)H_kv * prefix[mid] <= r0) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        L = (int)(prefix[b + 1] - prefix[b]);
+        h = (int)((r0 - (int64_t)H_kv * prefix[b]) / L);
+        ustart = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
+        t0 = (int)(r0 - ustart);
+        t1 = (int)((r1 < ustart + L ? r1 : ustart + L) - ustart);
+        valid = true;
+    }
+    __device__ void next() {
+        const int64_t pos = ustart + t1;
+        if (pos >= r1) { valid = false; return; }
+        if (++h == H_kv) {
+            h = 0;
+            do { ++b; } while (prefix[b + 1] == prefix[b]);  // skip empty sequences
+            L = (int)(prefix[b + 1] - prefix[b]);
+        }
+        ustart = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
+        t0 = 0;
+        t1 = (int)((r1 < ustart + L ? r1 : ustart + L) - ustart);
+    }
+};
+
+// Position in the CTA's tile sequence: segment + first token of the tile.
+template <int TT>
+struct TileCursor {
+    SegIter it;
+    int t;
+    bool valid;
+    __device__ void init(const int64_t* pre, int B, int H_kv, int64_t r0, int64_t r1) {
+        it.init(pre, B, H_kv, r0, r1);
+        t = it.t0;
+        valid = it.valid;
+    }
+    __device__ int n() const { return (it.t1 - t) < TT ? (it.t1 - t) : TT; }
+    __device__ bool first() const { return t == it.t0; }
+    __device__ bool last() const { return t + TT >= it.t1; }
+    __device__ void advance() {
+        t += TT;
+        if (t >= it.t1) {
+            it.next();
+            t = it.t0;
+            valid = it.valid;
+        }
+    }
+};
+
+// Transposing butterfly: N == LPT partial sums per lane in, lane `lig` of the group ends with
+// the full sum of value index `lig` in v[0].
+template <int N, int LPT>
+__device__ __forceinline__ void reduce_scatter(float (&v)[N], int lig) {
+#pragma unroll
+    for (int off = LPT / 2, n = N; off >= 1; off >>= 1, n >>= 1) {
+        const bool up = (lig & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL, send, off);
+        }
+    }
+}
+
+// Shared-memory vector index of register block i for a lane (see ROT).
+template <class C>
+__device__ __forceinline__ int vec_index(int i, int lig, int rot) {
+    return lig + C::LPT * ((i + rot) % C::NV);
+}
+
+// Issues the bulk copies of one tile into `stage` (one thread).  The last token of a stream in
+// the fused step comes from k_new / v_new instead of the cache; the first tile of a segment also
+// brings the group's G query rows.
+template <class C, int TT>
+__device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCursor<TT>& c,
+                                           unsigned char* ring, uint64_t* full_bar, int stage,
+                                           uint64_t pol) {
+    const int n = c.n();
+    const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
+    unsigned char* ks = ring + stage * C::STAGE_BYTES;
+    unsigned char* vs = ks + C::TILE_BYTES;
+    unsigned char* qs = vs + C::TILE_BYTES;
+    const bool with_q = c.first();
+    const bool last_here = p.k_new != nullptr && (c.t + n == c.it.L);
+    const int nc = last_here ? n - 1 : n;
+    uint32_t bytes = (uint32_t)(2 * n * C::ROWB);
+    if (with_q) bytes += C::G * C::ROWB;
+    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+    const char* Kg = static_cast<const char*>(p.K) + (unit * p.T_max + c.t) * C::ROWB;
+    const char* Vg = static_cast<const char*>(p.V) + (unit * p.T_max + c.t) * C::ROWB;
+    if (nc > 0) {
+        bulk_g2s(ks, Kg, nc * C::ROWB, &full_bar[stage], pol);
+        bulk_g2s(vs, Vg, nc * C::ROWB, &full_bar[stage], pol);
+    }
+    if (last_here) {
+        bulk_g2s(ks + nc * C::ROWB, static_cast<const char*>(p.k_new) + unit * C::ROWB, C::ROWB,
+                 &full_bar[stage], pol);
+        bulk_g2s(vs + nc * C::ROWB, static_cast<const char*>(p.v_new) + unit * C::ROWB, C::ROWB,
+                 &full_bar[stage], pol);
+    }
+    if (with_q)
+        bulk_g2s(qs, static_cast<const char*>(p.q) + unit * C::G * C::ROWB, C::G * C::ROWB,
+                 &full_bar[stage], pol);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
+    decode_kernel(const DecodeParams p) {
+    using C = DecodeCfg<T, D, G>;
+    constexpr int HS = C::HS, E = C::E, NV = C::NV, VEC = C::VEC, LPT = C::LPT, TPI = C::TPI;
+    constexpr int R = C::R, TT = C::TT, NW = C::NW, NWT = C::NWT, NST = C::NST;
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* ring = smem;
+    float* merge = reinterpret_cast<float*>(smem + NST * C::STAGE_BYTES);
+    int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(prefix + MAX_B + 1);
+    int* release_cnt = reinterpret_cast<int*>(full_bar + NST);   // [NST]
+    int* issued = release_cnt + NST;                                // [NST] tiles issued per stage
+    volatile int* abort_flag = issued + NST;
+    int* last_flag = issued + NST + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.B, H_kv = p.H_kv;
+    const size_t row_elems_q = (size_t)H_kv * G * D;  // one sequence of q / out
+
+    // ---- lengths -> stream prefix sums (warp 0); barriers (thread 32)
+    if (warp == 0) {
+        int64_t carry = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int64_t x = 0;
+            if (b < B) {
+                const int L = p.lens[b];
+                x = (L >= 1 && L <= p.T_max) ? L : 0;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(FULL, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < B) prefix[b + 1] = carry + x;
+            carry += __shfl_sync(FULL, x, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
+    if (tid == (NW > 1 ? 32 : 0)) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 1);
+            release_cnt[s] = 0;
+            issued[s] = 0;
+        }
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- rows with an invalid length: zero output, flag (one CTA per row)
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        if (prefix[b + 1] == prefix[b]) {
+            if (tid == 0) atomicOr(p.err, DEV_BAD_LENS);
+            for (size_t i = tid; i < row_elems_q; i += blockDim.x)
+                Elem<T>::store(p.out, (size_t)b * row_elems_q + i, 0.f);
+        }
+    }
+
+    const int64_t W = (int64_t)H_kv * prefix[B];
+    if (W == 0) return;
+    int64_t P = p.P;
+    {
+        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
+        if (want < P) P = want;
+    }
+    if ((int64_t)blockIdx.x >= P) return;
+    const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
+    if (r0 >= r1) return;
+    const bool fused = p.k_new != nullptr;
+    const uint64_t pol = policy_evict_first();
+
+    // ---- prime the ring: tiles 0 .. NST-1 (thread 0); every warp keeps the same prefetch cursor
+    TileCursor<TT> pref;
+    pref.init(prefix, B, H_kv, r0, r1);
+    for (int k = 0; k < NST && pref.valid; ++k) {
+        if (tid == 0) {
+            issue_tile<C, TT>(p, pref, ring, full_bar, k, pol);
+            issued[k] += 1;
+        }
+        pref.advance();
+    }
+
+    const int wt = warp % NWT;   // token warp within the head slice
+    const int sl = warp / NWT;   // head slice
+    const int grp = lane / LPT, lig = lane % LPT;
+    const int gbase = lane & ~(LPT - 1);
+    const int rot = (C::ROT > 1) ? (grp % C::ROT) : 0;
+
+    float q[HS][E];
+    float o[HS][E];
+    float m[R], l[R];
+
+    int stage = 0;
+    uint32_t phase = 0;
+    TileCursor<TT> cur;
+    cur.init(prefix, B, H_kv, r0, r1);
+    while (cur.valid) {
+        const size_t unit = (size_t)cur.it.b * H_kv + cur.it.h;
+        const int n = cur.n();
+        const bool ok = mbar_wait(&full_bar[stage], phase, abort_flag, p.err);
+        const T* Ks = reinterpret_cast<const T*>(ring + stage * C::STAGE_BYTES);
+        const T* Vs = Ks + TT * D;
+        if (cur.first()) {
+            // q rows of this slice from the stage, pre-scaled by log2(e)/sqrt(D)
+            const T* qs = Vs + TT * D + (size_t)sl * HS * D;
+#pragma unroll
+            for (int hh = 0; hh < HS; ++hh)
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        qs + (size_t)hh * D + vec_index<C>(i, lig, rot) * VEC);
+                    float f[VEC];
+                    Elem<T>::unpack(v, f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) q[hh][i * VEC + e] = f[e] * p.qscale;
+                }
+#pragma unroll
+            for (int hh = 0; hh < HS; ++hh)
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[hh][e] = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) { m[r] = -INFINITY; l[r] = 0.f; }
+        }
+        if (ok) {
+#pragma unroll 1
+            for (int itn = 0; itn < C::ITERS; ++itn) {
+                if ((itn * NWT + wt) * C::TPW >= n) break;
+                const int base = (itn * NWT + wt) * C::TPW + grp * TPI;
+                int tok[TPI];
+#pragma unroll
+                for (int k = 0; k < TPI; ++k) tok[k] = (base + k < n) ? base + k : 0;
+                // q . k partial dots
+                float acc[TPI * HS];
+#pragma unroll
+                for (int k = 0; k < TPI * HS; ++k) acc[k] = 0.f;
+#pragma unroll
+                for (int k = 0; k < TPI; ++k) {
+                    const T* kr = Ks + tok[k] * D;
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) {
+                        const uint4 v =
+                            *reinterpret_cast<const uint4*>(kr + vec_index<C>(i, lig, rot) * VEC);
+                        float f[VEC];
+                        Elem<T>::unpack(v, f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+#pragma unroll
+                            for (int hh = 0; hh < HS; ++hh)
+                                acc[k * HS + hh] = fmaf(q[hh][i * VEC + e], f[e], acc[k * HS + hh]);
+                    }
+                }
+                float s2[R];
+                if constexpr (LPT == 1) {
+                    const bool v0 = base < n;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) s2[r] = v0 ? acc[r] : -INFINITY;
+                } else {
+                    reduce_scatter<LPT, LPT>(acc, lig);
+                    s2[0] = (base + lig / HS) < n ? acc[0] : -INFINITY;
+                }
+                // online softmax with a lazily raised reference max
+                bool need = false;
+#pragma unroll
+                for (int r = 0; r < R; ++r) need |= s2[r] > m[r] + TAU;
+                if (__any_sync(FULL, need)) {
+                    float alpha[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        float mx = s2[r];
+#pragma unroll
+                        for (int off = HS; off < LPT; off <<= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+                        const float mn = fmaxf(m[r], mx);
+                        alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(m[r] - mn);
+                        m[r] = mn;
+                        l[r] *= alpha[r];
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < HS; ++hh) {
+                        float a;
+                        if constexpr (LPT == 1) a = alpha[hh];
+                        else a = __shfl_sync(FULL, alpha[0], gbase + hh);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) o[hh][e] *= a;
+                    }
+                }
+                float pr[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    pr[r] = (s2[r] == -INFINITY) ? 0.f : exp2f(s2[r] - m[r]);
+                    l[r] += pr[r];
+                }
+                float pk[TPI][HS];
+#pragma unroll
+                for (int k = 0; k < TPI; ++k)
+#pragma unroll
+                    for (int hh = 0; hh < HS; ++hh) {
+                        if constexpr (LPT == 1) pk[k][hh] = pr[hh];
+                        else pk[k][hh] = __shfl_sync(FULL, pr[0], gbase + k * HS + hh);
+                    }
+                // p . V
+#pragma unroll
+                for (int k = 0; k < TPI; ++k) {
+                    const T* vr = Vs + tok[k] * D;
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) {
+                        const uint4 v =
+                            *reinterpret_cast<const uint4*>(vr + vec_index<C>(i, lig, rot) * VEC);
+                        float f[VEC];
+                        Elem<T>::unpack(v, f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+#pragma unroll
+                            for (int hh = 0; hh < HS; ++hh)
+                                o[hh][i * VEC + e] = fmaf(pk[k][hh], f[e], o[hh][i * VEC + e]);
+                    }
+                }
+            }
+            // fused append: warp 0 stores the new token's rows (now in the tile) into the cache
+            if (fused && warp == 0 && cur.t + n == cur.it.L) {
+                const size_t dst = (unit * p.T_max + (size_t)(cur.it.L - 1)) * C::ROWB;
+                const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(Ks) + (n - 1) * C::ROWB;
+                const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(Vs) + (n - 1) * C::ROWB;
+                unsigned char* kd = static_cast<unsigned char*>(const_cast<void*>(p.K)) + dst;
+                unsigned char* vd = static_cast<unsigned char*>(const_cast<void*>(p.V)) + dst;
+                for (int v = lane; v < C::NVR; v += 32) {
+                    reinterpret_cast<uint4*>(kd)[v] = reinterpret_cast<const uint4*>(ksrc)[v];
+                    reinterpret_cast<uint4*>(vd)[v] = reinterpret_cast<const uint4*>(vsrc)[v];
+                }
+            }
+        }
+        // ---- release the stage; the last warp out refills it with the tile NST ahead
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&release_cnt[stage], 1) == NW - 1) {
+                release_cnt[stage] = 0;
+                if (pref.valid && !*abort_flag) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_tile<C, TT>(p, pref, ring, full_bar, stage, pol);
+                    issued[stage] += 1;
+                }
+            }
+        }
+        if (pref.valid) pref.advance();
+        if (++stage == NST) { stage = 0; phase ^= 1u; }
+
+        if (cur.last()) {
+            // ---- segment epilogue: merge groups (shuffles), then warps (shared memory)
+            float mh[HS], lh[HS];
+            if constexpr (LPT == 1) {
+#pragma unroll
+                for (int hh = 0; hh < HS; ++hh) { mh[hh] = m[hh]; lh[hh] = l[hh]; }
+            } else {
+                float lg = l[0];
+#pragma unroll
+                for (int off = HS; off < LPT; off <<= 1) lg += __shfl_xor_sync(FULL, lg, off);
+#pragma unroll
+                for (int hh = 0; hh < HS; ++hh) {
+                    mh[hh] = __shfl_sync(FULL, m[0], gbase + hh);
+                    lh[hh] = __shfl_sync(FULL, lg, gbase + hh);
+                }
+            }
+            if constexpr (C::ROT > 1) {  // undo the per-group column rotation
+#pragma unroll
+                for (int rr = 1; rr < C::ROT; ++rr) {
+                    if (rot == rr) {
+#pragma unroll
+                        for (int hh = 0; hh < HS; ++hh) {
+                            float tmp[E];
+#pragma unroll
+                            for (int i = 0; i < NV; ++i)
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e)
+                                    tmp[((i + rr) % NV) * VEC + e] = o[hh][i * VEC + e];
+#pragma unroll
+                            for (int e = 0; e < E; ++e) o[hh][e] = tmp[e];
+                        }
+                    }
+                }
+            }
+            if constexpr (C::NGRP > 1) {
+#pragma unroll
+                for (int hh = 0; hh < HS; ++hh) {
+                    float M = mh[hh];
+#pragma unroll
+                    for (int off = LPT; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+                    const float c = (mh[hh] == -INFINITY) ? 0.f : exp2f(mh[hh] - M);
+                    lh[hh] *= c;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[hh][e] *= c;
+#pragma unroll
+                    for (int off = LPT; off < 32; off <<= 1) {
+                        lh[hh] += __shfl_xor_sync(FULL, lh[hh], off);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) o[hh][e] += __shfl_xor_sync(FULL, o[hh][e], off);
+                    }
+                    mh[hh] = M;
+                }
+            }
+            float* mw = merge + warp * (HS * (D + 2));
+            if (grp == 0) {
+#pragma unroll
+                for (int hh = 0; hh < HS; ++hh)
+#pragma unroll
+                    for (int i = 0; i < NV; ++i)
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            mw[hh * (D + 2) + (lig + LPT * i) * VEC + e] = o[hh][i * VEC + e];
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int hh = 0; hh < HS; ++hh) {
+                    mw[hh * (D + 2) + D] = mh[hh];
+                    mw[hh * (D + 2) + D + 1] = lh[hh];
+                }
+            }
+            __syncthreads();
+
+            const bool whole = (cur.it.t0 == 0) && (cur.it.t1 == cur.it.L);
+            const int64_t us = cur.it.ustart;
+            const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + cur.it.L - 1, W, P);
+            const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
+            for (int idx = tid; idx < G * D; idx += NW * 32) {
+                const int hg = idx / D, d = idx - hg * D;
+                const int s_ = hg / HS, hh = hg - s_ * HS;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NWT; ++w)
+                    M = fmaxf(M, merge[(s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2) + D]);
+                float num = 0.f, den = 0.f;
+#pragma unroll
+                for (int w = 0; w < NWT; ++w) {
+                    const float* bw = merge + (s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2);
+                    const float c = (bw[D] == -INFINITY) ? 0.f : exp2f(bw[D] - M);
+                    num = fmaf(c, bw[d], num);
+                    den = fmaf(c, bw[D + 1], den);
+                }
+                if (whole) {
+                    Elem<T>::store(p.out, unit * G * D + idx, num / den);
+                } else {
+                    p.part_o[(size_t)slot * G * D + idx] = num;
+                    if (d == 0) {
+                        p.part_ml[((size_t)slot * G + hg) * 2] = M;
+                        p.part_ml[((size_t)slot * G + hg) * 2 + 1] = den;
+                    }
+                }
+            }
+            if (!whole && p.combine_mode == 0) {
+                __threadfence();
+                __syncthreads();
+                if (tid == 0) {
+                    const int prev = atomicAdd(&p.counters[unit], 1);
+                    *last_flag = (prev == (int)(clast - cfirst));
+                }
+                __syncthreads();
+                if (*last_flag) {
+                    __threadfence();
+                    for (int idx = tid; idx < G * D; idx += NW * 32) {
+                        const int hg = idx / D;
+                        float M = -INFINITY;
+                        for (int64_t c = cfirst; c <= clast; ++c)
+                            M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + unit) * G + hg) * 2]));
+                        float num = 0.f, den = 0.f;
+                        for (int64_t c = cfirst; c <= clast; ++c) {
+                            const size_t sidx = (size_t)(c + unit);
+                            const float mc = __ldcg(&p.part_ml[(sidx * G + hg) * 2]);
+                            const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+                            num = fmaf(w, __ldcg(&p.part_o[sidx * G * D + idx]), num);
+                            den = fmaf(w, __ldcg(&p.part_ml[(sidx * G + hg) * 2 + 1]), den);
+                        }
+                        Elem<T>::store(p.out, unit * G * D + idx, num / den);
+                    }
+                    if (tid == 0) p.counters[unit] = 0;  // every arrival is in: ready for next call
+                }
+            }
+            __syncthreads();  // merge buffer and flags are reused by the next segment
+        }
+        cur.advance();
+    }
+    if (*abort_flag) {
+        // A wait timed out (broken protocol): let every copy already issued land before the CTA
+        // exits, each wait bounded on its own.
+        __syncthreads();
+        if (tid == 0) {
+            for (int s = 0; s < NST; ++s) {
+                if (issued[s] == 0) continue;
+                const uint32_t par = (uint32_t)((issued[s] - 1) & 1);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&full_bar[s], par) && global_ns() - t0 < WAIT_LIMIT_NS) {
+                }
+            }
+        }
+    }
+}
+
+// Merges the partial states of streams cut across CTAs (combine_mode 1): one block per
+// (stream, query head of its group); threads over D.  Recomputes the same partition.
+template <typename T>
+__global__ void combine_kernel(const DecodeParams p, int D, int G) {
+    const int u = blockIdx.x / G, hg = blockIdx.x % G;
+    const int b = u / p.H_kv, h = u % p.H_kv;
+    __shared__ int64_t sh_sum[2];
+    if (threadIdx.x < 2) sh_sum[threadIdx.x] = 0;
+    __syncthreads();
+    int64_t before = 0, all = 0;
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        const int L = p.lens[i];
+        const int64_t v = (L >= 1 && L <= p.T_max) ? L : 0;
+        all += v;
+        if (i < b) before += v;
+    }
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[0]), (unsigned long long)before);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[1]), (unsigned long long)all);
+    __syncthreads();
+    const int Lb = p.lens[b];
+    if (Lb < 1 || Lb > p.T_max) return;
+    const int64_t W = (int64_t)p.H_kv * sh_sum[1];
+    int64_t P = p.P;
+    {
+        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
+        if (want < P) P = want;
+    }
+    const int64_t us = (int64_t)p.H_kv * sh_sum[0] + (int64_t)h * Lb;
+    const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + Lb - 1, W, P);
+    if (cfirst == clast) return;  // written directly by its CTA
+    float M = -INFINITY;
+    for (int64_t c = cfirst; c <= clast; ++c)
+        M = fmaxf(M, p.part_ml[((size_t)(c + u) * G + hg) * 2]);
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float num = 0.f, den = 0.f;
+        for (int64_t c = cfirst; c <= clast; ++c) {
+            const size_t sidx = (size_t)(c + u);
+            const float mc = p.part_ml[(sidx * G + hg) * 2];
+            const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+            num = fmaf(w, p.part_o[(sidx * G + hg) * D + d], num);
+            den = fmaf(w, p.part_ml[(sidx * G + hg) * 2 + 1], den);
+        }
+        Elem<T>::store(p.out, ((size_t)u * G + hg) * D + d, num / den);
+    }
+}
+
+}  // namespace kvc

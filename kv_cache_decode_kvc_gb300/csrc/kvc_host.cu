@@ -1,0 +1,314 @@
+// kvc_host.cu -- the C ABI of include/kvc.h: handle, allocation, argument checks, dispatch.
+//
+// Capacity: bytes = 2 * L * H_kv * D * (B * T) * s ("第 1 周 · Day 4：KV Cache 与 MQA / GQA"
+// §1.4; "KV 缓存" glossary page, 容量公式, ragged form with sum_i T_i).  The cache is one
+// preallocated, zero-filled device slab, written in place (same notes, §3.1).
+#include <math.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/kvc.h"
+#include "kvc_internal.cuh"
+
+struct kvc_cache {
+    int layers, B, H_q, H_kv, D, T_max, dtype, es, G;
+    int device, sms;
+    int ctas;          // 0 = one per SM
+    int combine_mode;  // -1 = automatic
+    int max_ctas;
+    char* slab;        // layer l: K at (2l) * layer_bytes, V at (2l+1) * layer_bytes
+    size_t layer_bytes;
+    float* part_o;
+    float* part_ml;
+    int* counters;
+    uint32_t* err;
+};
+
+namespace {
+
+bool d_supported(int dtype, int D) {
+    if (dtype == KVC_BF16) return D == 64 || D == 128 || D == 256;
+    if (dtype == KVC_F32) return D == 4 || D == 64 || D == 128 || D == 256;
+    return false;
+}
+
+bool g_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16 || G == 32; }
+
+// a * b with overflow detection (all operands >= 0)
+bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
+    if (a != 0 && b > UINT64_MAX / a) return false;
+    *r = a * b;
+    return true;
+}
+
+int launch_decode(const kvc_cache* h, const kvc::DecodeParams& p, cudaStream_t s) {
+    int smem = 0;
+    int e;
+    if (h->dtype == KVC_BF16) {
+        switch (h->D) {
+            case 64: e = kvc::launch_decode_bf16_d64(h->G, p, s, &smem); break;
+            case 128: e = kvc::launch_decode_bf16_d128(h->G, p, s, &smem); break;
+            case 256: e = kvc::launch_decode_bf16_d256(h->G, p, s, &smem); break;
+            default: return KVC_EUNSUPPORTED;
+        }
+    } else {
+        switch (h->D) {
+            case 4: e = kvc::launch_decode_f32_d4(h->G, p, s, &smem); break;
+            case 64: e = kvc::launch_decode_f32_d64(h->G, p, s, &smem); break;
+            case 128: e = kvc::launch_decode_f32_d128(h->G, p, s, &smem); break;
+            case 256: e = kvc::launch_decode_f32_d256(h->G, p, s, &smem); break;
+            default: return KVC_EUNSUPPORTED;
+        }
+    }
+    if (e != 0) return KVC_ECUDA;
+    if (p.combine_mode == 1) {
+        if (kvc::launch_combine(h->dtype, h->D, h->G, p, s) != 0) return KVC_ECUDA;
+    }
+    return KVC_OK;
+}
+
+int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new, void* out,
+                const int32_t* lens, void* stream) {
+    if (!h || !q || !out || !lens) return KVC_EINVAL;
+    if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    if ((k_new == nullptr) != (v_new == nullptr)) return KVC_EINVAL;
+    kvc::DecodeParams p;
+    p.K = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.V = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.q = q;
+    p.out = out;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.lens = lens;
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.counters = h->counters;
+    p.err = h->err;
+    p.B = h->B;
+    p.H_kv = h->H_kv;
+    p.T_max = h->T_max;
+    p.P = h->ctas > 0 ? h->ctas : h->sms;
+    p.min_tokens = h->ctas > 0 ? 1 : 256;
+    const int U = h->B * h->H_kv;
+    int mode = h->combine_mode;
+    if (mode < 0) {
+        // Merge cost of the last-arriving CTA grows with the segments per stream times the
+        // group's outputs; when streams are few and long, hand the merge to a wide kernel.
+        const long long nseg = (p.P + U - 1) / U + 1;
+        mode = (nseg * h->G * h->D * 4 > 65536) ? 1 : 0;
+    }
+    p.combine_mode = mode;
+    p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
+    return launch_decode(h, p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvc_status_str(int status) {
+    switch (status) {
+        case KVC_OK: return "ok";
+        case KVC_EINVAL: return "invalid argument";
+        case KVC_ENOMEM: return "out of device memory";
+        case KVC_ECUDA: return "CUDA error";
+        case KVC_ERANGE: return "size out of range";
+        case KVC_EDEVICE: return "device-side check failed";
+        case KVC_EUNSUPPORTED: return "unsupported shape or device";
+        default: return "unknown status";
+    }
+}
+
+uint64_t kvc_bytes_formula(int64_t L, int64_t B, int64_t H_kv, int64_t D, int64_t T,
+                           int64_t elem_bytes) {
+    if (L < 0 || B < 0 || H_kv < 0 || D < 0 || T < 0 || elem_bytes < 0) return 0;
+    uint64_t r = 2;
+    const int64_t f[6] = {L, H_kv, D, B, T, elem_bytes};
+    for (int i = 0; i < 6; ++i)
+        if (!mul_ok(r, (uint64_t)f[i], &r)) return 0;
+    return r;
+}
+
+int kvc_plan_cta_of(int64_t x, int64_t W, int P) {
+    if (W <= 0 || P <= 0 || x < 0 || x >= W) return -1;
+    return (int)kvc::cta_of(x, W, P);
+}
+
+int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
+    if (!out) return KVC_EINVAL;
+    *out = nullptr;
+    if (layers < 1 || B < 1 || H_q < 1 || H_kv < 1 || D < 1 || T_max < 1) return KVC_EINVAL;
+    if (dtype != KVC_BF16 && dtype != KVC_F32) return KVC_EINVAL;
+    if (H_q % H_kv != 0) return KVC_EINVAL;
+    if (B > kvc::MAX_B) return KVC_ERANGE;
+    const int G = H_q / H_kv;
+    if (!g_supported(G) || !d_supported(dtype, D)) return KVC_EUNSUPPORTED;
+    const int es = dtype == KVC_BF16 ? 2 : 4;
+    // partition positions: B * H_kv * T_max < 2^50
+    if ((double)B * H_kv * (double)T_max >= 1125899906842624.0) return KVC_ERANGE;
+    const uint64_t total = kvc_bytes_formula(layers, B, H_kv, D, T_max, es);
+    if (total == 0) return KVC_ERANGE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ECUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return KVC_ECUDA;
+    if (!(prop.major == 10 && prop.minor == 3)) return KVC_EUNSUPPORTED;  // built for sm_103a
+
+    kvc_cache* h = new (std::nothrow) kvc_cache();
+    if (!h) return KVC_ENOMEM;
+    h->layers = layers; h->B = B; h->H_q = H_q; h->H_kv = H_kv; h->D = D; h->T_max = T_max;
+    h->dtype = dtype; h->es = es; h->G = G; h->device = dev;
+    h->sms = prop.multiProcessorCount;
+    h->ctas = 0;
+    h->combine_mode = -1;
+    h->max_ctas = 4 * h->sms;
+    h->layer_bytes = (size_t)B * H_kv * (size_t)T_max * D * es;
+
+    const size_t U = (size_t)B * H_kv;
+    const size_t slots = (size_t)h->max_ctas + U;
+    const size_t ws_bytes = slots * G * (size_t)D * 4 + slots * G * 2 * 4 + U * 4 + 256;
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) { delete h; return KVC_ECUDA; }
+    if (total + ws_bytes > free_b) { delete h; return KVC_ENOMEM; }
+
+    if (cudaMalloc(&h->slab, total) != cudaSuccess) { cudaGetLastError(); delete h; return KVC_ENOMEM; }
+    char* ws = nullptr;
+    if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->slab);
+        delete h;
+        return KVC_ENOMEM;
+    }
+    h->part_o = reinterpret_cast<float*>(ws);
+    h->part_ml = h->part_o + slots * G * D;
+    h->counters = reinterpret_cast<int*>(h->part_ml + slots * G * 2);
+    h->err = reinterpret_cast<uint32_t*>(h->counters + U);
+    if (cudaMemset(h->slab, 0, total) != cudaSuccess || cudaMemset(ws, 0, ws_bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(ws);
+        cudaFree(h->slab);
+        delete h;
+        return KVC_ECUDA;
+    }
+    *out = h;
+    return KVC_OK;
+}
+
+int kvc_destroy(kvc_t h) {
+    if (!h) return KVC_OK;
+    int rc = KVC_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) rc = KVC_ECUDA;
+    cudaFree(h->part_o);  // workspace base
+    cudaFree(h->slab);
+    delete h;
+    return rc;
+}
+
+uint64_t kvc_bytes(kvc_t h) {
+    if (!h) return 0;
+    return kvc_bytes_formula(h->layers, h->B, h->H_kv, h->D, h->T_max, h->es);
+}
+
+uint64_t kvc_payload_bytes(kvc_t h, const int32_t* lens_host) {
+    if (!h || !lens_host) return 0;
+    uint64_t sum = 0;
+    for (int b = 0; b < h->B; ++b) sum += (uint64_t)(lens_host[b] > 0 ? lens_host[b] : 0);
+    return 2ull * h->layers * h->H_kv * h->D * h->es * sum;
+}
+
+int kvc_layer_ptrs(kvc_t h, int layer, void** K, void** V) {
+    if (!h || layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    if (K) *K = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    if (V) *V = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    return KVC_OK;
+}
+
+int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
+                  int* dtype) {
+    if (!h) return KVC_EINVAL;
+    if (layers) *layers = h->layers;
+    if (B) *B = h->B;
+    if (H_q) *H_q = h->H_q;
+    if (H_kv) *H_kv = h->H_kv;
+    if (D) *D = h->D;
+    if (T_max) *T_max = h->T_max;
+    if (dtype) *dtype = h->dtype;
+    return KVC_OK;
+}
+
+int kvc_set_ctas(kvc_t h, int ctas) {
+    if (!h || ctas < 0 || ctas > h->max_ctas) return KVC_EINVAL;
+    h->ctas = ctas;
+    return KVC_OK;
+}
+
+int kvc_get_ctas(kvc_t h) {
+    if (!h) return -1;
+    return h->ctas > 0 ? h->ctas : h->sms;
+}
+
+int kvc_set_combine_mode(kvc_t h, int mode) {
+    if (!h || mode < -1 || mode > 1) return KVC_EINVAL;
+    h->combine_mode = mode;
+    return KVC_OK;
+}
+
+int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in,
+                      const int32_t* lens, void* stream) {
+    if (!h || !K || !V || !lens) return KVC_EINVAL;
+    if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    if (T_in < 1 || T_in > h->T_max) return KVC_ERANGE;
+    kvc::CopyParams p;
+    p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.K = K;
+    p.V = V;
+    p.lens = lens;
+    p.err = h->err;
+    p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = T_in;
+    p.row_bytes = h->D * h->es;
+    return kvc::launch_prefill(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
+}
+
+int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const int32_t* lens,
+               void* stream) {
+    if (!h || !k_new || !v_new || !lens) return KVC_EINVAL;
+    if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    kvc::CopyParams p;
+    p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.K = k_new;
+    p.V = v_new;
+    p.lens = lens;
+    p.err = h->err;
+    p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = 1;
+    p.row_bytes = h->D * h->es;
+    return kvc::launch_append(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
+}
+
+int kvc_decode_attn(kvc_t h, int layer, const void* q, void* out, const int32_t* lens,
+                    void* stream) {
+    return attn_common(h, layer, q, nullptr, nullptr, out, lens, stream);
+}
+
+int kvc_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                    void* out, const int32_t* lens, void* stream) {
+    if (!k_new || !v_new) return KVC_EINVAL;
+    return attn_common(h, layer, q, k_new, v_new, out, lens, stream);
+}
+
+int kvc_last_error(kvc_t h, void* stream, uint32_t* detail) {
+    if (!h) return KVC_EINVAL;
+    if (detail) *detail = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ECUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, h->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return KVC_ECUDA;
+    if (v == 0) return KVC_OK;
+    if (cudaMemset(h->err, 0, sizeof v) != cudaSuccess) return KVC_ECUDA;
+    if (detail) *detail = v;
+    return KVC_EDEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,193 @@
+// kvc_internal.cuh -- device helpers and launch plumbing shared by the CUDA translation units
+// of libkvc (never by the CPU oracle).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvc {
+
+constexpr uint32_t DEV_BAD_LENS = 1u;      // mirrors KVC_DEV_BAD_LENS
+constexpr uint32_t DEV_WAIT_TIMEOUT = 2u;  // mirrors KVC_DEV_WAIT_TIMEOUT
+constexpr int MAX_B = 1024;
+// An in-kernel wait that has not completed after this long gives up, flags
+// DEV_WAIT_TIMEOUT and lets the kernel run to its end (no hang, output marked invalid).
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+// ------------------------------------------------------------------ split-T partition
+// The B*H_kv (sequence b, KV head h) streams are laid end to end, stream u = b*H_kv + h
+// holding L_b tokens; W = H_kv * sum_b L_b.  CTA i of P owns positions
+// [cta_begin(i), cta_begin(i+1)).  W < 2^50 and P <= 2^12 keep every product below 2^63.
+__host__ __device__ inline int64_t cta_begin(int64_t i, int64_t W, int64_t P) {
+    return (i * W) / P;
+}
+// CTA owning position x: the largest i with cta_begin(i) <= x.
+__host__ __device__ inline int64_t cta_of(int64_t x, int64_t W, int64_t P) {
+    return ((x + 1) * P - 1) / W;
+}
+
+// ------------------------------------------------------------------ launch parameters
+struct DecodeParams {
+    const void* K;        // layer base, [B, H_kv, T_max, D]
+    const void* V;
+    const void* q;        // [B, H_q, D]
+    void* out;            // [B, H_q, D]
+    const void* k_new;    // [B, H_kv, D] for the fused append, else nullptr
+    const void* v_new;
+    const int32_t* lens;  // [B], valid length after this step's append
+    float* part_o;        // [slots][G][D] unnormalised partial outputs of split streams
+    float* part_ml;       // [slots][G][2] (running max in log2 units, denominator)
+    int* counters;        // [B*H_kv] arrivals per split stream (all zero between calls)
+    uint32_t* err;        // device error word
+    int B, H_kv, T_max;
+    int P;                // CTAs of the partition (grid size)
+    int min_tokens;       // fewer CTAs when W / P would drop below this (1 = never)
+    int combine_mode;     // 0: the last CTA of a split stream merges it; 1: combine kernel
+    float qscale;         // log2(e) / sqrt(D), folded into q
+};
+
+struct CopyParams {
+    void* Kc;             // layer base of the cache
+    void* Vc;
+    const void* K;        // source: [B, H_kv, T_in, D] (prefill) or [B, H_kv, D] (append)
+    const void* V;
+    const int32_t* lens;
+    uint32_t* err;
+    int B, H_kv, T_max, T_in;
+    int row_bytes;        // D * element bytes (a multiple of 16)
+};
+
+// One launcher per (dtype, D) translation unit; G selects the instantiation.  Each returns
+// a cudaError_t (0 = launched) and writes the kernel's dynamic shared memory to *smem_out.
+#define KVC_DECLARE_LAUNCHER(NAME) \
+    int NAME(int G, const DecodeParams& p, cudaStream_t s, int* smem_out);
+KVC_DECLARE_LAUNCHER(launch_decode_bf16_d64)
+KVC_DECLARE_LAUNCHER(launch_decode_bf16_d128)
+KVC_DECLARE_LAUNCHER(launch_decode_bf16_d256)
+KVC_DECLARE_LAUNCHER(launch_decode_f32_d4)
+KVC_DECLARE_LAUNCHER(launch_decode_f32_d64)
+KVC_DECLARE_LAUNCHER(launch_decode_f32_d128)
+KVC_DECLARE_LAUNCHER(launch_decode_f32_d256)
+int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s);
+int launch_append(const CopyParams& p, cudaStream_t s);
+int launch_prefill(const CopyParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------------ device primitives
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most WAIT_LIMIT_NS.  On
+// timeout (or once another thread of the CTA has timed out) it returns false, having set the
+// CTA's abort flag and the device error word; callers then skip work but keep the protocol.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (*abort_flag) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicOr(err, DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// One bulk (TMA engine) copy global -> shared, completing `bytes` on the mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.  The L2 policy marks the stream as
+// evict-first: every KV byte is read once per step.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+        "%2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// bf16 pair (one 32-bit word) -> two floats, exact.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int BYTES = 2;
+    static constexpr int VEC = 8;  // elements per 16-byte vector
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[8]) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+        f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    }
+    __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
+        reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(x);
+    }
+};
+template <>
+struct Elem<float> {
+    static constexpr int BYTES = 4;
+    static constexpr int VEC = 4;
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
+        reinterpret_cast<float*>(base)[idx] = x;
+    }
+};
+#endif  // __CUDACC__
+
+}  // namespace kvc

@@ -1,0 +1,106 @@
+"""The decode workloads the pages describe, as shapes (no arithmetic).
+
+T is the number of tokens already cached before the step; the step appends one more, so
+every sequence attends over L_b = T_b + 1 slots and T_max = max_b L_b.  Values are bf16
+draws of the counter-based generator in :mod:`synth` (the pages name no dataset).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import synth
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    layers: int
+    B: int
+    H_q: int
+    H_kv: int
+    D: int
+    T: int | None          # uniform cached length, or None for the ragged range below
+    T_lo: int = 0
+    T_hi: int = 0
+    dtype: str = "bf16"
+    seed: int = 1234
+    note: str = ""
+
+    @property
+    def G(self) -> int:
+        return self.H_q // self.H_kv
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def lens_pre(self) -> torch.Tensor:
+        """Cached length of each sequence before the step (int32, CPU)."""
+        if self.T is not None:
+            return torch.full((self.B,), self.T, dtype=torch.int32)
+        return synth.uniform_lens(self.seed, self.B, self.T_lo, self.T_hi)
+
+    def lens(self) -> torch.Tensor:
+        return self.lens_pre() + 1
+
+    def T_max(self) -> int:
+        return int(self.lens().max())
+
+    def kv_read_bytes_per_layer(self) -> int:
+        """Algorithmic KV bytes one decode step reads per layer: 2 H_kv D s sum_b L_b."""
+        return 2 * self.H_kv * self.D * self.elem_bytes * int(self.lens().sum())
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("llama2_7b_mha_b1_t4096", 32, 1, 32, 32, 128, 4096,
+                 note="Llama-2-7B-shaped MHA, every sequence at 4096 cached tokens"),
+        Workload("gqa8b_b24_ragged3000_6000", 32, 24, 32, 8, 128, None, 3000, 6000,
+                 note="8B-shaped GQA serving batch, cached lengths U{3000..6000} (seed 1234)"),
+        Workload("gqa70b_b32_t8192", 80, 32, 64, 8, 128, 8192,
+                 note="70B-shaped GQA long context (80 GiB cache)"),
+        Workload("mqa_b64_t4096", 1, 64, 32, 1, 128, 4096, note="MQA, one layer"),
+        Workload("mqa_b1_t131072", 1, 1, 32, 1, 128, 131072, note="MQA long context, split-T stress"),
+    ]
+}
+
+HEADLINE = "gqa8b_b24_ragged3000_6000"
+
+
+def fill_layer(cache, layer: int, w: Workload, seed: int | None = None, device="cuda",
+               chunk_elems: int = 1 << 26):
+    """Write the layer's seeded history (slots [0, T_b)) through kvc_prefill_write."""
+    seed = w.seed if seed is None else seed
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    lp = w.lens_pre()
+    T_in = int(lp.max())
+    per_b = w.H_kv * T_in * w.D
+    step = max(1, chunk_elems // per_b)
+    K = torch.empty(w.B, w.H_kv, T_in, w.D, dtype=dt, device=device)
+    V = torch.empty_like(K)
+    for b0 in range(0, w.B, step):
+        b1 = min(w.B, b0 + step)
+        K[b0:b1] = synth.block(seed, layer, "K", b0, b1, w.H_kv, 0, T_in, w.D, w.B, dt, device)
+        V[b0:b1] = synth.block(seed, layer, "V", b0, b1, w.H_kv, 0, T_in, w.D, w.B, dt, device)
+    cache.prefill_write(layer, K, V, lp.to(device))
+    del K, V
+
+
+def step_inputs(w: Workload, layer: int, seed: int | None = None, device="cuda"):
+    """q [B,H_q,D], k_new / v_new [B,H_kv,D] (the generator's row T_b of each stream)."""
+    seed = w.seed if seed is None else seed
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    lp = w.lens_pre()
+    q = synth.queries(seed, layer, w.B, w.H_q, w.D, dt, device)
+    # row T_b of stream (b, h): gather with one generator call per distinct length
+    kn = torch.empty(w.B, w.H_kv, w.D, dtype=dt, device=device)
+    vn = torch.empty_like(kn)
+    for T_b in sorted(set(lp.tolist())):
+        idx = [b for b in range(w.B) if int(lp[b]) == T_b]
+        for b in idx:
+            kn[b] = synth.block(seed, layer, "K", b, b + 1, w.H_kv, T_b, T_b + 1, w.D, w.B, dt, device)[0, :, 0]
+            vn[b] = synth.block(seed, layer, "V", b, b + 1, w.H_kv, T_b, T_b + 1, w.D, w.B, dt, device)[0, :, 0]
+    return q, kn, vn

@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Sizes here span several tiles and ragged tails; test_gpu_configs.py runs the full-size
+workloads on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_decode_kvc_gb300 import kvc, synth
+
+from gpu_util import Case, check_close, host_bits
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [("bf16", 64), ("bf16", 128), ("bf16", 256), ("f32", 4), ("f32", 64), ("f32", 128), ("f32", 256)]
+GROUPS = [1, 2, 4, 8, 16, 32]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.init()
+
+
+def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0):
+    c = kvc.KVCache(layers, case.B, case.H_q, case.H_kv, case.D, T_max,
+                    "bf16" if case.dtype == torch.bfloat16 else "f32")
+    try:
+        if ctas:
+            c.set_ctas(ctas)
+        c.set_combine_mode(mode)
+        d = case.to_device()
+        out = torch.full((case.B, case.H_q, case.D), float("nan"), dtype=case.dtype, device="cuda")
+        c.prefill_write(layer, d["K"], d["V"], d["lens_pre"])
+        if fused:
+            c.decode_step(layer, d["q"], d["k_new"], d["v_new"], out, d["lens"])
+        else:
+            c.append(layer, d["k_new"], d["v_new"], d["lens"])
+            c.decode_attn(layer, d["q"], out, d["lens"])
+        st, detail = c.last_error()
+        assert st == kvc.KVC_OK, (st, detail)
+        Kv, Vv = c.layer_views(layer)
+        return out, Kv.cpu(), Vv.cpu()
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("dtype,D", SHAPES)
+@pytest.mark.parametrize("G", GROUPS)
+def test_decode_matches_oracle(dtype, D, G):
+    H_kv = 2
+    case = Case(100 + G + D, 3, G * H_kv, H_kv, D, [0, 37, 611], dtype)
+    T_max = 640
+    out, _, _ = _run(case, T_max)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"{dtype} D={D} G={G}")
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_append_is_bit_exact_and_leaves_other_slots(fused):
+    case = Case(7, 4, 8, 2, 128, [5, 0, 63, 64], "bf16")
+    T_max = 80
+    _, Kg, Vg = _run(case, T_max, fused=fused)
+    Kc, Vc = case.oracle_cache(T_max)
+    assert np.array_equal(host_bits(Kg), Kc)
+    assert np.array_equal(host_bits(Vg), Vc)
+
+
+def test_worked_example_through_the_cache():
+    """The glossary page's example: one GQA layer (hidden 16, H_q 4, H_kv 2, D 4, fp32, seed 7),
+    prefill 8 tokens, decode 5; each cached step matches full causal recomputation within the
+    page's tolerance, the attention matches the oracle within 1e-5, and the final cache has
+    shape [1, 2, 13, 4]."""
+    B, hidden, H_q, H_kv, D, T_p, T = 1, 16, 4, 2, 4, 8, 13
+    Ws, x = synth.worked_example(7, hidden, H_q, H_kv, D, B, T)
+    WQ, WK, WV, WO = Ws
+    # projections are the harness's job (fp32, CPU): q, k, v for every position
+    q_all = (x @ WQ).view(B, T, H_q, D).transpose(1, 2).contiguous()   # [B,H_q,T,D]
+    k_all = (x @ WK).view(B, T, H_kv, D).transpose(1, 2).contiguous()  # [B,H_kv,T,D]
+    v_all = (x @ WV).view(B, T, H_kv, D).transpose(1, 2).contiguous()
+    full_outs = []
+    for step in range(T - T_p):
+        full, _, _ = oracle.layer_full(x[:, : T_p + step + 1].numpy(), *[w.numpy() for w in Ws], H_q, H_kv, D)
+        full_outs.append(full[:, -1])
+    c = kvc.KVCache(1, B, H_q, H_kv, D, T, "f32")
+    try:
+        lens_pre = torch.tensor([T_p], dtype=torch.int32)
+        c.prefill_write(0, k_all[:, :, :T_p].cuda(), v_all[:, :, :T_p].cuda(), lens_pre.cuda())
+        Kc = np.zeros((B, H_kv, T, D), np.float32)
+        Vc = np.zeros_like(Kc)
+        oracle.prefill_write(Kc, Vc, k_all[:, :, :T_p].contiguous().numpy(), v_all[:, :, :T_p].contiguous().numpy(), lens_pre.numpy())
+        for step in range(T - T_p):
+            pos = T_p + step
+            lens = torch.tensor([pos + 1], dtype=torch.int32)
+            qt = q_all[:, :, pos].contiguous()
+            kt = k_all[:, :, pos].contiguous()
+            vt = v_all[:, :, pos].contiguous()
+            out = torch.empty(B, H_q, D, device="cuda")
+            c.decode_step(0, qt.cuda(), kt.cuda(), vt.cuda(), out, lens.cuda())
+            oracle.append(Kc, Vc, kt.numpy(), vt.numpy(), lens.numpy())
+            ref = oracle.decode_attn(qt.numpy(), Kc, Vc, lens.numpy())
+            check_close(out, ref, torch.float32, f"worked example step {step}")
+            y = out.cpu().reshape(B, 1, H_q * D) @ WO  # the harness's output projection
+            np.testing.assert_allclose(y[:, 0].numpy(), full_outs[step], rtol=1e-4, atol=1e-5)
+        Kv, Vv = c.layer_views(0)
+        assert tuple(Kv.shape) == tuple(Vv.shape) == (1, 2, 13, 4)
+        assert np.array_equal(Kv.cpu().numpy(), Kc)
+        assert c.last_error() == (kvc.KVC_OK, 0)
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 152, 600])
+def test_split_t_any_split_matches(ctas, mode):
+    # one long and one 1-token stream per KV head; every split count and both merge paths
+    case = Case(55, 2, 8, 2, 128, [1500, 0], "bf16")
+    T_max = 1600
+    out, _, _ = _run(case, T_max, ctas=ctas, mode=mode)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"ctas={ctas} mode={mode}")
+
+
+@pytest.mark.parametrize("ctas", [1, 5, 64])
+def test_split_t_fp32_is_tight(ctas):
+    case = Case(56, 3, 32, 1, 128, [2000, 17, 900], "f32")
+    T_max = 2048
+    out, _, _ = _run(case, T_max, ctas=ctas, mode=0)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"fp32 MQA ctas={ctas}")
+
+
+def test_maximum_length_and_single_token():
+    case = Case(57, 2, 4, 1, 128, [255, 0], "bf16")  # lens = [T_max, 1]
+    out, _, _ = _run(case, 256)
+    check_close(out, case.oracle_out(256), case.dtype, "T_max edge")
+    # a 1-token history returns v_new exactly (softmax of one score is 1)
+    assert torch.equal(out[1].cpu(), case.v_new[1, 0].expand(4, 128))
+
+
+def test_invalid_lengths_flag_and_zero_rows():
+    B, H_q, H_kv, D, T_max = 4, 8, 2, 128, 64
+    case = Case(58, B, H_q, H_kv, D, [10, 20, 30, 40], "bf16")
+    c = kvc.KVCache(1, B, H_q, H_kv, D, T_max, "bf16")
+    try:
+        d = case.to_device()
+        c.prefill_write(0, d["K"], d["V"], d["lens_pre"])
+        bad = torch.tensor([11, 0, 31, T_max + 5], dtype=torch.int32, device="cuda")
+        out = torch.full((B, H_q, D), 7.0, dtype=torch.bfloat16, device="cuda")
+        c.decode_step(0, d["q"], d["k_new"], d["v_new"], out, bad)
+        st, detail = c.last_error()
+        assert st == kvc.KVC_EDEVICE and detail & kvc.KVC_DEV_BAD_LENS
+        assert c.last_error() == (kvc.KVC_OK, 0)  # cleared
+        assert not out[1].float().abs().sum() and not out[3].float().abs().sum()
+        ref = case.oracle_out(T_max)
+        check_close(out[[0, 2]], ref[[0, 2]], torch.bfloat16, "valid rows beside invalid ones")
+        # the invalid rows appended nothing
+        Kv, _ = c.layer_views(0)
+        Kc, _ = case.oracle_cache(T_max)
+        assert np.array_equal(host_bits(Kv[[0, 2]].cpu()), Kc[[0, 2]])
+        assert not Kv[1, :, 20].float().abs().sum()  # slot lens_pre[1] untouched (was never written)
+    finally:
+        c.close()
+
+
+def test_repeated_steps_reuse_workspace():
+    # the arrival counters must be back at zero after every call
+    case = Case(59, 2, 16, 2, 128, [3000, 2999], "bf16")
+    T_max = 3001
+    c = kvc.KVCache(1, 2, 16, 2, 128, T_max, "bf16")
+    try:
+        c.set_combine_mode(0)
+        d = case.to_device()
+        c.prefill_write(0, d["K"], d["V"], d["lens_pre"])
+        ref = case.oracle_out(T_max)
+        for _ in range(5):
+            out = torch.empty(2, 16, 128, dtype=torch.bfloat16, device="cuda")
+            c.decode_step(0, d["q"], d["k_new"], d["v_new"], out, d["lens"])
+            check_close(out, ref, torch.bfloat16, "repeat")
+        assert c.last_error() == (kvc.KVC_OK, 0)
+    finally:
+        c.close()
+
+
+def test_generator_is_device_independent():
+    a = synth.block(3, 5, "V", 2, 6, 4, 100, 357, 128, 8, torch.bfloat16, "cpu")
+    b = synth.block(3, 5, "V", 2, 6, 4, 100, 357, 128, 8, torch.bfloat16, "cuda")
+    assert torch.equal(a, b.cpu())
