@@ -262,12 +262,14 @@ def run_ours(args, w):
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed_region")
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for _ in range(args.steps):
             run()
         ev1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier()
     clock_info = clocks.stop()
     ms_local = ev0.elapsed_time(ev1) / args.steps
@@ -402,11 +404,16 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only this many layers of the workload (profiling of small cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=min(args.layers, w.layers))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -302,8 +302,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
     const int gbase = lane & ~(LPT - 1);
     const int rot = (C::ROT > 1) ? (grp % C::ROT) : 0;
 
-    float q[HS][E];
-    float o[HS][E];
+    constexpr int PV = VEC / 2;  // fp32 pairs per 16-byte vector
+    constexpr int E2 = E / 2;    // fp32 pairs per lane per row
+    float2 q2[HS][E2];           // q, pre-scaled, as pairs of consecutive elements
+    float2 o2[HS][E2];           // unnormalised output accumulators
     float m[R], l[R];
 
     int stage = 0;
@@ -319,21 +321,22 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
         if (cur.first()) {
             // q rows of this slice from the stage, pre-scaled by log2(e)/sqrt(D)
             const T* qs = Vs + TT * D + (size_t)sl * HS * D;
+            const float2 sc = make_float2(p.qscale, p.qscale);
 #pragma unroll
             for (int hh = 0; hh < HS; ++hh)
 #pragma unroll
                 for (int i = 0; i < NV; ++i) {
                     const uint4 v = *reinterpret_cast<const uint4*>(
                         qs + (size_t)hh * D + vec_index<C>(i, lig, rot) * VEC);
-                    float f[VEC];
-                    Elem<T>::unpack(v, f);
+                    float2 f[PV];
+                    Elem<T>::unpack2(v, f);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) q[hh][i * VEC + e] = f[e] * p.qscale;
+                    for (int w = 0; w < PV; ++w) q2[hh][i * PV + w] = __fmul2_rn(f[w], sc);
                 }
 #pragma unroll
             for (int hh = 0; hh < HS; ++hh)
 #pragma unroll
-                for (int e = 0; e < E; ++e) o[hh][e] = 0.f;
+                for (int w = 0; w < E2; ++w) o2[hh][w] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < R; ++r) { m[r] = -INFINITY; l[r] = 0.f; }
         }
@@ -342,29 +345,40 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
             for (int itn = 0; itn < C::ITERS; ++itn) {
                 if ((itn * NWT + wt) * C::TPW >= n) break;
                 const int base = (itn * NWT + wt) * C::TPW + grp * TPI;
-                int tok[TPI];
+                // this lane's slices of the TPI token rows; masked rows read row 0 (p = 0 there).
+                // When the slices are few, K and V are both loaded up front.
+                constexpr bool PRE = TPI * NV <= 4;
+                int roff[TPI];
 #pragma unroll
-                for (int k = 0; k < TPI; ++k) tok[k] = (base + k < n) ? base + k : 0;
-                // q . k partial dots
-                float acc[TPI * HS];
+                for (int k = 0; k < TPI; ++k) roff[k] = ((base + k < n) ? base + k : 0) * D;
+                uint4 kv[TPI][NV], vv[PRE ? TPI : 1][PRE ? NV : 1];
 #pragma unroll
-                for (int k = 0; k < TPI * HS; ++k) acc[k] = 0.f;
-#pragma unroll
-                for (int k = 0; k < TPI; ++k) {
-                    const T* kr = Ks + tok[k] * D;
+                for (int k = 0; k < TPI; ++k)
 #pragma unroll
                     for (int i = 0; i < NV; ++i) {
-                        const uint4 v =
-                            *reinterpret_cast<const uint4*>(kr + vec_index<C>(i, lig, rot) * VEC);
-                        float f[VEC];
-                        Elem<T>::unpack(v, f);
+                        const int off = roff[k] + vec_index<C>(i, lig, rot) * VEC;
+                        kv[k][i] = *reinterpret_cast<const uint4*>(Ks + off);
+                        if constexpr (PRE) vv[k][i] = *reinterpret_cast<const uint4*>(Vs + off);
+                    }
+                // q . k partial dots: pairs of elements with packed fp32x2 FMAs
+                float2 acc2[TPI * HS];
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e)
+                for (int j = 0; j < TPI * HS; ++j) acc2[j] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+#pragma unroll
+                    for (int k = 0; k < TPI; ++k) {
+                        float2 f[PV];
+                        Elem<T>::unpack2(kv[k][i], f);
+#pragma unroll
+                        for (int w = 0; w < PV; ++w)
 #pragma unroll
                             for (int hh = 0; hh < HS; ++hh)
-                                acc[k * HS + hh] = fmaf(q[hh][i * VEC + e], f[e], acc[k * HS + hh]);
+                                acc2[k * HS + hh] = __ffma2_rn(q2[hh][i * PV + w], f[w], acc2[k * HS + hh]);
                     }
-                }
+                float acc[TPI * HS];
+#pragma unroll
+                for (int j = 0; j < TPI * HS; ++j) acc[j] = acc2[j].x + acc2[j].y;
                 float s2[R];
                 if constexpr (LPT == 1) {
                     const bool v0 = base < n;
@@ -387,7 +401,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                         for (int off = HS; off < LPT; off <<= 1)
                             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
                         const float mn = fmaxf(m[r], mx);
-                        alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(m[r] - mn);
+                        alpha[r] = (mn == -INFINITY) ? 1.f : fast_exp2(m[r] - mn);
                         m[r] = mn;
                         l[r] *= alpha[r];
                     }
@@ -396,39 +410,43 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                         float a;
                         if constexpr (LPT == 1) a = alpha[hh];
                         else a = __shfl_sync(FULL, alpha[0], gbase + hh);
+                        const float2 a2 = make_float2(a, a);
 #pragma unroll
-                        for (int e = 0; e < E; ++e) o[hh][e] *= a;
+                        for (int w = 0; w < E2; ++w) o2[hh][w] = __fmul2_rn(o2[hh][w], a2);
                     }
                 }
                 float pr[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    pr[r] = (s2[r] == -INFINITY) ? 0.f : exp2f(s2[r] - m[r]);
+                    pr[r] = (s2[r] == -INFINITY) ? 0.f : fast_exp2(s2[r] - m[r]);
                     l[r] += pr[r];
                 }
-                float pk[TPI][HS];
-#pragma unroll
-                for (int k = 0; k < TPI; ++k)
-#pragma unroll
-                    for (int hh = 0; hh < HS; ++hh) {
-                        if constexpr (LPT == 1) pk[k][hh] = pr[hh];
-                        else pk[k][hh] = __shfl_sync(FULL, pr[0], gbase + k * HS + hh);
-                    }
                 // p . V
 #pragma unroll
                 for (int k = 0; k < TPI; ++k) {
-                    const T* vr = Vs + tok[k] * D;
+                    float2 pp[HS];
+#pragma unroll
+                    for (int hh = 0; hh < HS; ++hh) {
+                        float pv;
+                        if constexpr (LPT == 1) pv = pr[hh];
+                        else pv = __shfl_sync(FULL, pr[0], gbase + k * HS + hh);
+                        pp[hh] = make_float2(pv, pv);
+                    }
 #pragma unroll
                     for (int i = 0; i < NV; ++i) {
-                        const uint4 v =
-                            *reinterpret_cast<const uint4*>(vr + vec_index<C>(i, lig, rot) * VEC);
-                        float f[VEC];
-                        Elem<T>::unpack(v, f);
+                        float2 f[PV];
+                        if constexpr (PRE) {
+                            Elem<T>::unpack2(vv[k][i], f);
+                        } else {
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                Vs + roff[k] + vec_index<C>(i, lig, rot) * VEC);
+                            Elem<T>::unpack2(v, f);
+                        }
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e)
+                        for (int w = 0; w < PV; ++w)
 #pragma unroll
                             for (int hh = 0; hh < HS; ++hh)
-                                o[hh][i * VEC + e] = fmaf(pk[k][hh], f[e], o[hh][i * VEC + e]);
+                                o2[hh][i * PV + w] = __ffma2_rn(pp[hh], f[w], o2[hh][i * PV + w]);
                     }
                 }
             }
@@ -463,6 +481,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 
         if (cur.last()) {
             // ---- segment epilogue: merge groups (shuffles), then warps (shared memory)
+            float o[HS][E];
+#pragma unroll
+            for (int hh = 0; hh < HS; ++hh)
+#pragma unroll
+                for (int w = 0; w < E2; ++w) { o[hh][2 * w] = o2[hh][w].x; o[hh][2 * w + 1] = o2[hh][w].y; }
             float mh[HS], lh[HS];
             if constexpr (LPT == 1) {
 #pragma unroll
@@ -501,7 +524,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                     float M = mh[hh];
 #pragma unroll
                     for (int off = LPT; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-                    const float c = (mh[hh] == -INFINITY) ? 0.f : exp2f(mh[hh] - M);
+                    const float c = (mh[hh] == -INFINITY) ? 0.f : fast_exp2(mh[hh] - M);
                     lh[hh] *= c;
 #pragma unroll
                     for (int e = 0; e < E; ++e) o[hh][e] *= c;

@@ -156,6 +156,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// 2^x with the SFU's approximate exp2 (relative error about 2^-22; results below the
+// smallest normal flush to zero, which the softmax weights tolerate: they are < 2^-126).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // bf16 pair (one 32-bit word) -> two floats, exact.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -172,6 +180,12 @@ struct Elem<__nv_bfloat16> {
         f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
         f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
     }
+    __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[4]) {
+        f[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+        f[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+        f[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+        f[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+    }
     __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
         reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(x);
     }
@@ -183,6 +197,10 @@ struct Elem<float> {
     __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[4]) {
         f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
         f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
     }
     __device__ __forceinline__ static void store(void* base, size_t idx, float x) {
         reinterpret_cast<float*>(base)[idx] = x;
