@@ -135,6 +135,25 @@ int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int
  * [floor(i*W/P), floor((i+1)*W/P)).  Returns the CTA that owns position x (0 <= x < W). */
 int kvc_plan_cta_of(int64_t x, int64_t W, int P);
 
+/* Decode attention for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is an interface variant of kvc_decode_attn, same kernel, same results.
+ * Who needs it: code that must not call cudaMalloc (a plugin whose host engine owns all device
+ * memory, a latency-critical loop where the allocator's device synchronisation is forbidden, a
+ * runtime with a fixed memory plan) and that keeps its K/V cache in memory it owns.
+ * Arguments: K, V are one layer's cache [B, H_kv, T_max, D] (device, dtype KVC_BF16 or
+ * KVC_F32, the same layout and limits as kvc_create); q, out [B, H_q, D] and lens [B] as in
+ * kvc_decode_attn; err is an optional device uint32 that receives the KVC_DEV_* bits (NULL:
+ * not reported); stream as elsewhere.
+ * Scratch: a fixed 8 MiB __device__ array inside the library (held by every device that loads
+ * it, until exit).  Shapes whose split-T scratch would exceed it return KVC_ERANGE before any
+ * launch.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ * The first call on a device looks the array's address up (cudaGetSymbolAddress) with that
+ * device current, so make it before any stream capture.  All calls share the array: calls
+ * that may overlap on the GPU (unordered streams) race and must not be made. */
+int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int H_q, int H_kv, int D,
+                            int T_max, int dtype, const void* q, void* out, const int32_t* lens,
+                            uint32_t* err, void* stream);
+
 /* Human-readable name of a status code. */
 const char* kvc_status_str(int status);
 

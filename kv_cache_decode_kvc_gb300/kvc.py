@@ -60,6 +60,7 @@ def load() -> ctypes.CDLL:
         "kvc_get_shape": (I, [P] + [ctypes.POINTER(I)] * 7),
         "kvc_plan_cta_of": (I, [I64, I64, I]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
+        "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -174,6 +175,15 @@ def kvc_get_shape(h) -> dict:
     _check(load().kvc_get_shape(h, *[ctypes.byref(v) for v in vals]), "kvc_get_shape")
     keys = ["layers", "B", "H_q", "H_kv", "D", "T_max", "dtype"]
     return {k: v.value for k, v in zip(keys, vals)}
+
+
+def kvc_decode_attn_noalloc(K, V, B, H_q, H_kv, D, T_max, dtype, q, out, lens, err=None,
+                            stream=None) -> None:
+    """Decode attention with no device allocation: K, V are one layer's cache buffers owned by
+    the caller; scratch lives in a fixed array inside the library (see include/kvc.h)."""
+    _check(load().kvc_decode_attn_noalloc(_ptr(K), _ptr(V), B, H_q, H_kv, D, T_max, dtype, _ptr(q),
+                                          _ptr(out), _ptr(lens), _ptr(err), _stream(stream)),
+           "kvc_decode_attn_noalloc")
 
 
 def kvc_plan_cta_of(x, W, P) -> int:
