@@ -125,6 +125,17 @@ int kvc_get_ctas(kvc_t h);
  * launched right after on the same stream.  Changes nothing beyond rounding. */
 int kvc_set_combine_mode(kvc_t h, int mode);
 
+/* Which units compute the two small contractions of the attention (q.K and p.V):
+ *   0 automatic: tcgen05 tensor cores for bf16 caches with D = 128, CUDA cores otherwise;
+ *   1 CUDA cores (fp32 arithmetic; the only path for fp32 caches);
+ *   2 warp-level mma.sync tensor instructions (bf16 caches);
+ *   3 tcgen05 tensor cores with tensor-memory accumulators (bf16 caches, D = 128).
+ * Paths 2 and 3 need B*H_kv*T_max < 2^31 (tensor-map coordinates), else KVC_EUNSUPPORTED.
+ * All paths agree within the bf16 tolerance.  kvc_get_math returns the path the next call
+ * takes (1, 2 or 3). */
+int kvc_set_math(kvc_t h, int mode);
+int kvc_get_math(kvc_t h);
+
 /* Shape query: writes layers, B, H_q, H_kv, D, T_max, dtype (any pointer may be NULL). */
 int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
                   int* dtype);

@@ -77,9 +77,8 @@ int launch_prefill(const CopyParams& p, cudaStream_t s) {
 
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s) {
     const int blocks = p.B * p.H_kv * G;
-    const int threads = D < 128 ? (D < 32 ? 32 : D) : 128;
-    if (dtype == 0) combine_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(p, D, G);
-    else combine_kernel<float><<<blocks, threads, 0, s>>>(p, D, G);
+    if (dtype == 0) combine_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(p, D, G);
+    else combine_kernel<float><<<blocks, 128, 0, s>>>(p, D, G);
     return (int)cudaGetLastError();
 }
 

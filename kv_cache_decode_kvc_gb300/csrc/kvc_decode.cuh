@@ -210,6 +210,138 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
                  &full_bar[stage], pol);
 }
 
+// Second half of a segment epilogue, shared by the decode kernels.  On entry every warp's state
+// (unnormalised output, max in log2 units, denominator) for its head slice is in `merge`
+// ([NW][HS][D+2]) and the CTA has synchronised.  Merges the warps of each slice, then either
+// writes the stream's output (the segment is the whole stream) or stores the partial state in
+// slot (CTA + stream); with combine_mode 0 the last CTA to arrive merges all partial states.
+// Synchronises the threads that run the epilogue: the whole CTA (BAR == 0) or the NT threads
+// of named barrier BAR.
+template <int BAR, int NT>
+__device__ __forceinline__ void group_sync() {
+    if constexpr (BAR == 0) __syncthreads();
+    else named_bar_sync(BAR, NT);
+}
+
+// Merges the partial states (slots c + unit, c in [cfirst, clast]) of one stream into its
+// output, o = sum_c w_c o_c / sum_c w_c l_c with w_c = 2^(m_c - M), M = max_c m_c.  Per-head
+// weights are formed once in shared memory (`scratch`, at least G * (D + 2) floats); the
+// output loop then issues its loads four segments at a time.  Run by NT threads.
+template <typename T, int G, int D, int NT, int BAR>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, float* scratch, size_t unit,
+                                               int64_t cfirst, int64_t clast, int tid) {
+    const int nseg = (int)(clast - cfirst + 1);
+    constexpr int CAP = (D + 2) / 2;  // segments whose (max, denominator) fit the scratch
+    if (nseg <= CAP) {
+        float* sm = scratch;               // [G][CAP]: maxima, then weights
+        float* sl = scratch + G * CAP;     // [G][CAP]: denominators
+        for (int i = tid; i < G * nseg; i += NT) {
+            const int h = i / nseg, c = i - h * nseg;
+            const size_t sidx = (size_t)(cfirst + c + (int64_t)unit);
+            sm[h * CAP + c] = __ldcg(&p.part_ml[(sidx * G + h) * 2]);
+            sl[h * CAP + c] = __ldcg(&p.part_ml[(sidx * G + h) * 2 + 1]);
+        }
+        group_sync<BAR, NT>();
+        for (int h = tid; h < G; h += NT) {
+            float M = -INFINITY;
+            for (int c = 0; c < nseg; ++c) M = fmaxf(M, sm[h * CAP + c]);
+            float den = 0.f;
+            for (int c = 0; c < nseg; ++c) {
+                const float w = (sm[h * CAP + c] == -INFINITY) ? 0.f : exp2f(sm[h * CAP + c] - M);
+                sm[h * CAP + c] = w;
+                den = fmaf(w, sl[h * CAP + c], den);
+            }
+            const float inv = 1.f / den;
+            for (int c = 0; c < nseg; ++c) sm[h * CAP + c] *= inv;
+        }
+        group_sync<BAR, NT>();
+        for (int idx = tid; idx < G * D; idx += NT) {
+            const int h = idx / D;
+            const float* po = p.part_o + (size_t)(cfirst + (int64_t)unit) * G * D + idx;
+            const size_t stride = (size_t)G * D;
+            float acc = 0.f;
+            int c = 0;
+            for (; c + 4 <= nseg; c += 4) {
+                const float v0 = __ldcg(po + (size_t)c * stride), v1 = __ldcg(po + (size_t)(c + 1) * stride);
+                const float v2 = __ldcg(po + (size_t)(c + 2) * stride), v3 = __ldcg(po + (size_t)(c + 3) * stride);
+                acc = fmaf(sm[h * CAP + c], v0, acc);
+                acc = fmaf(sm[h * CAP + c + 1], v1, acc);
+                acc = fmaf(sm[h * CAP + c + 2], v2, acc);
+                acc = fmaf(sm[h * CAP + c + 3], v3, acc);
+            }
+            for (; c < nseg; ++c) acc = fmaf(sm[h * CAP + c], __ldcg(po + (size_t)c * stride), acc);
+            Elem<T>::store(p.out, unit * G * D + idx, acc);
+        }
+    } else {
+        // many segments (few, very long streams): straightforward two passes per output
+        for (int idx = tid; idx < G * D; idx += NT) {
+            const int hg = idx / D;
+            float M = -INFINITY;
+            for (int64_t c = cfirst; c <= clast; ++c)
+                M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + unit) * G + hg) * 2]));
+            float num = 0.f, den = 0.f;
+            for (int64_t c = cfirst; c <= clast; ++c) {
+                const size_t sidx = (size_t)(c + unit);
+                const float mc = __ldcg(&p.part_ml[(sidx * G + hg) * 2]);
+                const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+                num = fmaf(w, __ldcg(&p.part_o[sidx * G * D + idx]), num);
+                den = fmaf(w, __ldcg(&p.part_ml[(sidx * G + hg) * 2 + 1]), den);
+            }
+            Elem<T>::store(p.out, unit * G * D + idx, num / den);
+        }
+    }
+}
+
+template <typename T, int G, int D, int HS, int NWT, int NW, int BAR = 0>
+__device__ __forceinline__ void finish_segment(const DecodeParams& p, float* merge,
+                                               const SegIter& it, size_t unit, int64_t W, int64_t P,
+                                               int* last_flag, int tid) {
+    const bool whole = (it.t0 == 0) && (it.t1 == it.L);
+    const int64_t us = it.ustart;
+    const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + it.L - 1, W, P);
+    const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int hg = idx / D, d = idx - hg * D;
+        const int s_ = hg / HS, hh = hg - s_ * HS;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NWT; ++w)
+            M = fmaxf(M, merge[(s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2) + D]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWT; ++w) {
+            const float* bw = merge + (s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2);
+            const float c = (bw[D] == -INFINITY) ? 0.f : exp2f(bw[D] - M);
+            num = fmaf(c, bw[d], num);
+            den = fmaf(c, bw[D + 1], den);
+        }
+        if (whole) {
+            Elem<T>::store(p.out, unit * G * D + idx, num / den);
+        } else {
+            p.part_o[(size_t)slot * G * D + idx] = num;
+            if (d == 0) {
+                p.part_ml[((size_t)slot * G + hg) * 2] = M;
+                p.part_ml[((size_t)slot * G + hg) * 2 + 1] = den;
+            }
+        }
+    }
+    if (!whole && p.combine_mode == 0) {
+        __threadfence();
+        group_sync<BAR, NW * 32>();  // also: every thread is done reading merge
+        if (tid == 0) {
+            const int prev = atomicAdd(&p.counters[unit], 1);
+            *last_flag = (prev == (int)(clast - cfirst));
+        }
+        group_sync<BAR, NW * 32>();
+        if (*last_flag) {
+            __threadfence();
+            merge_partials<T, G, D, NW * 32, BAR>(p, merge, unit, cfirst, clast, tid);
+            if (tid == 0) p.counters[unit] = 0;  // every arrival is in: ready for next call
+        }
+    }
+    group_sync<BAR, NW * 32>();  // merge buffer and flags are reused by the next segment
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
     decode_kernel(const DecodeParams p) {
@@ -556,64 +688,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
             }
             __syncthreads();
 
-            const bool whole = (cur.it.t0 == 0) && (cur.it.t1 == cur.it.L);
-            const int64_t us = cur.it.ustart;
-            const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + cur.it.L - 1, W, P);
-            const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
-            for (int idx = tid; idx < G * D; idx += NW * 32) {
-                const int hg = idx / D, d = idx - hg * D;
-                const int s_ = hg / HS, hh = hg - s_ * HS;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < NWT; ++w)
-                    M = fmaxf(M, merge[(s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2) + D]);
-                float num = 0.f, den = 0.f;
-#pragma unroll
-                for (int w = 0; w < NWT; ++w) {
-                    const float* bw = merge + (s_ * NWT + w) * (HS * (D + 2)) + hh * (D + 2);
-                    const float c = (bw[D] == -INFINITY) ? 0.f : exp2f(bw[D] - M);
-                    num = fmaf(c, bw[d], num);
-                    den = fmaf(c, bw[D + 1], den);
-                }
-                if (whole) {
-                    Elem<T>::store(p.out, unit * G * D + idx, num / den);
-                } else {
-                    p.part_o[(size_t)slot * G * D + idx] = num;
-                    if (d == 0) {
-                        p.part_ml[((size_t)slot * G + hg) * 2] = M;
-                        p.part_ml[((size_t)slot * G + hg) * 2 + 1] = den;
-                    }
-                }
-            }
-            if (!whole && p.combine_mode == 0) {
-                __threadfence();
-                __syncthreads();
-                if (tid == 0) {
-                    const int prev = atomicAdd(&p.counters[unit], 1);
-                    *last_flag = (prev == (int)(clast - cfirst));
-                }
-                __syncthreads();
-                if (*last_flag) {
-                    __threadfence();
-                    for (int idx = tid; idx < G * D; idx += NW * 32) {
-                        const int hg = idx / D;
-                        float M = -INFINITY;
-                        for (int64_t c = cfirst; c <= clast; ++c)
-                            M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + unit) * G + hg) * 2]));
-                        float num = 0.f, den = 0.f;
-                        for (int64_t c = cfirst; c <= clast; ++c) {
-                            const size_t sidx = (size_t)(c + unit);
-                            const float mc = __ldcg(&p.part_ml[(sidx * G + hg) * 2]);
-                            const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                            num = fmaf(w, __ldcg(&p.part_o[sidx * G * D + idx]), num);
-                            den = fmaf(w, __ldcg(&p.part_ml[(sidx * G + hg) * 2 + 1]), den);
-                        }
-                        Elem<T>::store(p.out, unit * G * D + idx, num / den);
-                    }
-                    if (tid == 0) p.counters[unit] = 0;  // every arrival is in: ready for next call
-                }
-            }
-            __syncthreads();  // merge buffer and flags are reused by the next segment
+            finish_segment<T, G, D, HS, NWT, NW>(p, merge, cur.it, unit, W, P, last_flag, tid);
         }
         cur.advance();
     }
@@ -634,12 +709,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 }
 
 // Merges the partial states of streams cut across CTAs (combine_mode 1): one block per
-// (stream, query head of its group); threads over D.  Recomputes the same partition.
+// (stream, query head of its group); threads over the segments, then over D.  Recomputes the
+// same partition as the decode kernels.
+constexpr int COMBINE_MAX_SEG = 1024;
 template <typename T>
-__global__ void combine_kernel(const DecodeParams p, int D, int G) {
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int D, int G) {
     const int u = blockIdx.x / G, hg = blockIdx.x % G;
     const int b = u / p.H_kv, h = u % p.H_kv;
     __shared__ int64_t sh_sum[2];
+    __shared__ float sw[COMBINE_MAX_SEG];
+    __shared__ float sred[4];
     if (threadIdx.x < 2) sh_sum[threadIdx.x] = 0;
     __syncthreads();
     int64_t before = 0, all = 0;
@@ -663,19 +742,46 @@ __global__ void combine_kernel(const DecodeParams p, int D, int G) {
     const int64_t us = (int64_t)p.H_kv * sh_sum[0] + (int64_t)h * Lb;
     const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + Lb - 1, W, P);
     if (cfirst == clast) return;  // written directly by its CTA
-    float M = -INFINITY;
-    for (int64_t c = cfirst; c <= clast; ++c)
-        M = fmaxf(M, p.part_ml[((size_t)(c + u) * G + hg) * 2]);
+    const int nseg = (int)(clast - cfirst + 1);
+    if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs
+    const size_t base = (size_t)(cfirst + u);
+    // weights w_c = 2^(m_c - M) / sum_c 2^(m_c - M) l_c, formed once in shared memory
+    float mx = -INFINITY;
+    for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
+        const float mc = p.part_ml[((base + c) * G + hg) * 2];
+        sw[c] = mc;
+        mx = fmaxf(mx, mc);
+    }
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    if ((threadIdx.x & 31) == 0) sred[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(sred[0], sred[1]), fmaxf(sred[2], sred[3]));
+    __syncthreads();
+    float den = 0.f;
+    for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
+        const float w = (sw[c] == -INFINITY) ? 0.f : exp2f(sw[c] - M);
+        sw[c] = w;
+        den = fmaf(w, p.part_ml[((base + c) * G + hg) * 2 + 1], den);
+    }
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
+    if ((threadIdx.x & 31) == 0) sred[threadIdx.x >> 5] = den;
+    __syncthreads();
+    const float inv = 1.f / (sred[0] + sred[1] + sred[2] + sred[3]);
+    const size_t stride = (size_t)G * D;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float num = 0.f, den = 0.f;
-        for (int64_t c = cfirst; c <= clast; ++c) {
-            const size_t sidx = (size_t)(c + u);
-            const float mc = p.part_ml[(sidx * G + hg) * 2];
-            const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-            num = fmaf(w, p.part_o[(sidx * G + hg) * D + d], num);
-            den = fmaf(w, p.part_ml[(sidx * G + hg) * 2 + 1], den);
+        const float* po = p.part_o + base * stride + (size_t)hg * D + d;
+        float acc = 0.f;
+        int c = 0;
+        for (; c + 4 <= nseg; c += 4) {
+            const float v0 = po[(size_t)c * stride], v1 = po[(size_t)(c + 1) * stride];
+            const float v2 = po[(size_t)(c + 2) * stride], v3 = po[(size_t)(c + 3) * stride];
+            acc = fmaf(sw[c], v0, acc);
+            acc = fmaf(sw[c + 1], v1, acc);
+            acc = fmaf(sw[c + 2], v2, acc);
+            acc = fmaf(sw[c + 3], v3, acc);
         }
-        Elem<T>::store(p.out, ((size_t)u * G + hg) * D + d, num / den);
+        for (; c < nseg; ++c) acc = fmaf(sw[c], po[(size_t)c * stride], acc);
+        Elem<T>::store(p.out, ((size_t)u * G + hg) * D + d, acc * inv);
     }
 }
 

@@ -1,0 +1,577 @@
+// kvc_decode_tc5.cuh -- decode attention over a bf16 cache with the two contractions on the
+// 5th-generation tensor cores (tcgen05: single-thread MMA issue, operands in shared memory,
+// accumulators in tensor memory).
+//
+// Same computation, split-T partition and merging as decode_kernel (kvc_decode.cuh): for every
+// query head j of sequence b, o = softmax_t(q . K_t / sqrt(D)) V over t < lens[b]
+// ("11.7 KV Cache：形状、显存与带宽" §2.2; head map of "第 1 周 · Day 4：KV Cache 与 MQA /
+// GQA" §3.4).  A CTA (producer warp, MMA warp, 4 softmax warps) consumes 128-token tiles:
+//   MMA1  S^T[128 tok x N]  = K[128 x D] . Q^T[D x N]   A = K tile (K-major), B = q (K-major)
+//   softmax: a thread owns one token (one tensor-memory lane) and all N head columns
+//   MMA2  O^T[D x N]        = V^T[D x 128] . P^T[128 x N]  A = V tile read MN-major, B = P
+//   O^T is read back per tile (a thread owns output element d = its lane) and accumulated in
+//   registers with the online-softmax rescale.  S^T, O^T and P are double-buffered so MMA1 of
+//   tile k+1 overlaps the softmax of tile k.
+// N = the query-head group padded to at least 16 (tcgen05 needs N % 16 == 0 at M = 128); the
+// padded q rows are zero.  P is stored as P_hi + P_lo (two bf16 terms) so the weights keep
+// fp32-level accuracy; MMA2 runs once per term.  Everything the tensor cores read is in the
+// 128-byte-swizzled K-major or MN-major canonical layout: K/V tiles arrive that way from TMA
+// tensor copies (boxes of 64 columns x 32 rows), q and P are written that way by the threads.
+// HBM traffic is unchanged: every K/V byte once per step, shared by the whole group.
+#pragma once
+
+#include "kvc_decode_tc.cuh"
+
+namespace kvc {
+
+template <int G_>
+struct Tc5Cfg {
+    static constexpr int D = 128;
+    static constexpr int G = G_;
+    static constexpr int N = G < 16 ? 16 : G;           // MMA N (heads, padded)
+    static constexpr int ROWB = D * 2;
+    static constexpr int HALVES = D / 64;               // 128-byte column blocks
+    static constexpr int NW = 4;                        // softmax warps (+ producer + MMA warp)
+    static constexpr int NTHREADS = 192;
+    static constexpr int TT = 128;                      // tokens per tile = MMA M
+    static constexpr int BOX_ROWS = TC_BOX_ROWS;
+    static constexpr int HALF_BYTES = TT * 128;         // one column block of a K or V tile
+    static constexpr int TILE_BYTES = TT * ROWB;
+    static constexpr int QRAW_BYTES = (G * ROWB + 1023) / 1024 * 1024;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + QRAW_BYTES;
+    static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128] operand
+    static constexpr int OPB_BYTES = HALVES * OPB_BLOCK;
+    static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
+    static constexpr int MERGE_FLOATS = G * (D + 2);
+    static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
+    static constexpr int RED_BYTES = NW * N * 4;        // cross-warp max reduction
+    // 4 tensor maps: K and V with 128-row boxes (full tiles) and 32-row boxes (partial tiles)
+    static constexpr int MISC_BYTES = 256;
+    static constexpr int ALIGN_PAD = 1024;
+    static constexpr int BUDGET = 232448;               // opt-in maximum per CTA (227 KB)
+    static constexpr int FIXED = 5 * OPB_BYTES + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
+                                 MISC_BYTES + ALIGN_PAD;
+    static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
+    static constexpr int NST = NST_A > 4 ? 4 : NST_A;
+    static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
+    static constexpr int TMEM_COLS = 4 * N <= 32 ? 32 : (4 * N <= 64 ? 64 : (4 * N <= 128 ? 128 : 256));
+    static_assert(NST >= 2, "ring too shallow");
+    static_assert(N % 16 == 0 && N <= 256, "MMA N");
+    static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
+};
+
+// ---- tcgen05 descriptors
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets (>> 4), the
+// descriptor version of this tensor-core generation (1), 128-byte swizzle layout (2).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness (0 = K-major,
+// 1 = MN-major), N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc5_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc5_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc5_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc5_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc5_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Issues one tile: a full tile is one 128-row box per column block of K and of V (maps tmKf /
+// tmVf); a partial tile uses 32-row boxes (tmK / tmV), rows past the stream's end being loaded
+// and masked; the first tile of a segment also brings q.
+template <class C, int TT>
+__device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const TileCursor<TT>& c,
+                                               uint32_t ring, uint64_t* full_bar, int stage,
+                                               uint64_t pol, const CUtensorMap* tmK,
+                                               const CUtensorMap* tmV, const CUtensorMap* tmKf,
+                                               const CUtensorMap* tmVf) {
+    const int n = c.n();
+    const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
+    const uint32_t ks = ring + stage * C::STAGE_BYTES;
+    const uint32_t vs = ks + C::TILE_BYTES;
+    const uint32_t qs = vs + C::TILE_BYTES;
+    const bool full = n == TT;
+    const int nbox = full ? 1 : (n + C::BOX_ROWS - 1) / C::BOX_ROWS;
+    const int rows = full ? TT : C::BOX_ROWS;
+    const bool with_q = c.first();
+    uint32_t bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
+    if (with_q) bytes += C::G * C::ROWB;
+    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+    const int row0 = (int)(unit * p.T_max + c.t);
+    const CUtensorMap* mk = full ? tmKf : tmK;
+    const CUtensorMap* mv = full ? tmVf : tmV;
+#pragma unroll
+    for (int hf = 0; hf < C::HALVES; ++hf)
+        for (int bx = 0; bx < nbox; ++bx) {
+            const uint32_t off = hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128;
+            tma_load_2d(ks + off, mk, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+            tma_load_2d(vs + off, mv, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+        }
+    if (with_q) {
+        asm volatile(
+            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+            "[%1], %2, [%3], %4;" ::"r"(qs),
+            "l"(static_cast<const char*>(p.q) + unit * C::G * C::ROWB), "r"(C::G * C::ROWB),
+            "r"(smem_addr(&full_bar[stage])), "l"(pol)
+            : "memory");
+    }
+}
+
+// Named barrier of the four softmax warps with an OR reduction of a predicate.
+__device__ __forceinline__ bool softmax_group_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Warp roles: warp 0 issues the tensor copies (producer), warp 1 issues the MMAs, warps 2-5 run
+// the softmax, write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane).
+// Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
+// the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
+template <int G>
+__global__ void __launch_bounds__(192, 1)
+    decode_tc5_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKf,
+                      const __grid_constant__ CUtensorMap tmVf) {
+    using C = Tc5Cfg<G>;
+    using T = __nv_bfloat16;
+    constexpr int D = C::D, N = C::N, TT = C::TT, NST = C::NST, KS = D / 16, TS = TT / 16;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* ring = smem;
+    unsigned char* qsw = ring + NST * C::STAGE_BYTES;        // q, [N][D] K-major swizzled
+    unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][hi, lo][N][TT]
+    float* merge = reinterpret_cast<float*>(pbuf + 4 * C::OPB_BYTES);
+    int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
+    float* red = reinterpret_cast<float*>(prefix + MAX_B + 1);  // [4][N]
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(red + 4 * N);
+    uint64_t* empty_bar = full_bar + NST;
+    uint64_t* s_full = empty_bar + NST;   // [2]
+    uint64_t* s_empty = s_full + 2;
+    uint64_t* p_full = s_empty + 2;
+    uint64_t* o_full = p_full + 2;
+    uint64_t* o_empty = o_full + 2;
+    int* issued = reinterpret_cast<int*>(o_empty + 2);       // [NST]
+    volatile int* abort_flag = issued + NST;
+    int* last_flag = issued + NST + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(issued + NST + 2);
+    int* mma_issued = issued + NST + 3;                      // MMA2 commits issued (abort drain)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.B, H_kv = p.H_kv;
+    const size_t row_elems_q = (size_t)H_kv * G * D;
+
+    if (warp == 0) {
+        int64_t carry = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) {
+            const int b = b0 + lane;
+            int64_t x = 0;
+            if (b < B) {
+                const int L = p.lens[b];
+                x = (L >= 1 && L <= p.T_max) ? L : 0;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(FULL, x, o);
+                if (lane >= o) x += y;
+            }
+            if (b < B) prefix[b + 1] = carry + x;
+            carry += __shfl_sync(FULL, x, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
+    if (tid == 32) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+            issued[s] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
+        }
+        *abort_flag = 0;
+        *last_flag = 0;
+        *mma_issued = 0;
+        fence_mbar_init();
+    }
+    // padded q rows and P rows of padded heads stay zero for the whole kernel
+    for (int i = tid; i < 5 * C::OPB_BYTES / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        if (prefix[b + 1] == prefix[b]) {
+            if (tid == 0) atomicOr(p.err, DEV_BAD_LENS);
+            for (size_t i = tid; i < row_elems_q; i += blockDim.x)
+                Elem<T>::store(p.out, (size_t)b * row_elems_q + i, 0.f);
+        }
+    }
+
+    const int64_t W = (int64_t)H_kv * prefix[B];
+    if (W == 0) return;
+    int64_t P = p.P;
+    {
+        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
+        if (want < P) P = want;
+    }
+    if ((int64_t)blockIdx.x >= P) return;
+    const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
+    if (r0 >= r1) return;
+
+    // ---- fused append (see kvc_decode_tc.cuh): new rows into the cache before any tensor copy
+    if (p.k_new != nullptr && warp == 0) {
+        SegIter it;
+        it.init(prefix, B, H_kv, r0, r1);
+        while (it.valid) {
+            if (it.t1 == it.L) {
+                const size_t unit = (size_t)it.b * H_kv + it.h;
+                const size_t dst = (unit * p.T_max + (size_t)(it.L - 1)) * C::ROWB;
+                const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + unit * C::ROWB);
+                const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + unit * C::ROWB);
+                uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + dst);
+                uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.V)) + dst);
+                for (int v = lane; v < C::ROWB / 16; v += 32) {
+                    kd[v] = __ldg(ksrc + v);
+                    vd[v] = __ldg(vsrc + v);
+                }
+            }
+            it.next();
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+    }
+    // ---- tensor memory: S^T buffers at columns [0, N) and [N, 2N); O^T at [2N, 3N) and [3N, 4N)
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc5_fence_before();
+    __syncthreads();
+    tc5_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t ring_s = smem_addr(ring);
+
+    if (warp == 0) {
+        // ======================================================= producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKf)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVf)) : "memory");
+            const uint64_t pol = policy_evict_first();
+            TileCursor<TT> pref;
+            pref.init(prefix, B, H_kv, r0, r1);
+            int s = 0;
+            uint32_t ph = 0;
+            while (pref.valid) {
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err)) break;
+                issue_tile_tc5<C, TT>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf);
+                issued[s] += 1;
+                pref.advance();
+                if (++s == NST) { s = 0; ph ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ======================================================= MMA issue
+        constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
+        constexpr uint32_t IDESC2 = instr_desc_bf16(128, N, 1, 0);  // V read MN-major x P (K-major)
+        const uint32_t qsw_s = smem_addr(qsw), pbuf_s = smem_addr(pbuf);
+        const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, 1024u);                    // + stage, block, k-step
+        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, (uint32_t)C::HALF_BYTES, 1024u);
+        const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
+        const uint64_t dP0 = smem_desc_sw128(pbuf_s, 16u, 1024u);
+        TileCursor<TT> cur;
+        cur.init(prefix, B, H_kv, r0, r1);
+        int s = 0, s_prev = 0;
+        uint32_t ph = 0;
+        bool alive = true;
+        for (int k = 0;; ++k) {
+            // MMA2 of the previous tile first: it frees a ring stage as soon as P is ready
+            if (k > 0 && alive) {
+                // ---- MMA2(k-1): O^T[(k-1)&1] = V(stage s_prev)^T . (P_hi + P_lo)^T
+                const int j = k - 1;
+                alive = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err) &&
+                        mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
+                if (alive && lane == 0) {
+                    tc5_fence_after();
+                    const uint32_t tO = tmem + (uint32_t)((2 + (j & 1)) * N);
+                    const uint32_t pb = (uint32_t)((j & 1) * 2 * C::OPB_BYTES);
+#pragma unroll
+                    for (int term = 0; term < 2; ++term)
+#pragma unroll
+                        for (int kk = 0; kk < TS; ++kk) {
+                            const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2048);
+                            const uint32_t poff = pb + (uint32_t)(term * C::OPB_BYTES + (kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
+                            tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, (term > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    tc5_commit(&o_full[j & 1]);
+                    tc5_commit(&empty_bar[s_prev]);  // K/V of the stage are consumed
+                    *mma_issued += 1;
+                }
+                __syncwarp();
+            }
+            const bool have = cur.valid && alive;
+            if (!have) break;
+            // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
+            alive = mbar_wait(&full_bar[s], ph, abort_flag, p.err);
+            if (alive && cur.first()) {
+                // the previous MMA1 read q_sw: let it finish before q is replaced
+                if (k > 0) alive = mbar_wait(&s_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err);
+                const unsigned char* qraw = ring + s * C::STAGE_BYTES + 2 * C::TILE_BYTES;
+                for (int c = lane; c < G * (D / 8); c += 32) {
+                    const int h = c / (D / 8), cc = c % (D / 8);
+                    const uint4 v = *reinterpret_cast<const uint4*>(qraw + h * C::ROWB + cc * 16);
+                    *reinterpret_cast<uint4*>(qsw + (cc >> 3) * C::OPB_BLOCK + h * 128 +
+                                              (((cc & 7) ^ (h & 7)) << 4)) = v;
+                }
+                fence_async_smem();
+                __syncwarp();
+            }
+            if (alive) alive = mbar_wait(&s_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+            if (alive && lane == 0) {
+                tc5_fence_after();
+                const uint32_t tS = tmem + (uint32_t)((k & 1) * N);
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32);
+                    const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
+                    tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
+                }
+                tc5_commit(&s_full[k & 1]);
+            }
+            __syncwarp();
+            s_prev = s;
+            cur.advance();
+            if (++s == NST) { s = 0; ph ^= 1u; }
+        }
+    } else {
+        // ======================================================= softmax + accumulate
+        const int q4 = warp & 3;            // tensor-memory lane quadrant of this warp
+        const int row = q4 * 32 + lane;     // token of S^T rows / element d of O^T rows
+        const int gt = tid - 64;            // 0..127 within the group
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const float qscale = p.qscale;
+        float o[G], m[G], l[G], alpha[G], alpha_prev[G];
+        TileCursor<TT> cur;
+        cur.init(prefix, B, H_kv, r0, r1);
+        int s = 0;
+        uint32_t ph = 0;
+        bool alive = true;
+        auto absorb = [&](int j, const float* a) {
+            // O^T(j) into the accumulator: o = o * alpha_j + O^T(j)[row, :]
+            alive = alive && mbar_wait(&o_full[j & 1], (j >> 1) & 1, abort_flag, p.err);
+            tc5_fence_after();
+            float v[16];
+#pragma unroll
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                tc5_ld16(tmem + (uint32_t)((2 + (j & 1)) * N + c0) + lane_off, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (c0 + i < G) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], v[i]) : o[c0 + i];
+            }
+            tc5_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[j & 1]);
+        };
+        for (int k = 0; cur.valid; ++k) {
+            const size_t unit = (size_t)cur.it.b * H_kv + cur.it.h;
+            const int n = cur.n();
+            const bool first = cur.first(), last = cur.last();
+            if (first) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) { o[h] = 0.f; m[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f; }
+            }
+            // ---- scores of tile k
+            alive = alive && mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
+            tc5_fence_after();
+            float x[G];
+            {
+                float v[16];
+#pragma unroll
+                for (int c0 = 0; c0 < N && c0 < G; c0 += 16) {
+                    tc5_ld16(tmem + (uint32_t)((k & 1) * N + c0) + lane_off, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (c0 + i < G) x[c0 + i] = v[i];
+                }
+            }
+            tc5_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[k & 1]);
+            const bool valid = row < n;
+            bool need = false;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                x[h] = valid ? x[h] * qscale : -INFINITY;
+                need |= x[h] > m[h] + TAU;
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) alpha[h] = 1.f;
+            if (softmax_group_any(need)) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float mx = x[h];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+                    if (lane == 0) red[q4 * N + h] = mx;
+                }
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float mx = red[h];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[w * N + h]);
+                    const float mn = fmaxf(m[h], mx);
+                    alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
+                    m[h] = mn;
+                    l[h] *= alpha[h];
+                }
+                named_bar_sync(1, 128);  // red is reused
+            }
+            // ---- P(k) = P_hi + P_lo, K-major swizzled rows h, column (token) row
+            {
+                unsigned char* pb = pbuf + (k & 1) * 2 * C::OPB_BYTES;
+                const uint32_t coff = (uint32_t)(row >> 6) * C::OPB_BLOCK;
+                const int chunk = (row & 63) >> 3, e = row & 7;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float pv = (x[h] == -INFINITY) ? 0.f : fast_exp2(x[h] - m[h]);
+                    l[h] += pv;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+                    const uint32_t off = coff + h * 128 + (((chunk ^ (h & 7)) << 4) | (e << 1));
+                    *reinterpret_cast<__nv_bfloat16*>(pb + off) = hi;
+                    *reinterpret_cast<__nv_bfloat16*>(pb + C::OPB_BYTES + off) = lo;
+                }
+            }
+            // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2)
+            const int loaded = ((n + C::BOX_ROWS - 1) / C::BOX_ROWS) * C::BOX_ROWS;
+            if (row >= loaded) {
+                unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + row * 128;
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(vt + hf * C::HALF_BYTES + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[k & 1]);
+            // ---- fold in O^T of the previous tile of this segment
+            if (!first) absorb(k - 1, alpha_prev);
+#pragma unroll
+            for (int h = 0; h < G; ++h) alpha_prev[h] = alpha[h];
+            if (last) {
+                absorb(k, alpha);
+                // ---- segment epilogue: group-wide denominators, then the shared merge
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float s_ = l[h];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) s_ += __shfl_xor_sync(FULL, s_, off);
+                    if (lane == 0) red[q4 * N + h] = s_;
+                }
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int h = 0; h < G; ++h) merge[h * (D + 2) + row] = o[h];
+                if (gt < G) {
+                    float s_ = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) s_ += red[w * N + gt];
+                    merge[gt * (D + 2) + D] = m[gt];
+                    merge[gt * (D + 2) + D + 1] = s_;
+                }
+                named_bar_sync(1, 128);
+                finish_segment<T, G, D, C::HS, 1, 4, 1>(p, merge, cur.it, unit, W, P, last_flag, gt);
+            }
+            cur.advance();
+            if (++s == NST) { s = 0; ph ^= 1u; }
+        }
+    }
+    if (*abort_flag) {
+        // broken protocol (a wait timed out): let issued copies and MMAs land, bounded
+        if (tid == 0) {
+            for (int s = 0; s < NST; ++s) {
+                if (issued[s] == 0) continue;
+                const uint32_t par = (uint32_t)((issued[s] - 1) & 1);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&full_bar[s], par) && global_ns() - t0 < WAIT_LIMIT_NS) {
+                }
+            }
+        }
+        if (tid == 32 && *mma_issued > 0) {
+            const int j = *mma_issued - 1;
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(&o_full[j & 1], (j >> 1) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+            }
+        }
+    }
+    tc5_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc5_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+}  // namespace kvc

@@ -1,0 +1,36 @@
+// kvc_decode_tc5_inst.cu -- instantiates the tcgen05 decode kernel (bf16 cache, D = 128); the
+// query-head group G is dispatched at run time.
+#include "kvc_decode_tc5.cuh"
+
+namespace kvc {
+
+template <int G>
+static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                        int* smem_out) {
+    using C = Tc5Cfg<G>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return (int)e;
+        attr_set = true;
+    }
+    if (smem_out) *smem_out = C::SMEM;
+    decode_tc5_kernel<G><<<p.P, C::NTHREADS, C::SMEM, s>>>(p, maps[0], maps[1], maps[2], maps[3]);
+    return (int)cudaGetLastError();
+}
+
+int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                           int* smem_out) {
+    switch (G) {
+        case 1: return launch_tc5_g<1>(p, maps, s, smem_out);
+        case 2: return launch_tc5_g<2>(p, maps, s, smem_out);
+        case 4: return launch_tc5_g<4>(p, maps, s, smem_out);
+        case 8: return launch_tc5_g<8>(p, maps, s, smem_out);
+        case 16: return launch_tc5_g<16>(p, maps, s, smem_out);
+        case 32: return launch_tc5_g<32>(p, maps, s, smem_out);
+        default: return (int)cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace kvc

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <new>
+#include <vector>
 
 #include "../../include/kvc.h"
 #include "kvc_internal.cuh"
@@ -23,6 +24,9 @@ struct kvc_cache {
     float* part_ml;
     int* counters;
     uint32_t* err;
+    int math;                        // 0 automatic, 1 CUDA cores, 2 warp MMA, 3 tcgen05
+    bool tc_ok;                      // tensor maps built (bf16 cache, rows < 2^31)
+    std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes)
 };
 
 namespace {
@@ -35,6 +39,41 @@ bool d_supported(int dtype, int D) {
 
 bool g_supported(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16 || G == 32; }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched through the runtime (no link-time libcuda).
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D map over one layer's K or V cache: columns D (contiguous), rows B*H_kv*T_max; boxes of 64
+// columns (128 bytes) x box_rows rows, 128-byte swizzle, zero fill past the last row.
+bool make_kv_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // a * b with overflow detection (all operands >= 0)
 bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
     if (a != 0 && b > UINT64_MAX / a) return false;
@@ -42,10 +81,30 @@ bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
     return true;
 }
 
-int launch_decode(const kvc_cache* h, const kvc::DecodeParams& p, cudaStream_t s) {
+// Which kernel computes the attention: 1 CUDA cores, 2 warp-level MMA, 3 tcgen05.
+int kvc_math_path(const kvc_cache* h) {
+    if (!h->tc_ok || h->math == 1) return 1;
+    if (h->math == 2) return 2;
+    if (h->math == 3) return 3;
+    return h->D == 128 ? 3 : 1;  // automatic
+}
+
+int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cudaStream_t s) {
     int smem = 0;
     int e;
-    if (h->dtype == KVC_BF16) {
+    const int path = kvc_math_path(h);
+    if (path == 3) {
+        e = kvc::launch_decode_tc5_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem);
+    } else if (path == 2) {
+        const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
+        const CUtensorMap& tv = h->tmaps[4 * (size_t)layer + 1];
+        switch (h->D) {
+            case 64: e = kvc::launch_decode_tc_d64(h->G, p, tk, tv, s, &smem); break;
+            case 128: e = kvc::launch_decode_tc_d128(h->G, p, tk, tv, s, &smem); break;
+            case 256: e = kvc::launch_decode_tc_d256(h->G, p, tk, tv, s, &smem); break;
+            default: return KVC_EUNSUPPORTED;
+        }
+    } else if (h->dtype == KVC_BF16) {
         switch (h->D) {
             case 64: e = kvc::launch_decode_bf16_d64(h->G, p, s, &smem); break;
             case 128: e = kvc::launch_decode_bf16_d128(h->G, p, s, &smem); break;
@@ -100,7 +159,7 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     }
     p.combine_mode = mode;
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
-    return launch_decode(h, p, static_cast<cudaStream_t>(stream));
+    return launch_decode(h, layer, p, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -163,6 +222,8 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
     h->sms = prop.multiProcessorCount;
     h->ctas = 0;
     h->combine_mode = -1;
+    h->math = 0;
+    h->tc_ok = false;
     h->max_ctas = 4 * h->sms;
     h->layer_bytes = (size_t)B * H_kv * (size_t)T_max * D * es;
 
@@ -191,6 +252,23 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
         cudaFree(h->slab);
         delete h;
         return KVC_ECUDA;
+    }
+    // tensor maps for the tensor-core kernel (bf16 caches whose rows fit the map's coordinates)
+    const uint64_t rows = (uint64_t)B * H_kv * (uint64_t)T_max;
+    if (dtype == KVC_BF16 && rows < (1ull << 31)) {
+        h->tmaps.resize(4 * (size_t)layers);
+        bool ok = true;
+        for (int l = 0; l < layers && ok; ++l) {
+            void* kb = h->slab + (size_t)(2 * l) * h->layer_bytes;
+            void* vb = h->slab + (size_t)(2 * l + 1) * h->layer_bytes;
+            CUtensorMap* m4 = &h->tmaps[4 * (size_t)l];
+            ok = make_kv_tensor_map(&m4[0], kb, rows, D, kvc::TC_BOX_ROWS) &&
+                 make_kv_tensor_map(&m4[1], vb, rows, D, kvc::TC_BOX_ROWS) &&
+                 make_kv_tensor_map(&m4[2], kb, rows, D, kvc::TC_FULL_ROWS) &&
+                 make_kv_tensor_map(&m4[3], vb, rows, D, kvc::TC_FULL_ROWS);
+        }
+        h->tc_ok = ok;
+        if (!ok) h->tmaps.clear();
     }
     *out = h;
     return KVC_OK;
@@ -247,6 +325,19 @@ int kvc_set_ctas(kvc_t h, int ctas) {
 int kvc_get_ctas(kvc_t h) {
     if (!h) return -1;
     return h->ctas > 0 ? h->ctas : h->sms;
+}
+
+int kvc_set_math(kvc_t h, int mode) {
+    if (!h || mode < 0 || mode > 3) return KVC_EINVAL;
+    if (mode >= 2 && !h->tc_ok) return KVC_EUNSUPPORTED;
+    if (mode == 3 && h->D != 128) return KVC_EUNSUPPORTED;
+    h->math = mode;
+    return KVC_OK;
+}
+
+int kvc_get_math(kvc_t h) {
+    if (!h) return -1;
+    return kvc_math_path(h);
 }
 
 int kvc_set_combine_mode(kvc_t h, int mode) {

@@ -2,6 +2,7 @@
 // of libkvc (never by the CPU oracle).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -69,6 +70,21 @@ KVC_DECLARE_LAUNCHER(launch_decode_f32_d4)
 KVC_DECLARE_LAUNCHER(launch_decode_f32_d64)
 KVC_DECLARE_LAUNCHER(launch_decode_f32_d128)
 KVC_DECLARE_LAUNCHER(launch_decode_f32_d256)
+// Tensor-core decode (bf16 cache), one launcher per head dimension; tmK / tmV are the layer's
+// 2-D tensor maps (rows = B*H_kv*T_max, columns = D; boxes of 64 columns x 32 rows, 128-byte
+// swizzle), built by make_kv_tensor_map.
+int launch_decode_tc_d64(int G, const DecodeParams& p, const CUtensorMap& tmK,
+                         const CUtensorMap& tmV, cudaStream_t s, int* smem_out);
+int launch_decode_tc_d128(int G, const DecodeParams& p, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, cudaStream_t s, int* smem_out);
+int launch_decode_tc_d256(int G, const DecodeParams& p, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, cudaStream_t s, int* smem_out);
+// tcgen05 decode (bf16 cache, D = 128): maps[0..3] = K and V with TC_BOX_ROWS-row boxes, then
+// K and V with TC_FULL_ROWS-row boxes (whole 128-token tiles).
+int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                           int* smem_out);
+constexpr int TC_BOX_ROWS = 32;
+constexpr int TC_FULL_ROWS = 128;
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s);
 int launch_append(const CopyParams& p, cudaStream_t s);
 int launch_prefill(const CopyParams& p, cudaStream_t s);

@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
         "kvc_set_ctas": (I, [P, I]),
         "kvc_get_ctas": (I, [P]),
         "kvc_set_combine_mode": (I, [P, I]),
+        "kvc_set_math": (I, [P, I]),
+        "kvc_get_math": (I, [P]),
         "kvc_get_shape": (I, [P] + [ctypes.POINTER(I)] * 7),
         "kvc_plan_cta_of": (I, [I64, I64, I]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
@@ -170,6 +172,14 @@ def kvc_set_combine_mode(h, mode) -> None:
     _check(load().kvc_set_combine_mode(h, mode), "kvc_set_combine_mode")
 
 
+def kvc_set_math(h, mode) -> None:
+    _check(load().kvc_set_math(h, mode), "kvc_set_math")
+
+
+def kvc_get_math(h) -> int:
+    return int(load().kvc_get_math(h))
+
+
 def kvc_get_shape(h) -> dict:
     vals = [ctypes.c_int() for _ in range(7)]
     _check(load().kvc_get_shape(h, *[ctypes.byref(v) for v in vals]), "kvc_get_shape")
@@ -245,6 +255,12 @@ class KVCache:
 
     def set_combine_mode(self, mode):
         kvc_set_combine_mode(self.h, mode)
+
+    def set_math(self, mode):
+        kvc_set_math(self.h, mode)
+
+    def math(self) -> int:
+        return kvc_get_math(self.h)
 
 
 def _wrap_device(ptr: int, shape, dtype):

@@ -54,10 +54,10 @@ class Case:
         return {k: getattr(self, k).to(dev) for k in ("K", "V", "q", "k_new", "v_new", "lens_pre", "lens")}
 
 
-def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what=""):
+def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what="", tight=True):
     """The tolerance of the decode path: fp32 max abs <= 1e-5; bf16 max abs <= 2e-2 and
-    ||got - ref||_2 / ||ref||_2 <= 1e-2.  Also a tight check: within one bf16 ulp (fp32: 1e-6
-    relative) of the exact value, which the fp32 accumulation must meet."""
+    ||got - ref||_2 / ||ref||_2 <= 1e-2.  With `tight` (ref exact, e.g. the oracle's fp64) also:
+    every bf16 output within one bf16 ulp of ref, which fp32 accumulation must meet."""
     g = got.float().cpu().numpy().astype(np.float64)
     err = np.abs(g - ref)
     mx = float(err.max()) if err.size else 0.0
@@ -66,6 +66,8 @@ def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what=""):
         return mx, 0.0
     rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
     assert mx <= 2e-2 and rel <= 1e-2, f"{what}: max abs {mx:.3e} rel {rel:.3e}"
+    if not tight:
+        return mx, rel
     tight = np.abs(ref) * 2.0 ** -8 + 1e-6
     bad = np.argwhere(err > tight)
     assert bad.size == 0, f"{what}: {len(bad)} outputs beyond one bf16 ulp, first {bad[:3].tolist()}"

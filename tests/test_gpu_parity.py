@@ -24,13 +24,18 @@ def _built():
     torch.cuda.init()
 
 
-def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0):
+def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0, math=0):
     c = kvc.KVCache(layers, case.B, case.H_q, case.H_kv, case.D, T_max,
                     "bf16" if case.dtype == torch.bfloat16 else "f32")
     try:
         if ctas:
             c.set_ctas(ctas)
         c.set_combine_mode(mode)
+        c.set_math(math)
+        if math:
+            assert c.math() == math
+        elif case.dtype == torch.bfloat16 and case.D == 128:
+            assert c.math() == 3  # bf16 caches with D = 128 default to the tcgen05 kernel
         d = case.to_device()
         out = torch.full((case.B, case.H_q, case.D), float("nan"), dtype=case.dtype, device="cuda")
         c.prefill_write(layer, d["K"], d["V"], d["lens_pre"])
@@ -47,21 +52,28 @@ def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0):
         c.close()
 
 
-@pytest.mark.parametrize("dtype,D", SHAPES)
+# bf16 runs every kernel that supports the shape: tcgen05 (3, D = 128), warp MMA (2), CUDA
+# cores (1); fp32 is CUDA cores only
+PATHS = [(dt, D, m) for dt, D in SHAPES
+         for m in (((3, 2, 1) if D == 128 else (2, 1)) if dt == "bf16" else (0,))]
+
+
+@pytest.mark.parametrize("dtype,D,math", PATHS)
 @pytest.mark.parametrize("G", GROUPS)
-def test_decode_matches_oracle(dtype, D, G):
+def test_decode_matches_oracle(dtype, D, math, G):
     H_kv = 2
     case = Case(100 + G + D, 3, G * H_kv, H_kv, D, [0, 37, 611], dtype)
     T_max = 640
-    out, _, _ = _run(case, T_max)
-    check_close(out, case.oracle_out(T_max), case.dtype, f"{dtype} D={D} G={G}")
+    out, _, _ = _run(case, T_max, math=math)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"{dtype} D={D} G={G} math={math}")
 
 
+@pytest.mark.parametrize("math", [1, 2, 3])
 @pytest.mark.parametrize("fused", [True, False])
-def test_append_is_bit_exact_and_leaves_other_slots(fused):
+def test_append_is_bit_exact_and_leaves_other_slots(fused, math):
     case = Case(7, 4, 8, 2, 128, [5, 0, 63, 64], "bf16")
     T_max = 80
-    _, Kg, Vg = _run(case, T_max, fused=fused)
+    _, Kg, Vg = _run(case, T_max, fused=fused, math=math)
     Kc, Vc = case.oracle_cache(T_max)
     assert np.array_equal(host_bits(Kg), Kc)
     assert np.array_equal(host_bits(Vg), Vc)
@@ -111,14 +123,15 @@ def test_worked_example_through_the_cache():
         c.close()
 
 
+@pytest.mark.parametrize("math", [1, 2, 3])
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 152, 600])
-def test_split_t_any_split_matches(ctas, mode):
+def test_split_t_any_split_matches(ctas, mode, math):
     # one long and one 1-token stream per KV head; every split count and both merge paths
     case = Case(55, 2, 8, 2, 128, [1500, 0], "bf16")
     T_max = 1600
-    out, _, _ = _run(case, T_max, ctas=ctas, mode=mode)
-    check_close(out, case.oracle_out(T_max), case.dtype, f"ctas={ctas} mode={mode}")
+    out, _, _ = _run(case, T_max, ctas=ctas, mode=mode, math=math)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"ctas={ctas} mode={mode} math={math}")
 
 
 @pytest.mark.parametrize("ctas", [1, 5, 64])
@@ -129,19 +142,22 @@ def test_split_t_fp32_is_tight(ctas):
     check_close(out, case.oracle_out(T_max), case.dtype, f"fp32 MQA ctas={ctas}")
 
 
-def test_maximum_length_and_single_token():
+@pytest.mark.parametrize("math", [1, 2, 3])
+def test_maximum_length_and_single_token(math):
     case = Case(57, 2, 4, 1, 128, [255, 0], "bf16")  # lens = [T_max, 1]
-    out, _, _ = _run(case, 256)
+    out, _, _ = _run(case, 256, math=math)
     check_close(out, case.oracle_out(256), case.dtype, "T_max edge")
     # a 1-token history returns v_new exactly (softmax of one score is 1)
     assert torch.equal(out[1].cpu(), case.v_new[1, 0].expand(4, 128))
 
 
-def test_invalid_lengths_flag_and_zero_rows():
+@pytest.mark.parametrize("math", [1, 2, 3])
+def test_invalid_lengths_flag_and_zero_rows(math):
     B, H_q, H_kv, D, T_max = 4, 8, 2, 128, 64
     case = Case(58, B, H_q, H_kv, D, [10, 20, 30, 40], "bf16")
     c = kvc.KVCache(1, B, H_q, H_kv, D, T_max, "bf16")
     try:
+        c.set_math(math)
         d = case.to_device()
         c.prefill_write(0, d["K"], d["V"], d["lens_pre"])
         bad = torch.tensor([11, 0, 31, T_max + 5], dtype=torch.int32, device="cuda")
@@ -162,13 +178,15 @@ def test_invalid_lengths_flag_and_zero_rows():
         c.close()
 
 
-def test_repeated_steps_reuse_workspace():
+@pytest.mark.parametrize("math", [1, 2, 3])
+def test_repeated_steps_reuse_workspace(math):
     # the arrival counters must be back at zero after every call
     case = Case(59, 2, 16, 2, 128, [3000, 2999], "bf16")
     T_max = 3001
     c = kvc.KVCache(1, 2, 16, 2, 128, T_max, "bf16")
     try:
         c.set_combine_mode(0)
+        c.set_math(math)
         d = case.to_device()
         c.prefill_write(0, d["K"], d["V"], d["lens_pre"])
         ref = case.oracle_out(T_max)

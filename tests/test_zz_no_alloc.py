@@ -51,7 +51,10 @@ def test_noalloc_matches_handle_path_twice(dtype):
                                         d["q"], out, d["lens"], err)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
-            check_close(out, ref.double().cpu().numpy(), case.dtype, f"noalloc {dtype} B={case.B}")
+            # both outputs are rounded results, so compare with the tolerance itself (the
+            # one-ulp-of-exact bar applies to comparisons against the oracle)
+            check_close(out, ref.double().cpu().numpy(), case.dtype, f"noalloc {dtype} B={case.B}",
+                        tight=False)
         finally:
             c.close()
 
