@@ -13,8 +13,8 @@
 //   registers with the online-softmax rescale.  S^T, O^T and P are double-buffered so MMA1 of
 //   tile k+1 overlaps the softmax of tile k.
 // N = the query-head group padded to at least 16 (tcgen05 needs N % 16 == 0 at M = 128); the
-// padded q rows are zero.  P is stored as P_hi + P_lo (two bf16 terms) so the weights keep
-// fp32-level accuracy; MMA2 runs once per term.  Everything the tensor cores read is in the
+// padded q rows are zero.  P is stored as P_hi + P_lo (two bf16 terms, stacked as 2N operand
+// columns of one MMA2) so the weights keep fp32-level accuracy while V is read once.  Everything the tensor cores read is in the
 // 128-byte-swizzled K-major or MN-major canonical layout: K/V tiles arrive that way from TMA
 // tensor copies (boxes of 64 columns x 32 rows), q and P are written that way by the threads.
 // HBM traffic is unchanged: every K/V byte once per step, shared by the whole group.
@@ -41,6 +41,11 @@ struct Tc5Cfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + QRAW_BYTES;
     static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128] operand
     static constexpr int OPB_BYTES = HALVES * OPB_BLOCK;
+    // P operand of MMA2: rows [0, N) = P_hi, rows [N, 2N) = P_lo (one MMA with N2 = 2N columns);
+    // PBLOCK = one 64-token column block of it, PBUF = one whole 128-token buffer
+    static constexpr int N2 = 2 * N;
+    static constexpr int PBLOCK = N2 * 128;
+    static constexpr int PBUF = (TT / 64) * PBLOCK;
     static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
     static constexpr int MERGE_FLOATS = G * (D + 2);
     static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
@@ -49,12 +54,13 @@ struct Tc5Cfg {
     static constexpr int MISC_BYTES = 256;
     static constexpr int ALIGN_PAD = 1024;
     static constexpr int BUDGET = 232448;               // opt-in maximum per CTA (227 KB)
-    static constexpr int FIXED = 5 * OPB_BYTES + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
+    static constexpr int FIXED = OPB_BYTES + 2 * PBUF + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
                                  MISC_BYTES + ALIGN_PAD;
     static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NST = NST_A > 4 ? 4 : NST_A;
     static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
-    static constexpr int TMEM_COLS = 4 * N <= 32 ? 32 : (4 * N <= 64 ? 64 : (4 * N <= 128 ? 128 : 256));
+    // S^T buffers [0, N) and [N, 2N); O^T buffers (hi and lo halves) [2N, 4N) and [4N, 6N)
+    static constexpr int TMEM_COLS = 6 * N <= 32 ? 32 : (6 * N <= 64 ? 64 : (6 * N <= 128 ? 128 : 256));
     static_assert(NST >= 2, "ring too shallow");
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
@@ -191,8 +197,8 @@ __global__ void __launch_bounds__(192, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = smem;
     unsigned char* qsw = ring + NST * C::STAGE_BYTES;        // q, [N][D] K-major swizzled
-    unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][hi, lo][N][TT]
-    float* merge = reinterpret_cast<float*>(pbuf + 4 * C::OPB_BYTES);
+    unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][2 blocks][2N rows][128 B]
+    float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
     int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
     float* red = reinterpret_cast<float*>(prefix + MAX_B + 1);  // [4][N]
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(red + 4 * N);
@@ -207,10 +213,44 @@ __global__ void __launch_bounds__(192, 1)
     int* last_flag = issued + NST + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(issued + NST + 2);
     int* mma_issued = issued + NST + 3;                      // MMA2 commits issued (abort drain)
+    // (append_bar follows at the next 8-byte boundary)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.B, H_kv = p.H_kv;
     const size_t row_elems_q = (size_t)H_kv * G * D;
+    uint64_t* append_bar = reinterpret_cast<uint64_t*>(
+        (reinterpret_cast<uintptr_t>(mma_issued + 1) + 7) & ~uintptr_t(7));
+
+    // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
+    // CTAs take SMs as ours exit) but waits in griddepcontrol.wait until this grid is complete.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 32) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+            issued[s] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
+        }
+        mbar_init(append_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        *mma_issued = 0;
+        fence_mbar_init();
+    }
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKf)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVf)) : "memory");
+    }
+    // everything below may read what earlier work on the stream wrote
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         int64_t carry = 0;
@@ -231,27 +271,6 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (lane == 0) prefix[0] = 0;
     }
-    if (tid == 32) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
-            issued[s] = 0;
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&o_full[i], 1);
-            mbar_init(&o_empty[i], 4);
-        }
-        *abort_flag = 0;
-        *last_flag = 0;
-        *mma_issued = 0;
-        fence_mbar_init();
-    }
-    // padded q rows and P rows of padded heads stay zero for the whole kernel
-    for (int i = tid; i < 5 * C::OPB_BYTES / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
@@ -272,50 +291,13 @@ __global__ void __launch_bounds__(192, 1)
     if ((int64_t)blockIdx.x >= P) return;
     const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
     if (r0 >= r1) return;
-
-    // ---- fused append (see kvc_decode_tc.cuh): new rows into the cache before any tensor copy
-    if (p.k_new != nullptr && warp == 0) {
-        SegIter it;
-        it.init(prefix, B, H_kv, r0, r1);
-        while (it.valid) {
-            if (it.t1 == it.L) {
-                const size_t unit = (size_t)it.b * H_kv + it.h;
-                const size_t dst = (unit * p.T_max + (size_t)(it.L - 1)) * C::ROWB;
-                const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + unit * C::ROWB);
-                const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + unit * C::ROWB);
-                uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + dst);
-                uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.V)) + dst);
-                for (int v = lane; v < C::ROWB / 16; v += 32) {
-                    kd[v] = __ldg(ksrc + v);
-                    vd[v] = __ldg(vsrc + v);
-                }
-            }
-            it.next();
-        }
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        __syncwarp();
-    }
-    // ---- tensor memory: S^T buffers at columns [0, N) and [N, 2N); O^T at [2N, 3N) and [3N, 4N)
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(tmem_slot)),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc5_fence_before();
-    __syncthreads();
-    tc5_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const bool fused = p.k_new != nullptr;
     const uint32_t ring_s = smem_addr(ring);
+    uint32_t tmem = 0;
 
     if (warp == 0) {
         // ======================================================= producer
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKf)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVf)) : "memory");
             const uint64_t pol = policy_evict_first();
             TileCursor<TT> pref;
             pref.init(prefix, B, H_kv, r0, r1);
@@ -323,6 +305,10 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t ph = 0;
             while (pref.valid) {
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err)) break;
+                // a tile that holds a stream's new token waits for the fused append's writes
+                if (fused && pref.t + pref.n() == pref.it.L &&
+                    !mbar_wait(append_bar, 0u, abort_flag, p.err))
+                    break;
                 issue_tile_tc5<C, TT>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf);
                 issued[s] += 1;
                 pref.advance();
@@ -331,8 +317,18 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         // ======================================================= MMA issue
+        // tensor memory: S^T buffers at columns [0, N) and [N, 2N); O^T at [2N, 3N) and [3N, 4N)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc5_fence_before();
+        named_bar_sync(2, 160);
+        tc5_fence_after();
+        tmem = *tmem_slot;
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
-        constexpr uint32_t IDESC2 = instr_desc_bf16(128, N, 1, 0);  // V read MN-major x P (K-major)
+        constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, 0);  // V read MN-major x [P_hi; P_lo]
         const uint32_t qsw_s = smem_addr(qsw), pbuf_s = smem_addr(pbuf);
         const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, 1024u);                    // + stage, block, k-step
         const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, (uint32_t)C::HALF_BYTES, 1024u);
@@ -352,16 +348,14 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
                 if (alive && lane == 0) {
                     tc5_fence_after();
-                    const uint32_t tO = tmem + (uint32_t)((2 + (j & 1)) * N);
-                    const uint32_t pb = (uint32_t)((j & 1) * 2 * C::OPB_BYTES);
+                    const uint32_t tO = tmem + (uint32_t)(2 * N + (j & 1) * C::N2);
+                    const uint32_t pb = (uint32_t)((j & 1) * C::PBUF);
 #pragma unroll
-                    for (int term = 0; term < 2; ++term)
-#pragma unroll
-                        for (int kk = 0; kk < TS; ++kk) {
-                            const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2048);
-                            const uint32_t poff = pb + (uint32_t)(term * C::OPB_BYTES + (kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
-                            tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, (term > 0 || kk > 0) ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < TS; ++kk) {
+                        const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2048);
+                        const uint32_t poff = pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
+                        tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
+                    }
                     tc5_commit(&o_full[j & 1]);
                     tc5_commit(&empty_bar[s_prev]);  // K/V of the stage are consumed
                     *mma_issued += 1;
@@ -404,6 +398,38 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ======================================================= softmax + accumulate
+        // zero the padded q rows and the P rows of padded heads (they stay zero), and write the
+        // fused append's new rows; then meet the MMA warp (named barrier 2) for the TMEM base
+        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += 128)
+            reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (warp == 2 && fused) {
+            SegIter it;
+            it.init(prefix, B, H_kv, r0, r1);
+            while (it.valid) {
+                if (it.t1 == it.L) {
+                    const size_t unit = (size_t)it.b * H_kv + it.h;
+                    const size_t dst = (unit * p.T_max + (size_t)(it.L - 1)) * C::ROWB;
+                    const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + unit * C::ROWB);
+                    const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + unit * C::ROWB);
+                    uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + dst);
+                    uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.V)) + dst);
+                    for (int v = lane; v < C::ROWB / 16; v += 32) {
+                        kd[v] = __ldg(ksrc + v);
+                        vd[v] = __ldg(vsrc + v);
+                    }
+                }
+                it.next();
+            }
+            // order these generic-proxy writes before the producer's tensor copies of the rows
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(append_bar);
+        }
+        fence_async_smem();
+        tc5_fence_before();
+        named_bar_sync(2, 160);
+        tc5_fence_after();
+        tmem = *tmem_slot;
         const int q4 = warp & 3;            // tensor-memory lane quadrant of this warp
         const int row = q4 * 32 + lane;     // token of S^T rows / element d of O^T rows
         const int gt = tid - 64;            // 0..127 within the group
@@ -416,16 +442,18 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t ph = 0;
         bool alive = true;
         auto absorb = [&](int j, const float* a) {
-            // O^T(j) into the accumulator: o = o * alpha_j + O^T(j)[row, :]
+            // O^T(j) into the accumulator: o = o * alpha_j + (O^T_hi + O^T_lo)(j)[row, :]
             alive = alive && mbar_wait(&o_full[j & 1], (j >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
-            float v[16];
+            const uint32_t ob = tmem + (uint32_t)(2 * N + (j & 1) * C::N2) + lane_off;
+            float hi[16], lo[16];
 #pragma unroll
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                tc5_ld16(tmem + (uint32_t)((2 + (j & 1)) * N + c0) + lane_off, v);
+            for (int c0 = 0; c0 < N && c0 < G; c0 += 16) {
+                tc5_ld16(ob + c0, hi);
+                tc5_ld16(ob + N + c0, lo);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    if (c0 + i < G) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], v[i]) : o[c0 + i];
+                    if (c0 + i < G) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], hi[i] + lo[i]) : o[c0 + i];
             }
             tc5_fence_before();
             __syncwarp();
@@ -486,10 +514,10 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 named_bar_sync(1, 128);  // red is reused
             }
-            // ---- P(k) = P_hi + P_lo, K-major swizzled rows h, column (token) row
+            // ---- P(k) = P_hi + P_lo: rows h (hi) and N + h (lo) of the K-major swizzled operand,
+            // column = this thread's token
             {
-                unsigned char* pb = pbuf + (k & 1) * 2 * C::OPB_BYTES;
-                const uint32_t coff = (uint32_t)(row >> 6) * C::OPB_BLOCK;
+                unsigned char* pb = pbuf + (k & 1) * C::PBUF + (row >> 6) * C::PBLOCK;
                 const int chunk = (row & 63) >> 3, e = row & 7;
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -497,9 +525,9 @@ __global__ void __launch_bounds__(192, 1)
                     l[h] += pv;
                     const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
                     const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
-                    const uint32_t off = coff + h * 128 + (((chunk ^ (h & 7)) << 4) | (e << 1));
-                    *reinterpret_cast<__nv_bfloat16*>(pb + off) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(pb + C::OPB_BYTES + off) = lo;
+                    const uint32_t off = (((chunk ^ (h & 7)) << 4) | (e << 1));  // N % 8 == 0
+                    *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + off) = hi;
+                    *reinterpret_cast<__nv_bfloat16*>(pb + (N + h) * 128 + off) = lo;
                 }
             }
             // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2)

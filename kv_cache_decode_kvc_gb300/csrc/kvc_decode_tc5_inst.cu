@@ -16,7 +16,21 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
         attr_set = true;
     }
     if (smem_out) *smem_out = C::SMEM;
-    decode_tc5_kernel<G><<<p.P, C::NTHREADS, C::SMEM, s>>>(p, maps[0], maps[1], maps[2], maps[3]);
+    // programmatic stream serialisation: this grid may be scheduled while the previous kernel on
+    // the stream finishes; the kernel's griddepcontrol.wait holds every read of stream data
+    // until that kernel is complete and its writes are visible
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.P);
+    cfg.blockDim = dim3(C::NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc5_kernel<G>, p, maps[0], maps[1], maps[2], maps[3]);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 
