@@ -304,8 +304,14 @@ def run_ours(args, w):
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
     alg_bytes_launch = (w.kv_read_bytes_per_layer() + 2 * B * Hq * D * s  # q read, out written
                         + 4 * B * Hkv * D * s + 4 * B)                    # k/v new read + written, lens
-    achieved = alg_bytes_launch / (launch_ms * 1e-3) / 1e9
+    # average launch duration over the timed region (graph replay, gaps included)
+    region_launch_ms = ms_local / launches_per_step
+    achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
     traffic = traffic_from_profiles(kernel_source_hash())
+    path = kvc.kvc_get_math(cache.h)
+    kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
+                   2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
+                   3: f"decode_tc5_kernel<{w.G}> (tcgen05)"}[path]
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     h_q = [i[0].cpu().pin_memory() for i in ins]
@@ -378,7 +384,8 @@ def run_ours(args, w):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                         "kernel": "decode_kernel<bf16,128,4>", "launch_us": round(launch_ms * 1e3, 2),
+                         "kernel": kernel_name, "launch_us": round(region_launch_ms * 1e3, 2),
+                         "launch_us_eager_events": round(launch_ms * 1e3, 2),
                          "alg_bytes_per_launch": alg_bytes_launch},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
