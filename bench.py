@@ -137,7 +137,7 @@ def oracle_sample(w, budget_s: float, threads: int, max_layers: int | None = Non
 
 
 def run_reference(args, w):
-    rank = _env_int("RANK", 0)
+    rank = _env_int("RANK", 0)  # under torchrun only rank 0 runs the CPU arm
     if rank != 0:
         return 0
     threads = os.cpu_count() or 1
@@ -196,11 +196,10 @@ def run_ours(args, w):
     import torch.distributed as dist
 
     from kv_cache_decode_kvc_gb300 import kvc
+    from kv_cache_decode_kvc_gb300.replicas import env_rank, max_over_ranks, replica_seed, whole_job_rate
     from kv_cache_decode_kvc_gb300.workloads import fill_layer, step_inputs
 
-    world = _env_int("WORLD_SIZE", 1)
-    rank = _env_int("RANK", 0)
-    local = _env_int("LOCAL_RANK", 0)
+    rank, local, world = env_rank()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -211,7 +210,7 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    seed = w.seed + 7919 * rank  # each replica decodes its own batch (weak scaling)
+    seed = replica_seed(w.seed, rank)  # each replica decodes its own batch (weak scaling)
     L = w.layers
     cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
     t_fill = time.perf_counter()
@@ -273,17 +272,13 @@ def run_ours(args, w):
     barrier()
     clock_info = clocks.stop()
     ms_local = ev0.elapsed_time(ev1) / args.steps
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms_local, world, dev)
     st, detail = cache.last_error(sptr)
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
 
     kv_bytes_step = L * w.kv_read_bytes_per_layer()
-    gbs = world * kv_bytes_step / (ms * 1e-3) / 1e9
+    gbs = whole_job_rate(world, kv_bytes_step, ms)
     peak, peak_kind = measured_peaks()
 
     # ---- per-launch durations of the decode kernel (events around each launch, same stream)
@@ -348,11 +343,8 @@ def run_ours(args, w):
         stream.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_gbs = world * kv_bytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_gbs = whole_job_rate(world, kv_bytes_step, e2e_ms)
     st, detail = cache.last_error(sptr)
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the e2e region: status {st} detail {detail:#x}")
