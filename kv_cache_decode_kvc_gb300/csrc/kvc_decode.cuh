@@ -226,7 +226,8 @@ __device__ __forceinline__ void group_sync() {
 // Merges the partial states (slots c + unit, c in [cfirst, clast]) of one stream into its
 // output, o = sum_c w_c o_c / sum_c w_c l_c with w_c = 2^(m_c - M), M = max_c m_c.  Per-head
 // weights are formed once in shared memory (`scratch`, at least G * (D + 2) floats); the
-// output loop then issues its loads four segments at a time.  Run by NT threads.
+// output loop then issues 16-byte loads, many per thread at a time.  Run by NT threads.  The
+// partial outputs of a slot are 16-byte aligned (G * D is a multiple of 4).
 template <typename T, int G, int D, int NT, int BAR>
 __device__ __forceinline__ void merge_partials(const DecodeParams& p, float* scratch, size_t unit,
                                                int64_t cfirst, int64_t clast, int tid) {
@@ -255,22 +256,50 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, float* scr
             for (int c = 0; c < nseg; ++c) sm[h * CAP + c] *= inv;
         }
         group_sync<BAR, NT>();
-        for (int idx = tid; idx < G * D; idx += NT) {
-            const int h = idx / D;
-            const float* po = p.part_o + (size_t)(cfirst + (int64_t)unit) * G * D + idx;
-            const size_t stride = (size_t)G * D;
-            float acc = 0.f;
-            int c = 0;
-            for (; c + 4 <= nseg; c += 4) {
-                const float v0 = __ldcg(po + (size_t)c * stride), v1 = __ldcg(po + (size_t)(c + 1) * stride);
-                const float v2 = __ldcg(po + (size_t)(c + 2) * stride), v3 = __ldcg(po + (size_t)(c + 3) * stride);
-                acc = fmaf(sm[h * CAP + c], v0, acc);
-                acc = fmaf(sm[h * CAP + c + 1], v1, acc);
-                acc = fmaf(sm[h * CAP + c + 2], v2, acc);
-                acc = fmaf(sm[h * CAP + c + 3], v3, acc);
+        // outputs in groups of 4 (one 16-byte load per segment); UNR groups per thread and up to
+        // 4 segments per batch, every load of a batch issued before any is used
+        constexpr int V4 = G * D / 4;
+        constexpr int UNR = 4;
+        const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)(cfirst + (int64_t)unit) * G * D);
+        for (int base = tid; base < V4; base += NT * UNR) {
+            float4 acc[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < nseg; c0 += 4) {
+                float4 v[UNR][4];
+#pragma unroll
+                for (int u = 0; u < UNR; ++u)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int i4 = base + u * NT;
+                        v[u][j] = (i4 < V4 && c0 + j < nseg) ? __ldcg(po4 + (size_t)(c0 + j) * V4 + i4)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int u = 0; u < UNR; ++u) {
+                    int h = ((base + u * NT) * 4) / D;
+                    h = h < G ? h : G - 1;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float w = (c0 + j < nseg) ? sm[h * CAP + c0 + j] : 0.f;
+                        acc[u].x = fmaf(w, v[u][j].x, acc[u].x);
+                        acc[u].y = fmaf(w, v[u][j].y, acc[u].y);
+                        acc[u].z = fmaf(w, v[u][j].z, acc[u].z);
+                        acc[u].w = fmaf(w, v[u][j].w, acc[u].w);
+                    }
+                }
             }
-            for (; c < nseg; ++c) acc = fmaf(sm[h * CAP + c], __ldcg(po + (size_t)c * stride), acc);
-            Elem<T>::store(p.out, unit * G * D + idx, acc);
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int i4 = base + u * NT;
+                if (i4 < V4) {
+                    const size_t o = unit * G * D + (size_t)i4 * 4;
+                    Elem<T>::store(p.out, o, acc[u].x);
+                    Elem<T>::store(p.out, o + 1, acc[u].y);
+                    Elem<T>::store(p.out, o + 2, acc[u].z);
+                    Elem<T>::store(p.out, o + 3, acc[u].w);
+                }
+            }
         }
     } else {
         // many segments (few, very long streams): straightforward two passes per output

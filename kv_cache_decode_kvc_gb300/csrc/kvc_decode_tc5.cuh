@@ -5,7 +5,8 @@
 // Same computation, split-T partition and merging as decode_kernel (kvc_decode.cuh): for every
 // query head j of sequence b, o = softmax_t(q . K_t / sqrt(D)) V over t < lens[b]
 // ("11.7 KV Cache：形状、显存与带宽" §2.2; head map of "第 1 周 · Day 4：KV Cache 与 MQA /
-// GQA" §3.4).  A CTA (producer warp, MMA warp, 4 softmax warps) consumes 128-token tiles:
+// GQA" §3.4).  A CTA (producer warp, MMA warp, 4 softmax warps, 2 epilogue warps) consumes
+// 128-token tiles:
 //   MMA1  S^T[128 tok x N]  = K[128 x D] . Q^T[D x N]   A = K tile (K-major), B = q (K-major)
 //   softmax: a thread owns one token (one tensor-memory lane) and all N head columns
 //   MMA2  O^T[D x N]        = V^T[D x 128] . P^T[128 x N]  A = V tile read MN-major, B = P
@@ -32,7 +33,8 @@ struct Tc5Cfg {
     static constexpr int ROWB = D * 2;
     static constexpr int HALVES = D / 64;               // 128-byte column blocks
     static constexpr int NW = 4;                        // softmax warps (+ producer + MMA warp)
-    static constexpr int NTHREADS = 192;
+    static constexpr int NEPI = 2;                      // segment-epilogue warps
+    static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
     static constexpr int TT = 128;                      // tokens per tile = MMA M
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
     static constexpr int HALF_BYTES = TT * 128;         // one column block of a K or V tile
@@ -179,11 +181,13 @@ __device__ __forceinline__ bool softmax_group_any(bool pred) {
 }
 
 // Warp roles: warp 0 issues the tensor copies (producer), warp 1 issues the MMAs, warps 2-5 run
-// the softmax, write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane).
+// the softmax, write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane),
+// warps 6-7 finish segments (output or partial state, and the merge of a stream whose last
+// segment this CTA completes) while the next segment streams.
 // Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
 // the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
 template <int G>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     decode_tc5_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKf,
@@ -208,7 +212,9 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* p_full = s_empty + 2;
     uint64_t* o_full = p_full + 2;
     uint64_t* o_empty = o_full + 2;
-    int* issued = reinterpret_cast<int*>(o_empty + 2);       // [NST]
+    uint64_t* m_full = o_empty + 2;       // merge buffer written (softmax warps -> epilogue warps)
+    uint64_t* m_empty = m_full + 1;       // merge buffer consumed
+    int* issued = reinterpret_cast<int*>(m_empty + 1);       // [NST]
     volatile int* abort_flag = issued + NST;
     int* last_flag = issued + NST + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(issued + NST + 2);
@@ -237,6 +243,8 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&o_full[i], 1);
             mbar_init(&o_empty[i], 4);
         }
+        mbar_init(m_full, C::NW * 32);
+        mbar_init(m_empty, C::NEPI * 32);
         mbar_init(append_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
@@ -396,6 +404,23 @@ __global__ void __launch_bounds__(192, 1)
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
+    } else if (warp >= 2 + C::NW) {
+        // ======================================================= segment epilogues
+        // For each segment of this CTA, in order: wait for the softmax warps' final state in
+        // `merge`, write the output or the partial state, merge the stream if this CTA is the
+        // last to finish it, release `merge`.  Runs beside the next segment's tiles.
+        const int et = tid - (2 + C::NW) * 32;
+        SegIter it;
+        it.init(prefix, B, H_kv, r0, r1);
+        bool ok = true;
+        for (int sg = 0; it.valid; ++sg) {
+            ok = ok && mbar_wait(m_full, (uint32_t)(sg & 1), abort_flag, p.err);
+            if (ok)
+                finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
+                                                              W, P, last_flag, et);
+            mbar_arrive(m_empty);
+            it.next();
+        }
     } else {
         // ======================================================= softmax + accumulate
         // zero the padded q rows and the P rows of padded heads (they stay zero), and write the
@@ -438,7 +463,7 @@ __global__ void __launch_bounds__(192, 1)
         float o[G], m[G], l[G], alpha[G], alpha_prev[G];
         TileCursor<TT> cur;
         cur.init(prefix, B, H_kv, r0, r1);
-        int s = 0;
+        int s = 0, sg = 0;
         uint32_t ph = 0;
         bool alive = true;
         auto absorb = [&](int j, const float* a) {
@@ -460,7 +485,6 @@ __global__ void __launch_bounds__(192, 1)
             if (lane == 0) mbar_arrive(&o_empty[j & 1]);
         };
         for (int k = 0; cur.valid; ++k) {
-            const size_t unit = (size_t)cur.it.b * H_kv + cur.it.h;
             const int n = cur.n();
             const bool first = cur.first(), last = cur.last();
             if (first) {
@@ -558,6 +582,8 @@ __global__ void __launch_bounds__(192, 1)
                     if (lane == 0) red[q4 * N + h] = s_;
                 }
                 named_bar_sync(1, 128);
+                // hand the segment's state to the epilogue warps (merge: [G][D + 2])
+                alive = alive && mbar_wait(m_empty, (uint32_t)(sg & 1) ^ 1u, abort_flag, p.err);
 #pragma unroll
                 for (int h = 0; h < G; ++h) merge[h * (D + 2) + row] = o[h];
                 if (gt < G) {
@@ -567,8 +593,8 @@ __global__ void __launch_bounds__(192, 1)
                     merge[gt * (D + 2) + D] = m[gt];
                     merge[gt * (D + 2) + D + 1] = s_;
                 }
-                named_bar_sync(1, 128);
-                finish_segment<T, G, D, C::HS, 1, 4, 1>(p, merge, cur.it, unit, W, P, last_flag, gt);
+                mbar_arrive(m_full);
+                ++sg;
             }
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
