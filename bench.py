@@ -213,6 +213,9 @@ def run_ours(args, w):
     seed = replica_seed(w.seed, rank)  # each replica decodes its own batch (weak scaling)
     L = w.layers
     cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
+    # the launch preceding each decode launch is the previous layer's decode step, which writes
+    # neither lens nor this layer's history rows: early history loads are allowed
+    cache.set_launch_overlap(0 if args.no_overlap else 1)
     t_fill = time.perf_counter()
     for layer in range(L):
         fill_layer(cache, layer, w, seed=seed)
@@ -372,7 +375,8 @@ def run_ours(args, w):
                        "kv_bytes_per_step": kv_bytes_step,
                        "l2": "inputs larger than L2 (each layer has its own cache; "
                              f"{kv_bytes_step / 1e9:.1f} GB read per step)",
-                       "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
+                       "cuda_graph": graph is not None, "launch_overlap": cache.launch_overlap(),
+                       "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
@@ -401,6 +405,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch overlap off: nothing is read before the preceding launch ends")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=None,

@@ -136,6 +136,20 @@ int kvc_set_combine_mode(kvc_t h, int mode);
 int kvc_set_math(kvc_t h, int mode);
 int kvc_get_math(kvc_t h);
 
+/* Launch overlap (default 0).  The tcgen05 attention kernel is launched with programmatic
+ * dependent launch: its CTAs may become resident while the preceding kernel on the stream is
+ * still finishing.  With 0 they read nothing before that kernel has completed.  With 1 they
+ * read lens[] and start loading the history rows [0, lens[b] - 1) of each stream before it has
+ * completed, and wait for it before touching anything else (q, k_new, v_new, the new row
+ * lens[b] - 1, outputs, workspace).  Set 1 only when the kernel launched just before on the
+ * stream writes neither lens nor those rows: e.g. a decode loop over layers where the
+ * preceding kernel is another layer's kvc_decode_step or a projection writing q / k_new /
+ * v_new.  Results are identical either way; only the start of each launch moves earlier.
+ * Not part of the pages' method (a scheduling choice of this implementation).  Other math
+ * paths ignore it.  Returns KVC_EINVAL for a value other than 0 or 1. */
+int kvc_set_launch_overlap(kvc_t h, int on);
+int kvc_get_launch_overlap(kvc_t h);
+
 /* Shape query: writes layers, B, H_q, H_kv, D, T_max, dtype (any pointer may be NULL). */
 int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
                   int* dtype);

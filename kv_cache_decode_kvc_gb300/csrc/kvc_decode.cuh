@@ -224,99 +224,79 @@ __device__ __forceinline__ void group_sync() {
 }
 
 // Merges the partial states (slots c + unit, c in [cfirst, clast]) of one stream into its
-// output, o = sum_c w_c o_c / sum_c w_c l_c with w_c = 2^(m_c - M), M = max_c m_c.  Per-head
-// weights are formed once in shared memory (`scratch`, at least G * (D + 2) floats); the
-// output loop then issues 16-byte loads, many per thread at a time.  Run by NT threads.  The
-// partial outputs of a slot are 16-byte aligned (G * D is a multiple of 4).
-template <typename T, int G, int D, int NT, int BAR>
-__device__ __forceinline__ void merge_partials(const DecodeParams& p, float* scratch, size_t unit,
-                                               int64_t cfirst, int64_t clast, int tid) {
+// output, o = sum_c w_c o_c / sum_c w_c l_c with w_c = 2^(m_c - M), M = max_c m_c.  A thread
+// owns groups of 4 consecutive outputs (one head); for up to 4 segments at a time it issues
+// every 16-byte partial-output load and 8-byte (max, denominator) load of its UNR groups before
+// using any, and folds them in with a running maximum, so a stream split over at most 4 CTAs
+// costs one round trip to L2 per UNR groups.  Run by NT threads.  Slots are 16-byte aligned
+// (G * D is a multiple of 4).
+template <typename T, int G, int D, int NT>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, size_t unit, int64_t cfirst,
+                                               int64_t clast, int tid) {
     const int nseg = (int)(clast - cfirst + 1);
-    constexpr int CAP = (D + 2) / 2;  // segments whose (max, denominator) fit the scratch
-    if (nseg <= CAP) {
-        float* sm = scratch;               // [G][CAP]: maxima, then weights
-        float* sl = scratch + G * CAP;     // [G][CAP]: denominators
-        for (int i = tid; i < G * nseg; i += NT) {
-            const int h = i / nseg, c = i - h * nseg;
-            const size_t sidx = (size_t)(cfirst + c + (int64_t)unit);
-            sm[h * CAP + c] = __ldcg(&p.part_ml[(sidx * G + h) * 2]);
-            sl[h * CAP + c] = __ldcg(&p.part_ml[(sidx * G + h) * 2 + 1]);
+    constexpr int V4 = G * D / 4;
+    constexpr int PER = (V4 + NT - 1) / NT;
+    constexpr int UMAX = NT >= 256 ? 2 : 4;  // fewer registers in the 8-warp CUDA-core kernel
+    constexpr int UNR = PER < UMAX ? PER : UMAX;
+    const size_t s0 = (size_t)(cfirst + (int64_t)unit);
+    const float4* po4 = reinterpret_cast<const float4*>(p.part_o + s0 * G * D);
+    const float2* pml = reinterpret_cast<const float2*>(p.part_ml + s0 * G * 2);
+    for (int base = tid; base < V4; base += NT * UNR) {
+        float4 acc[UNR];
+        float M[UNR], den[UNR];
+        int h[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            M[u] = -INFINITY;
+            den[u] = 0.f;
+            const int hh = ((base + u * NT) * 4) / D;
+            h[u] = hh < G ? hh : G - 1;
         }
-        group_sync<BAR, NT>();
-        for (int h = tid; h < G; h += NT) {
-            float M = -INFINITY;
-            for (int c = 0; c < nseg; ++c) M = fmaxf(M, sm[h * CAP + c]);
-            float den = 0.f;
-            for (int c = 0; c < nseg; ++c) {
-                const float w = (sm[h * CAP + c] == -INFINITY) ? 0.f : exp2f(sm[h * CAP + c] - M);
-                sm[h * CAP + c] = w;
-                den = fmaf(w, sl[h * CAP + c], den);
-            }
-            const float inv = 1.f / den;
-            for (int c = 0; c < nseg; ++c) sm[h * CAP + c] *= inv;
-        }
-        group_sync<BAR, NT>();
-        // outputs in groups of 4 (one 16-byte load per segment); UNR groups per thread and up to
-        // 4 segments per batch, every load of a batch issued before any is used
-        constexpr int V4 = G * D / 4;
-        constexpr int UNR = 4;
-        const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)(cfirst + (int64_t)unit) * G * D);
-        for (int base = tid; base < V4; base += NT * UNR) {
-            float4 acc[UNR];
+        for (int c0 = 0; c0 < nseg; c0 += 4) {
+            float4 v[UNR][4];
+            float2 ml[UNR][4];
 #pragma unroll
-            for (int u = 0; u < UNR; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c0 = 0; c0 < nseg; c0 += 4) {
-                float4 v[UNR][4];
+            for (int u = 0; u < UNR; ++u)
 #pragma unroll
-                for (int u = 0; u < UNR; ++u)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int i4 = base + u * NT;
-                        v[u][j] = (i4 < V4 && c0 + j < nseg) ? __ldcg(po4 + (size_t)(c0 + j) * V4 + i4)
-                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                for (int u = 0; u < UNR; ++u) {
-                    int h = ((base + u * NT) * 4) / D;
-                    h = h < G ? h : G - 1;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float w = (c0 + j < nseg) ? sm[h * CAP + c0 + j] : 0.f;
-                        acc[u].x = fmaf(w, v[u][j].x, acc[u].x);
-                        acc[u].y = fmaf(w, v[u][j].y, acc[u].y);
-                        acc[u].z = fmaf(w, v[u][j].z, acc[u].z);
-                        acc[u].w = fmaf(w, v[u][j].w, acc[u].w);
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = base + u * NT < V4 && c0 + j < nseg;
+                    v[u][j] = in ? __ldcg(po4 + (size_t)(c0 + j) * V4 + base + u * NT)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                    ml[u][j] = in ? __ldcg(pml + (size_t)(c0 + j) * G + h[u]) : make_float2(-INFINITY, 0.f);
                 }
-            }
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
-                const int i4 = base + u * NT;
-                if (i4 < V4) {
-                    const size_t o = unit * G * D + (size_t)i4 * 4;
-                    Elem<T>::store(p.out, o, acc[u].x);
-                    Elem<T>::store(p.out, o + 1, acc[u].y);
-                    Elem<T>::store(p.out, o + 2, acc[u].z);
-                    Elem<T>::store(p.out, o + 3, acc[u].w);
+                float mn = M[u];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mn = fmaxf(mn, ml[u][j].x);
+                if (mn == -INFINITY) continue;  // nothing valid yet
+                const float sc = (M[u] == -INFINITY) ? 0.f : exp2f(M[u] - mn);
+                acc[u].x *= sc; acc[u].y *= sc; acc[u].z *= sc; acc[u].w *= sc;
+                den[u] *= sc;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float w = (ml[u][j].x == -INFINITY) ? 0.f : exp2f(ml[u][j].x - mn);
+                    acc[u].x = fmaf(w, v[u][j].x, acc[u].x);
+                    acc[u].y = fmaf(w, v[u][j].y, acc[u].y);
+                    acc[u].z = fmaf(w, v[u][j].z, acc[u].z);
+                    acc[u].w = fmaf(w, v[u][j].w, acc[u].w);
+                    den[u] = fmaf(w, ml[u][j].y, den[u]);
                 }
+                M[u] = mn;
             }
         }
-    } else {
-        // many segments (few, very long streams): straightforward two passes per output
-        for (int idx = tid; idx < G * D; idx += NT) {
-            const int hg = idx / D;
-            float M = -INFINITY;
-            for (int64_t c = cfirst; c <= clast; ++c)
-                M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + unit) * G + hg) * 2]));
-            float num = 0.f, den = 0.f;
-            for (int64_t c = cfirst; c <= clast; ++c) {
-                const size_t sidx = (size_t)(c + unit);
-                const float mc = __ldcg(&p.part_ml[(sidx * G + hg) * 2]);
-                const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                num = fmaf(w, __ldcg(&p.part_o[sidx * G * D + idx]), num);
-                den = fmaf(w, __ldcg(&p.part_ml[(sidx * G + hg) * 2 + 1]), den);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int i4 = base + u * NT;
+            if (i4 < V4) {
+                const float inv = 1.f / den[u];
+                const size_t o = unit * G * D + (size_t)i4 * 4;
+                Elem<T>::store(p.out, o, acc[u].x * inv);
+                Elem<T>::store(p.out, o + 1, acc[u].y * inv);
+                Elem<T>::store(p.out, o + 2, acc[u].z * inv);
+                Elem<T>::store(p.out, o + 3, acc[u].w * inv);
             }
-            Elem<T>::store(p.out, unit * G * D + idx, num / den);
         }
     }
 }
@@ -364,7 +344,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
         group_sync<BAR, NW * 32>();
         if (*last_flag) {
             __threadfence();
-            merge_partials<T, G, D, NW * 32, BAR>(p, merge, unit, cfirst, clast, tid);
+            merge_partials<T, G, D, NW * 32>(p, unit, cfirst, clast, tid);
             if (tid == 0) p.counters[unit] = 0;  // every arrival is in: ready for next call
         }
     }

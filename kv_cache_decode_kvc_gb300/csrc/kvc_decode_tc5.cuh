@@ -127,13 +127,17 @@ __device__ __forceinline__ void tc5_ld16(uint32_t taddr, float (&v)[16]) {
 
 // Issues one tile: a full tile is one 128-row box per column block of K and of V (maps tmKf /
 // tmVf); a partial tile uses 32-row boxes (tmK / tmV), rows past the stream's end being loaded
-// and masked; the first tile of a segment also brings q.
+// and masked; the first tile of a segment also brings q.  `part` splits the issue in two for
+// tiles loaded before the preceding grid has finished: TILE_KV registers the K/V bytes on the
+// stage's barrier without arriving and starts the K/V copies; TILE_Q then adds q (first tile
+// of a segment) and arrives, so the stage cannot complete before q is in.
+enum { TILE_ALL = 0, TILE_KV = 1, TILE_Q = 2 };
 template <class C, int TT>
 __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const TileCursor<TT>& c,
                                                uint32_t ring, uint64_t* full_bar, int stage,
                                                uint64_t pol, const CUtensorMap* tmK,
                                                const CUtensorMap* tmV, const CUtensorMap* tmKf,
-                                               const CUtensorMap* tmVf) {
+                                               const CUtensorMap* tmVf, int part = TILE_ALL) {
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
@@ -143,20 +147,29 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     const int nbox = full ? 1 : (n + C::BOX_ROWS - 1) / C::BOX_ROWS;
     const int rows = full ? TT : C::BOX_ROWS;
     const bool with_q = c.first();
-    uint32_t bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
-    if (with_q) bytes += C::G * C::ROWB;
-    mbar_arrive_expect_tx(&full_bar[stage], bytes);
-    const int row0 = (int)(unit * p.T_max + c.t);
-    const CUtensorMap* mk = full ? tmKf : tmK;
-    const CUtensorMap* mv = full ? tmVf : tmV;
+    const uint32_t kv_bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
+    const uint32_t q_bytes = with_q ? (uint32_t)(C::G * C::ROWB) : 0u;
+    if (part == TILE_Q) {
+        if (with_q) mbar_arrive_expect_tx(&full_bar[stage], q_bytes);
+        else mbar_arrive(&full_bar[stage]);
+    } else if (part == TILE_KV) {
+        mbar_expect_tx(&full_bar[stage], kv_bytes);
+    } else {
+        mbar_arrive_expect_tx(&full_bar[stage], kv_bytes + q_bytes);
+    }
+    if (part != TILE_Q) {
+        const int row0 = (int)(unit * p.T_max + c.t);
+        const CUtensorMap* mk = full ? tmKf : tmK;
+        const CUtensorMap* mv = full ? tmVf : tmV;
 #pragma unroll
-    for (int hf = 0; hf < C::HALVES; ++hf)
-        for (int bx = 0; bx < nbox; ++bx) {
-            const uint32_t off = hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128;
-            tma_load_2d(ks + off, mk, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
-            tma_load_2d(vs + off, mv, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
-        }
-    if (with_q) {
+        for (int hf = 0; hf < C::HALVES; ++hf)
+            for (int bx = 0; bx < nbox; ++bx) {
+                const uint32_t off = hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128;
+                tma_load_2d(ks + off, mk, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+                tma_load_2d(vs + off, mv, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+            }
+    }
+    if (with_q && part != TILE_KV) {
         asm volatile(
             "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
             "[%1], %2, [%3], %4;" ::"r"(qs),
@@ -257,8 +270,11 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKf)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVf)) : "memory");
     }
-    // everything below may read what earlier work on the stream wrote
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // With overlap, lens and the history rows below each stream's last row are read before the
+    // preceding grid on the stream has finished (the caller guarantees it does not write them);
+    // everything else waits for it.
+    const bool early = p.overlap != 0;
+    if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         int64_t carry = 0;
@@ -281,6 +297,32 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     }
     __syncthreads();
 
+    const int64_t W = (int64_t)H_kv * prefix[B];
+    int64_t P = p.P;
+    {
+        const int64_t want = W > 0 ? (W + p.min_tokens - 1) / p.min_tokens : 0;
+        if (want < P) P = want;
+    }
+    const int64_t r0 = W > 0 ? cta_begin(blockIdx.x, W, P) : 0;
+    const int64_t r1 = W > 0 ? cta_begin(blockIdx.x + 1, W, P) : 0;
+    const bool work = W > 0 && (int64_t)blockIdx.x < P && r0 < r1;
+    const uint32_t ring_s = smem_addr(ring);
+    const uint64_t pol = policy_evict_first();
+    TileCursor<TT> pref;  // producer's cursor (thread 0)
+    int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
+    if (tid == 0 && work) {
+        pref.init(prefix, B, H_kv, r0, r1);
+        if (early)
+            while (pref.valid && npre < NST && pref.t + pref.n() < pref.it.L) {
+                issue_tile_tc5<C, TT>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
+                                      TILE_KV);
+                issued[npre] += 1;
+                pref.advance();
+                ++npre;
+            }
+    }
+    if (early) asm volatile("griddepcontrol.wait;" ::: "memory");
+
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         if (prefix[b + 1] == prefix[b]) {
             if (tid == 0) atomicOr(p.err, DEV_BAD_LENS);
@@ -288,29 +330,22 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 Elem<T>::store(p.out, (size_t)b * row_elems_q + i, 0.f);
         }
     }
-
-    const int64_t W = (int64_t)H_kv * prefix[B];
-    if (W == 0) return;
-    int64_t P = p.P;
-    {
-        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
-        if (want < P) P = want;
-    }
-    if ((int64_t)blockIdx.x >= P) return;
-    const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
-    if (r0 >= r1) return;
+    if (!work) return;
     const bool fused = p.k_new != nullptr;
-    const uint32_t ring_s = smem_addr(ring);
     uint32_t tmem = 0;
 
     if (warp == 0) {
         // ======================================================= producer
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            TileCursor<TT> pref;
-            pref.init(prefix, B, H_kv, r0, r1);
-            int s = 0;
-            uint32_t ph = 0;
+            // finish the tiles started early: q (segment's first tile) and the arrival
+            TileCursor<TT> c0;
+            c0.init(prefix, B, H_kv, r0, r1);
+            for (int i = 0; i < npre; ++i) {
+                issue_tile_tc5<C, TT>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf, TILE_Q);
+                c0.advance();
+            }
+            int s = npre == NST ? 0 : npre;
+            uint32_t ph = npre == NST ? 1u : 0u;
             while (pref.valid) {
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err)) break;
                 // a tile that holds a stream's new token waits for the fused append's writes

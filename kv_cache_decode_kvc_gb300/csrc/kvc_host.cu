@@ -25,6 +25,7 @@ struct kvc_cache {
     int* counters;
     uint32_t* err;
     int math;                        // 0 automatic, 1 CUDA cores, 2 warp MMA, 3 tcgen05
+    int overlap;                     // 1: early history reads before the preceding grid ends
     bool tc_ok;                      // tensor maps built (bf16 cache, rows < 2^31)
     std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes)
 };
@@ -159,6 +160,7 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     }
     p.combine_mode = mode;
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
+    p.overlap = h->overlap;
     return launch_decode(h, layer, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -222,6 +224,7 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
     h->sms = prop.multiProcessorCount;
     h->ctas = 0;
     h->combine_mode = -1;
+    h->overlap = 0;
     h->math = 0;
     h->tc_ok = false;
     h->max_ctas = 4 * h->sms;
@@ -338,6 +341,17 @@ int kvc_set_math(kvc_t h, int mode) {
 int kvc_get_math(kvc_t h) {
     if (!h) return -1;
     return kvc_math_path(h);
+}
+
+int kvc_set_launch_overlap(kvc_t h, int on) {
+    if (!h || on < 0 || on > 1) return KVC_EINVAL;
+    h->overlap = on;
+    return KVC_OK;
+}
+
+int kvc_get_launch_overlap(kvc_t h) {
+    if (!h) return -1;
+    return h->overlap;
 }
 
 int kvc_set_combine_mode(kvc_t h, int mode) {

@@ -46,6 +46,7 @@ struct DecodeParams {
     int min_tokens;       // fewer CTAs when W / P would drop below this (1 = never)
     int combine_mode;     // 0: the last CTA of a split stream merges it; 1: combine kernel
     float qscale;         // log2(e) / sqrt(D), folded into q
+    int overlap;          // 1: lens and history rows may be read before the preceding grid ends
 };
 
 struct CopyParams {
@@ -106,6 +107,13 @@ __device__ __forceinline__ void fence_mbar_init() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Adds expected transaction bytes to the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
 }

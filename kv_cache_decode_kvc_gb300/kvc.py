@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
         "kvc_set_combine_mode": (I, [P, I]),
         "kvc_set_math": (I, [P, I]),
         "kvc_get_math": (I, [P]),
+        "kvc_set_launch_overlap": (I, [P, I]),
+        "kvc_get_launch_overlap": (I, [P]),
         "kvc_get_shape": (I, [P] + [ctypes.POINTER(I)] * 7),
         "kvc_plan_cta_of": (I, [I64, I64, I]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
@@ -180,6 +182,14 @@ def kvc_get_math(h) -> int:
     return int(load().kvc_get_math(h))
 
 
+def kvc_set_launch_overlap(h, on) -> None:
+    _check(load().kvc_set_launch_overlap(h, int(on)), "kvc_set_launch_overlap")
+
+
+def kvc_get_launch_overlap(h) -> int:
+    return int(load().kvc_get_launch_overlap(h))
+
+
 def kvc_get_shape(h) -> dict:
     vals = [ctypes.c_int() for _ in range(7)]
     _check(load().kvc_get_shape(h, *[ctypes.byref(v) for v in vals]), "kvc_get_shape")
@@ -261,6 +271,12 @@ class KVCache:
 
     def math(self) -> int:
         return kvc_get_math(self.h)
+
+    def set_launch_overlap(self, on):
+        kvc_set_launch_overlap(self.h, on)
+
+    def launch_overlap(self) -> int:
+        return kvc_get_launch_overlap(self.h)
 
 
 def _wrap_device(ptr: int, shape, dtype):

@@ -114,3 +114,11 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.kvc_prefill_write(None, 0, 1, 1, 1, 1, None) == kvc.KVC_EINVAL
     assert lib.kvc_bytes(None) == 0
     assert lib.kvc_destroy(None) == kvc.KVC_OK
+
+
+def test_null_handle_setters_are_rejected(lib):
+    assert lib.kvc_set_launch_overlap(None, 1) == kvc.KVC_EINVAL
+    assert lib.kvc_get_launch_overlap(None) == -1
+    assert lib.kvc_set_math(None, 0) == kvc.KVC_EINVAL
+    assert lib.kvc_get_math(None) == -1
+    assert lib.kvc_set_combine_mode(None, 0) == kvc.KVC_EINVAL

@@ -24,7 +24,7 @@ def _built():
     torch.cuda.init()
 
 
-def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0, math=0):
+def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0, math=0, overlap=0):
     c = kvc.KVCache(layers, case.B, case.H_q, case.H_kv, case.D, T_max,
                     "bf16" if case.dtype == torch.bfloat16 else "f32")
     try:
@@ -32,6 +32,8 @@ def _run(case, T_max, fused=True, ctas=0, mode=-1, layers=1, layer=0, math=0):
             c.set_ctas(ctas)
         c.set_combine_mode(mode)
         c.set_math(math)
+        c.set_launch_overlap(overlap)
+        assert c.launch_overlap() == overlap
         if math:
             assert c.math() == math
         elif case.dtype == torch.bfloat16 and case.D == 128:
@@ -203,3 +205,42 @@ def test_generator_is_device_independent():
     a = synth.block(3, 5, "V", 2, 6, 4, 100, 357, 128, 8, torch.bfloat16, "cpu")
     b = synth.block(3, 5, "V", 2, 6, 4, 100, 357, 128, 8, torch.bfloat16, "cuda")
     assert torch.equal(a, b.cpu())
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("ctas", [3, 152])
+@pytest.mark.parametrize("G", [1, 4, 32])
+def test_launch_overlap_gives_the_same_results(G, ctas, fused):
+    """Early history loads (before the preceding grid completes) change no result: every
+    (stream, tile) layout, including tiles holding a stream's new row, which are loaded only
+    after the wait."""
+    case = Case(300 + G, 3, 2 * G, 2, 128, [700, 0, 129], "bf16")
+    T_max = 800
+    out, Kg, Vg = _run(case, T_max, fused=fused, ctas=ctas, math=3, overlap=1)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"overlap G={G} ctas={ctas}")
+    Kc, Vc = case.oracle_cache(T_max)
+    assert np.array_equal(host_bits(Kg), Kc) and np.array_equal(host_bits(Vg), Vc)
+
+
+def test_launch_overlap_layer_loop_matches_oracle():
+    """A decode step over several layers back to back on one stream with overlap on: each
+    launch starts loading while the previous layer's launch is finishing."""
+    B, H_q, H_kv, D, T_max, L = 4, 32, 8, 128, 1200, 6
+    lens_pre = [1100, 5, 640, 999]
+    cases = [Case(400 + l, B, H_q, H_kv, D, lens_pre, "bf16", layer=l) for l in range(L)]
+    c = kvc.KVCache(L, B, H_q, H_kv, D, T_max, "bf16")
+    try:
+        c.set_math(3)
+        c.set_launch_overlap(1)
+        devs = [cs.to_device() for cs in cases]
+        for l, d in enumerate(devs):
+            c.prefill_write(l, d["K"], d["V"], d["lens_pre"])
+        outs = [torch.full((B, H_q, D), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        for _ in range(3):  # repeated steps: the same token re-appended, same outputs
+            for l, d in enumerate(devs):
+                c.decode_step(l, d["q"], d["k_new"], d["v_new"], outs[l], d["lens"])
+        assert c.last_error() == (kvc.KVC_OK, 0)
+        for l in range(L):
+            check_close(outs[l], cases[l].oracle_out(T_max), torch.bfloat16, f"layer {l}")
+    finally:
+        c.close()
