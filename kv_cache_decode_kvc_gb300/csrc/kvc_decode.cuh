@@ -229,10 +229,12 @@ __device__ __forceinline__ void group_sync() {
 // every 16-byte partial-output load and 8-byte (max, denominator) load of its UNR groups before
 // using any, and folds them in with a running maximum, so a stream split over at most 4 CTAs
 // costs one round trip to L2 per UNR groups.  Run by NT threads.  Slots are 16-byte aligned
-// (G * D is a multiple of 4).
+// (G * D is a multiple of 4).  With `loc`, the state of CTA `self` is taken from shared memory
+// (layout [G][D + 2]: unnormalised output, max, denominator) instead of its slot.
 template <typename T, int G, int D, int NT>
 __device__ __forceinline__ void merge_partials(const DecodeParams& p, size_t unit, int64_t cfirst,
-                                               int64_t clast, int tid) {
+                                               int64_t clast, int tid, const float* loc = nullptr,
+                                               int64_t self = -1) {
     const int nseg = (int)(clast - cfirst + 1);
     constexpr int V4 = G * D / 4;
     constexpr int PER = (V4 + NT - 1) / NT;
@@ -252,6 +254,13 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, size_t uni
             den[u] = 0.f;
             const int hh = ((base + u * NT) * 4) / D;
             h[u] = hh < G ? hh : G - 1;
+            if (loc != nullptr && base + u * NT < V4) {
+                const float* lh = loc + h[u] * (D + 2);
+                const int d0 = (base + u * NT) * 4 - h[u] * D;
+                acc[u] = make_float4(lh[d0], lh[d0 + 1], lh[d0 + 2], lh[d0 + 3]);
+                M[u] = lh[D];
+                den[u] = lh[D + 1];
+            }
         }
         for (int c0 = 0; c0 < nseg; c0 += 4) {
             float4 v[UNR][4];
@@ -260,7 +269,7 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, size_t uni
             for (int u = 0; u < UNR; ++u)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const bool in = base + u * NT < V4 && c0 + j < nseg;
+                    const bool in = base + u * NT < V4 && c0 + j < nseg && cfirst + c0 + j != self;
                     v[u][j] = in ? __ldcg(po4 + (size_t)(c0 + j) * V4 + base + u * NT)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                     ml[u][j] = in ? __ldcg(pml + (size_t)(c0 + j) * G + h[u]) : make_float2(-INFINITY, 0.f);
@@ -309,6 +318,25 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
     const int64_t us = it.ustart;
     const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + it.L - 1, W, P);
     const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
+    if constexpr (NWT == 1) {
+        // `merge` holds this segment's final state.  If every other CTA of the stream has
+        // already published its partial state (and counted itself), this CTA is the last: it
+        // merges from shared memory without publishing its own.
+        if (!whole && p.combine_mode == 0) {
+            if (tid == 0) {
+                int seen;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(&p.counters[unit]) : "memory");
+                *last_flag = (seen == (int)(clast - cfirst));
+            }
+            group_sync<BAR, NW * 32>();
+            if (*last_flag) {
+                merge_partials<T, G, D, NW * 32>(p, unit, cfirst, clast, tid, merge, (int64_t)blockIdx.x);
+                if (tid == 0) p.counters[unit] = 0;  // every other arrival is in: ready for next call
+                group_sync<BAR, NW * 32>();
+                return;
+            }
+        }
+    }
     for (int idx = tid; idx < G * D; idx += NW * 32) {
         const int hg = idx / D, d = idx - hg * D;
         const int s_ = hg / HS, hh = hg - s_ * HS;

@@ -62,8 +62,11 @@ WORKLOADS = {
                  note="8B-shaped GQA serving batch, cached lengths U{3000..6000} (seed 1234)"),
         Workload("gqa70b_b32_t8192", 80, 32, 64, 8, 128, 8192,
                  note="70B-shaped GQA long context (80 GiB cache)"),
-        Workload("mqa_b64_t4096", 1, 64, 32, 1, 128, 4096, note="MQA, one layer"),
-        Workload("mqa_b1_t131072", 1, 1, 32, 1, 128, 131072, note="MQA long context, split-T stress"),
+        # the MQA shapes are single-layer; 4 layer copies make a step read 4x their bytes, more
+        # than L2 holds, so that timed reads come from HBM
+        Workload("mqa_b64_t4096", 4, 64, 32, 1, 128, 4096, note="MQA, one layer's shape x 4 copies"),
+        Workload("mqa_b1_t131072", 4, 1, 32, 1, 128, 131072,
+                 note="MQA long context, split-T stress, one layer's shape x 4 copies"),
     ]
 }
 
