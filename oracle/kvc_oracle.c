@@ -20,7 +20,7 @@
  *   - score scale is 1/sqrt(D): [M11] §2.2 prints "/d_k" (the square root was lost in
  *     extraction); the teaching code in [KVG] divides by math.sqrt(head_dim).
  *   - the new token attends to itself: append first, then attend over all L slots
- *     ([W1D4] §1.3: "q 对缓存里全部 t+1 个 key 做注意力").
+ *     ([W1D4] §1.3: after the append the new query attends to all t+1 cached keys).
  *   - lens[b] is the valid length AFTER the call's write; append writes slot lens[b]-1.
  *   - query head j reads KV head floor(j / (H_q/H_kv))  ([W1D4] §3.4, repeat_interleave).
  *   - a row with lens[b] < 1 or lens[b] > T_max is invalid: its output is zero and it is
