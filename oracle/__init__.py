@@ -58,6 +58,12 @@ def lib() -> ctypes.CDLL:
         L.oracle_layer_full.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P]
         L.oracle_layer_incremental.restype = None
         L.oracle_layer_incremental.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+        L.oracle_paged_append.restype = I
+        L.oracle_paged_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I]
+        L.oracle_paged_prefill_write.restype = I
+        L.oracle_paged_prefill_write.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I]
+        L.oracle_paged_decode_attn.restype = I
+        L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P]
         L.oracle_set_fault.restype = None
         L.oracle_set_fault.argtypes = [I]
         L.oracle_get_fault.restype = I
@@ -118,6 +124,45 @@ def decode_attn(q, Kc, Vc, lens, return_bad: bool = False):
     return (out, bad) if return_bad else out
 
 
+def _paged_shape(Kp, table):
+    num_blocks, H_kv, bs, D = Kp.shape
+    B, max_blocks = table.shape
+    return num_blocks, H_kv, bs, D, B, max_blocks
+
+
+def paged_append(Kp, Vp, k_new, v_new, table, lens) -> int:
+    """In place: token lens[b]-1 of sequence b (pool [num_blocks,H_kv,bs,D], table
+    [B,max_blocks]) takes k_new/v_new [B,H_kv,D].  Returns the number of invalid rows."""
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    nbk, H_kv, bs, D, B, mb = _paged_shape(Kp, table)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_paged_append(_ptr(Kp), _ptr(Vp), _ptr(k_new), _ptr(v_new), _ptr(table),
+                                     _ptr(lens), B, H_kv, D, bs, mb, nbk, _dtype_code(Kp))
+
+
+def paged_prefill_write(Kp, Vp, K, V, table, lens) -> int:
+    """In place: tokens [0, lens[b]) of K/V [B,H_kv,T_in,D] into the pool through the table."""
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    nbk, H_kv, bs, D, B, mb = _paged_shape(Kp, table)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_paged_prefill_write(_ptr(Kp), _ptr(Vp), _ptr(K), _ptr(V), K.shape[2],
+                                            _ptr(table), _ptr(lens), B, H_kv, D, bs, mb, nbk,
+                                            _dtype_code(Kp))
+
+
+def paged_decode_attn(q, Kp, Vp, table, lens, return_bad: bool = False):
+    """out[B,H_q,D] (float64): decode attention over the history read through the table."""
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    nbk, H_kv, bs, D, B, mb = _paged_shape(Kp, table)
+    Bq, H_q, Dq = q.shape
+    assert Bq == B and Dq == D and Kp.shape == Vp.shape and q.dtype == Kp.dtype == Vp.dtype
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros((B, H_q, D), dtype=np.float64)
+    bad = lib().oracle_paged_decode_attn(_ptr(q), _ptr(Kp), _ptr(Vp), _ptr(table), _ptr(lens), B,
+                                         H_q, H_kv, D, bs, mb, nbk, _dtype_code(q), _ptr(out))
+    return (out, bad) if return_bad else out
+
+
 def layer_full(x, WQ, WK, WV, WO, H_q, H_kv, D):
     """Path A (dense causal layer).  Returns (out[B,T,hidden], K[B,H_kv,T,D], V[...])."""
     x = np.ascontiguousarray(x, dtype=np.float64)
@@ -149,7 +194,7 @@ class planted_fault:
     """Context manager that plants a known mistake in the oracle (tests only).
 
     1 = interleaved GQA map (j mod H_kv), 2 = score scale 1/D, 3 = append one slot late,
-    4 = the new token left out of the attention."""
+    4 = the new token left out of the attention, 5 = paged block stored token-major."""
 
     def __init__(self, which: int):
         self.which = which

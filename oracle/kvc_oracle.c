@@ -220,6 +220,128 @@ int oracle_decode_attn(const void* q, const void* Kc, const void* Vc, const int3
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Paged cache.  The pages describe storage cut into fixed-size blocks handed out on demand,
+ * found through a table, with the attention arithmetic unchanged ([W1D4] §1.6; [KVG]
+ * "先把它放回推理链路" and "成本转移、失败场景与常见误解"; [M11] §8).  They fix no layout; the
+ * reading taken here:
+ *   pool  [num_blocks, H_kv, bs, D]   (dtype), one per layer for K and one for V
+ *   table [B, max_blocks]             int32, physical block of logical block j of sequence b
+ *   token t of sequence b, head h  ->  pool[table[b, t / bs], h, t % bs, :]
+ * A row is invalid when lens[b] is out of [1, max_blocks * bs] (appends and attention) or
+ * when a table entry it needs is out of [0, num_blocks).
+ * ------------------------------------------------------------------------------------- */
+
+static int paged_row_ok(const int32_t* table, int b, int L, int L_min, int bs, int max_blocks,
+                        int num_blocks) {
+    if (L < L_min || L > max_blocks * bs) return 0;
+    int nb = (L + bs - 1) / bs;
+    for (int j = 0; j < nb; ++j) {
+        int e = table[(size_t)b * max_blocks + j];
+        if (e < 0 || e >= num_blocks) return 0;
+    }
+    return 1;
+}
+
+static size_t paged_row_offset(const int32_t* table, int b, int h, int t, int H_kv, int bs,
+                               int max_blocks) {
+    int e = table[(size_t)b * max_blocks + t / bs];
+    if (g_fault == 5) /* planted: token-major block ([bs, H_kv] instead of [H_kv, bs]) */
+        return ((size_t)e * bs + (size_t)(t % bs)) * H_kv + h;
+    return (((size_t)e * H_kv + h) * bs + (size_t)(t % bs));
+}
+
+/* Writes k_new[b,h,:] (layout [B,H_kv,D]) into token lens[b]-1 of sequence b.  Returns the
+ * number of invalid rows (skipped). */
+int oracle_paged_append(void* Kp, void* Vp, const void* k_new, const void* v_new,
+                        const int32_t* table, const int32_t* lens, int B, int H_kv, int D,
+                        int bs, int max_blocks, int num_blocks, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (!paged_row_ok(table, b, L, 1, bs, max_blocks, num_blocks)) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            size_t dst = paged_row_offset(table, b, h, L - 1, H_kv, bs, max_blocks) * row;
+            size_t src = ((size_t)b * H_kv + h) * row;
+            memcpy((char*)Kp + dst, (const char*)k_new + src, row);
+            memcpy((char*)Vp + dst, (const char*)v_new + src, row);
+        }
+    }
+    return bad;
+}
+
+/* Writes K[b,h,0:lens[b],:] (layout [B,H_kv,T_in,D]) into tokens [0, lens[b]) of sequence b.
+ * Returns the number of invalid rows (lens[b] > T_in counts as invalid; lens[b] = 0 writes
+ * nothing and is valid). */
+int oracle_paged_prefill_write(void* Kp, void* Vp, const void* K, const void* V, int T_in,
+                               const int32_t* table, const int32_t* lens, int B, int H_kv, int D,
+                               int bs, int max_blocks, int num_blocks, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L > T_in || !paged_row_ok(table, b, L, 0, bs, max_blocks, num_blocks)) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h)
+            for (int t = 0; t < L; ++t) {
+                size_t dst = paged_row_offset(table, b, h, t, H_kv, bs, max_blocks) * row;
+                size_t src = (((size_t)b * H_kv + h) * T_in + t) * row;
+                memcpy((char*)Kp + dst, (const char*)K + src, row);
+                memcpy((char*)Vp + dst, (const char*)V + src, row);
+            }
+    }
+    return bad;
+}
+
+/* Decode attention over a paged cache: for every query row, the history rows are read
+ * through the table in token order, then the same arithmetic as oracle_decode_attn.
+ * out [B, H_q, D] double; invalid rows are zero.  Returns the number of invalid rows. */
+int oracle_paged_decode_attn(const void* q, const void* Kp, const void* Vp, const int32_t* table,
+                             const int32_t* lens, int B, int H_q, int H_kv, int D, int bs,
+                             int max_blocks, int num_blocks, int dtype, double* out) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        if (!paged_row_ok(table, b, lens[b], 1, bs, max_blocks, num_blocks)) ++bad;
+    const int rows = B * H_q;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) if (g_threads > 1)
+#endif
+    for (int r = 0; r < rows; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (!paged_row_ok(table, b, L, 1, bs, max_blocks, num_blocks)) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        for (int t = 0; t < L; ++t) {
+            size_t base = paged_row_offset(table, b, h, t, H_kv, bs, max_blocks) * D;
+            for (int d = 0; d < D; ++d) {
+                Kd[(size_t)t * D + d] = load_elem(Kp, dtype, base + d);
+                Vd[(size_t)t * D + d] = load_elem(Vp, dtype, base + d);
+            }
+        }
+        decode_row_f64(qd, Kd, Vd, L, D, (size_t)D, o, s);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(s);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
  * One attention layer, two ways ([KVG] "两条数学等价的 decode 路径"; [W1D4] §1.3).
  * x: [B, T, hidden]; W_Q [hidden, H_q*D], W_K / W_V [hidden, H_kv*D], W_O [H_q*D, hidden],
  * all double, row-major.  No RoPE, no norm: the pages' single-layer teaching setting.
