@@ -57,6 +57,7 @@ typedef struct kvc_cache* kvc_t;
 /* Bits of the device error word returned through kvc_last_error's `detail`. */
 #define KVC_DEV_BAD_LENS 1u     /* some lens[b] < 1 (or < 0 for prefill) or > T_max */
 #define KVC_DEV_WAIT_TIMEOUT 2u /* an in-kernel wait gave up (internal error; output invalid) */
+#define KVC_DEV_BAD_BLOCK 4u    /* a paged call met a block-table entry outside [0, num_blocks) */
 
 /* Create a cache of `layers` layers, each holding K and V of shape [B, H_kv, T_max, D].
  * Supported: dtype KVC_BF16 with D in {64, 128, 256}; KVC_F32 with D in {4, 64, 128, 256};
@@ -150,6 +151,44 @@ int kvc_get_math(kvc_t h);
 int kvc_set_launch_overlap(kvc_t h, int on);
 int kvc_get_launch_overlap(kvc_t h);
 
+/* ---------------------------------------------------------------------------------------
+ * Paged cache.  The pages describe storage cut into fixed-size blocks that are handed out on
+ * demand and found through a table, with the attention arithmetic unchanged ("第 1 周 · Day 4"
+ * §1.6; "KV 缓存", "先把它放回推理链路" and "成本转移、失败场景与常见误解"; "11.7 KV Cache" §8).
+ * They fix no layout; this one:
+ *   - per layer, K and V are pools [num_blocks, H_kv, block_size, D] owned by the handle
+ *     (zero at create), block_size in {16, 32, 64, 128, 256};
+ *   - block_table (int32 [B, max_blocks], DEVICE memory, owned by the caller, who also
+ *     decides which blocks a sequence gets) maps logical block j of sequence b to a pool block;
+ *     the same table serves every layer;
+ *   - token t of sequence b, KV head h is row (block_table[b][t / block_size], h,
+ *     t % block_size) of the layer's pools; a sequence holds up to T_max = max_blocks *
+ *     block_size tokens (lens[b] <= T_max, else KVC_DEV_BAD_LENS as for contiguous caches).
+ * Only table entries of blocks [0, ceil(lens[b] / block_size)) are read.  An entry outside
+ * [0, num_blocks) sets KVC_DEV_BAD_BLOCK: writes to that row are skipped and attention reads
+ * pool block 0 in its place (no out-of-bounds access; the outputs of that sequence are then
+ * unspecified).  A paged handle accepts only the kvc_paged_* writes and attention calls
+ * below (the contiguous ones return KVC_EINVAL, and vice versa); kvc_layer_ptrs returns the
+ * pools, kvc_bytes the pools' size, kvc_get_shape T_max = max_blocks * block_size.  Math
+ * paths: 0, 1, 3 (warp MMA, 2, is KVC_EUNSUPPORTED).  With launch overlap on, block-table
+ * entries of history blocks are read early as well. */
+int kvc_create_paged(kvc_t* out, int layers, int num_blocks, int block_size, int B, int max_blocks,
+                     int H_q, int H_kv, int D, int dtype);
+/* K, V: [B, H_kv, T_in, D]; writes tokens [0, lens[b]) of each sequence (lens[b] <= T_in). */
+int kvc_paged_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in,
+                            const int32_t* block_table, const int32_t* lens, void* stream);
+/* k_new, v_new: [B, H_kv, D]; writes token lens[b] - 1 of each sequence. */
+int kvc_paged_append(kvc_t h, int layer, const void* k_new, const void* v_new,
+                     const int32_t* block_table, const int32_t* lens, void* stream);
+/* Decode attention over tokens [0, lens[b]) read through the table; q, out [B, H_q, D]. */
+int kvc_paged_decode_attn(kvc_t h, int layer, const void* q, void* out, const int32_t* block_table,
+                          const int32_t* lens, void* stream);
+/* kvc_paged_append + kvc_paged_decode_attn in one launch (same results). */
+int kvc_paged_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                          void* out, const int32_t* block_table, const int32_t* lens, void* stream);
+/* Paged geometry (any pointer may be NULL); KVC_EINVAL for a contiguous handle. */
+int kvc_get_paged_shape(kvc_t h, int* num_blocks, int* block_size, int* max_blocks);
+
 /* Shape query: writes layers, B, H_q, H_kv, D, T_max, dtype (any pointer may be NULL). */
 int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
                   int* dtype);
@@ -159,6 +198,19 @@ int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int
  * holding lens[b] tokens; with W tokens in total, CTA i of P takes positions
  * [floor(i*W/P), floor((i+1)*W/P)).  Returns the CTA that owns position x (0 <= x < W). */
 int kvc_plan_cta_of(int64_t x, int64_t W, int P);
+
+/* The partition the attention kernels use, on the host (for tests).  lens_host [B] holds
+ * post-append lengths (invalid ones count as 0); block_size 1 for a contiguous cache.  The
+ * kernels use Pu = min(P, ceil(W / min_tokens)) CTAs, further capped at floor(W / block_size)
+ * for a paged cache; CTA i takes stream positions [cuts[i], cuts[i+1]).  A paged cache rounds
+ * each cut down to a block boundary of the stream it falls in, so every segment starts on a
+ * block.  Writes cuts[0..Pu] (Pu + 1 values; cuts must hold P + 1) and returns Pu (0 when
+ * W = 0, -1 for bad arguments). */
+int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+                  int min_tokens, int64_t* cuts);
+/* First and last CTA holding stream (b, h) under that partition (KVC_EINVAL if it is empty). */
+int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+                         int min_tokens, int b, int h, int* first, int* last);
 
 /* Decode attention for callers that cannot allocate device memory.  The pages have no
  * counterpart: this is an interface variant of kvc_decode_attn, same kernel, same results.

@@ -5,6 +5,8 @@
 // "两条数学等价的 decode 路径", path B).  The write costs 2*B*H_kv*D*s bytes whatever the
 // history length ("11.7 KV Cache：形状、显存与带宽" §1.1: constant-cost append).
 // prefill write: the prompt's T_p rows per (b, h) go to slots [0, lens[b]).
+// Paged caches reach token t of (b, h) through the block table (cache_row); a row whose table
+// entry is out of range is not written (and DEV_BAD_BLOCK is flagged).
 #include "kvc_decode.cuh"
 
 namespace kvc {
@@ -20,7 +22,10 @@ __global__ void append_kernel(const CopyParams p) {
         if (h == 0 && lane == 0) atomicOr(p.err, DEV_BAD_LENS);
         return;
     }
-    const size_t dst = ((size_t)gw * p.T_max + (size_t)(L - 1)) * p.row_bytes;
+    const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b, h,
+                                   L - 1, p.err);
+    if (drow < 0) return;
+    const size_t dst = (size_t)drow * p.row_bytes;
     const size_t src = (size_t)gw * p.row_bytes;
     const int nvec = p.row_bytes >> 4;
     for (int v = lane; v < nvec; v += 32) {
@@ -51,7 +56,9 @@ __global__ void prefill_kernel(const CopyParams p) {
         if (t >= L) continue;
         const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + row * p.row_bytes) + v);
         const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + row * p.row_bytes) + v);
-        const size_t drow = bh * p.T_max + t;
+        const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b,
+                                       (int)(bh - (size_t)b * p.H_kv), t, p.err);
+        if (drow < 0) continue;
         reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + drow * p.row_bytes)[v] = kx;
         reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + drow * p.row_bytes)[v] = vx;
     }

@@ -193,11 +193,26 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
     uint32_t bytes = (uint32_t)(2 * n * C::ROWB);
     if (with_q) bytes += C::G * C::ROWB;
     mbar_arrive_expect_tx(&full_bar[stage], bytes);
-    const char* Kg = static_cast<const char*>(p.K) + (unit * p.T_max + c.t) * C::ROWB;
-    const char* Vg = static_cast<const char*>(p.V) + (unit * p.T_max + c.t) * C::ROWB;
-    if (nc > 0) {
-        bulk_g2s(ks, Kg, nc * C::ROWB, &full_bar[stage], pol);
-        bulk_g2s(vs, Vg, nc * C::ROWB, &full_bar[stage], pol);
+    if (p.table == nullptr) {
+        const char* Kg = static_cast<const char*>(p.K) + (unit * p.T_max + c.t) * C::ROWB;
+        const char* Vg = static_cast<const char*>(p.V) + (unit * p.T_max + c.t) * C::ROWB;
+        if (nc > 0) {
+            bulk_g2s(ks, Kg, nc * C::ROWB, &full_bar[stage], pol);
+            bulk_g2s(vs, Vg, nc * C::ROWB, &full_bar[stage], pol);
+        }
+    } else {
+        // paged: one copy per block piece (the rows of one (block, head) are contiguous)
+        for (int r = 0; r < nc;) {
+            const int t = c.t + r;
+            const int m = (p.bs - t % p.bs) < (nc - r) ? (p.bs - t % p.bs) : (nc - r);
+            const int64_t row = cache_row_rd(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv,
+                                             p.T_max, c.it.b, c.it.h, t, p.err);
+            bulk_g2s(ks + r * C::ROWB, static_cast<const char*>(p.K) + row * C::ROWB, m * C::ROWB,
+                     &full_bar[stage], pol);
+            bulk_g2s(vs + r * C::ROWB, static_cast<const char*>(p.V) + row * C::ROWB, m * C::ROWB,
+                     &full_bar[stage], pol);
+            r += m;
+        }
     }
     if (last_here) {
         bulk_g2s(ks + nc * C::ROWB, static_cast<const char*>(p.k_new) + unit * C::ROWB, C::ROWB,
@@ -316,7 +331,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
                                                int* last_flag, int tid) {
     const bool whole = (it.t0 == 0) && (it.t1 == it.L);
     const int64_t us = it.ustart;
-    const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + it.L - 1, W, P);
+    const int64_t cfirst = cta_first_of_stream(us, it.L, W, P, p.bs), clast = cta_of(us + it.L - 1, W, P);
     const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
     if constexpr (NWT == 1) {
         // `merge` holds this segment's final state.  If every other CTA of the stream has
@@ -443,13 +458,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 
     const int64_t W = (int64_t)H_kv * prefix[B];
     if (W == 0) return;
-    int64_t P = p.P;
-    {
-        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
-        if (want < P) P = want;
-    }
+    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
     if ((int64_t)blockIdx.x >= P) return;
-    const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
+    const int64_t r0 = cta_cut(blockIdx.x, prefix, B, H_kv, W, P, p.bs);
+    const int64_t r1 = cta_cut(blockIdx.x + 1, prefix, B, H_kv, W, P, p.bs);
     if (r0 >= r1) return;
     const bool fused = p.k_new != nullptr;
     const uint64_t pol = policy_evict_first();
@@ -620,8 +632,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                 }
             }
             // fused append: warp 0 stores the new token's rows (now in the tile) into the cache
-            if (fused && warp == 0 && cur.t + n == cur.it.L) {
-                const size_t dst = (unit * p.T_max + (size_t)(cur.it.L - 1)) * C::ROWB;
+            const int64_t arow = (fused && warp == 0 && cur.t + n == cur.it.L)
+                                     ? cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max,
+                                                 cur.it.b, cur.it.h, cur.it.L - 1, p.err)
+                                     : -1;
+            if (arow >= 0) {
+                const size_t dst = (size_t)arow * C::ROWB;
                 const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(Ks) + (n - 1) * C::ROWB;
                 const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(Vs) + (n - 1) * C::ROWB;
                 unsigned char* kd = static_cast<unsigned char*>(const_cast<void*>(p.K)) + dst;
@@ -771,13 +787,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     const int Lb = p.lens[b];
     if (Lb < 1 || Lb > p.T_max) return;
     const int64_t W = (int64_t)p.H_kv * sh_sum[1];
-    int64_t P = p.P;
-    {
-        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
-        if (want < P) P = want;
-    }
+    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
     const int64_t us = (int64_t)p.H_kv * sh_sum[0] + (int64_t)h * Lb;
-    const int64_t cfirst = cta_of(us, W, P), clast = cta_of(us + Lb - 1, W, P);
+    const int64_t cfirst = cta_first_of_stream(us, Lb, W, P, p.bs), clast = cta_of(us + Lb - 1, W, P);
     if (cfirst == clast) return;  // written directly by its CTA
     const int nseg = (int)(clast - cfirst + 1);
     if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs

@@ -207,11 +207,7 @@ __global__ void __launch_bounds__(TcCfg<D, G>::NTHREADS, 1)
 
     const int64_t W = (int64_t)H_kv * prefix[B];
     if (W == 0) return;
-    int64_t P = p.P;
-    {
-        const int64_t want = (W + p.min_tokens - 1) / p.min_tokens;
-        if (want < P) P = want;
-    }
+    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
     if ((int64_t)blockIdx.x >= P) return;
     const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
     if (r0 >= r1) return;

@@ -132,20 +132,33 @@ __device__ __forceinline__ void tc5_ld16(uint32_t taddr, float (&v)[16]) {
 // stage's barrier without arriving and starts the K/V copies; TILE_Q then adds q (first tile
 // of a segment) and arrives, so the stage cannot complete before q is in.
 enum { TILE_ALL = 0, TILE_KV = 1, TILE_Q = 2 };
-template <class C, int TT>
+// Paged cache: the tile's blocks are table[b][t / bs + i] for i < ceil(n / bs) (one block when
+// bs >= 128); loaded ahead by the producer so the lookup latency hides behind a stage wait.
+constexpr int TC5_MAX_BLK = 8;  // 128-token tile / smallest block (16)
+template <int TT>
+__device__ __forceinline__ void load_tile_blocks(const DecodeParams& p, const TileCursor<TT>& c,
+                                                 int (&ent)[TC5_MAX_BLK]) {
+    const int nb = p.bs >= TT ? 1 : (c.n() + p.bs - 1) / p.bs;
+    const int32_t* row = p.table + (size_t)c.it.b * p.max_blocks + c.t / p.bs;
+#pragma unroll
+    for (int i = 0; i < TC5_MAX_BLK; ++i) ent[i] = i < nb ? __ldg(row + i) : 0;
+}
+template <class C, int TT, bool PAGED>
 __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const TileCursor<TT>& c,
                                                uint32_t ring, uint64_t* full_bar, int stage,
                                                uint64_t pol, const CUtensorMap* tmK,
                                                const CUtensorMap* tmV, const CUtensorMap* tmKf,
-                                               const CUtensorMap* tmVf, int part = TILE_ALL) {
+                                               const CUtensorMap* tmVf, int part,
+                                               const int (&ent)[TC5_MAX_BLK]) {
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
     const uint32_t vs = ks + C::TILE_BYTES;
     const uint32_t qs = vs + C::TILE_BYTES;
-    const bool full = n == TT;
-    const int nbox = full ? 1 : (n + C::BOX_ROWS - 1) / C::BOX_ROWS;
-    const int rows = full ? TT : C::BOX_ROWS;
+    constexpr bool paged = PAGED;
+    const bool full = n == TT && !paged;
+    const int rows = paged ? p.box_rows : (full ? TT : C::BOX_ROWS);
+    const int nbox = full ? 1 : (n + rows - 1) / rows;
     const bool with_q = c.first();
     const uint32_t kv_bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
     const uint32_t q_bytes = with_q ? (uint32_t)(C::G * C::ROWB) : 0u;
@@ -157,7 +170,28 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     } else {
         mbar_arrive_expect_tx(&full_bar[stage], kv_bytes + q_bytes);
     }
-    if (part != TILE_Q) {
+    if constexpr (PAGED) {
+      if (part != TILE_Q) {
+        // one box per block (or per 128-row piece of a larger block), from the block's rows
+#pragma unroll
+        for (int bx = 0; bx < TC5_MAX_BLK; ++bx) {
+            if (bx >= nbox) break;
+            int e = ent[bx];
+            if ((unsigned)e >= (unsigned)p.num_blocks) {
+                atomicOr(p.err, DEV_BAD_BLOCK);
+                e = 0;
+            }
+            const int tt = c.t + bx * rows;
+            const int row = (int)(((int64_t)e * p.H_kv + c.it.h) * p.bs + tt % p.bs);
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf) {
+                const uint32_t off = hf * C::HALF_BYTES + bx * rows * 128;
+                tma_load_2d(ks + off, tmK, hf * 64, row, &full_bar[stage], pol);
+                tma_load_2d(vs + off, tmV, hf * 64, row, &full_bar[stage], pol);
+            }
+        }
+      }
+    } else if (part != TILE_Q) {
         const int row0 = (int)(unit * p.T_max + c.t);
         const CUtensorMap* mk = full ? tmKf : tmK;
         const CUtensorMap* mv = full ? tmVf : tmV;
@@ -199,7 +233,7 @@ __device__ __forceinline__ bool softmax_group_any(bool pred) {
 // segment this CTA completes) while the next segment streams.
 // Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
 // the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
-template <int G>
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     decode_tc5_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
@@ -298,24 +332,23 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     __syncthreads();
 
     const int64_t W = (int64_t)H_kv * prefix[B];
-    int64_t P = p.P;
-    {
-        const int64_t want = W > 0 ? (W + p.min_tokens - 1) / p.min_tokens : 0;
-        if (want < P) P = want;
-    }
-    const int64_t r0 = W > 0 ? cta_begin(blockIdx.x, W, P) : 0;
-    const int64_t r1 = W > 0 ? cta_begin(blockIdx.x + 1, W, P) : 0;
+    const int64_t P = W > 0 ? plan_ctas(W, p.P, p.min_tokens, p.bs) : 0;
+    const int64_t r0 = W > 0 ? cta_cut(blockIdx.x, prefix, B, H_kv, W, P, p.bs) : 0;
+    const int64_t r1 = W > 0 ? cta_cut(blockIdx.x + 1, prefix, B, H_kv, W, P, p.bs) : 0;
     const bool work = W > 0 && (int64_t)blockIdx.x < P && r0 < r1;
     const uint32_t ring_s = smem_addr(ring);
     const uint64_t pol = policy_evict_first();
-    TileCursor<TT> pref;  // producer's cursor (thread 0)
-    int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
+    constexpr bool paged = PAGED;  // paged pool through the block table (separate instantiation)
+    TileCursor<TT> pref;       // producer's cursor (thread 0)
+    int ent[TC5_MAX_BLK] = {};  // paged: physical blocks of the tile at pref
+    int npre = 0;              // tiles whose K/V copies started before the grid dependency wait
     if (tid == 0 && work) {
         pref.init(prefix, B, H_kv, r0, r1);
         if (early)
             while (pref.valid && npre < NST && pref.t + pref.n() < pref.it.L) {
-                issue_tile_tc5<C, TT>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                      TILE_KV);
+                if constexpr (PAGED) load_tile_blocks<TT>(p, pref, ent);
+                issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
+                                      TILE_KV, ent);
                 issued[npre] += 1;
                 pref.advance();
                 ++npre;
@@ -341,20 +374,25 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             TileCursor<TT> c0;
             c0.init(prefix, B, H_kv, r0, r1);
             for (int i = 0; i < npre; ++i) {
-                issue_tile_tc5<C, TT>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf, TILE_Q);
+                issue_tile_tc5<C, TT, PAGED>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf, TILE_Q,
+                                      ent);
                 c0.advance();
             }
             int s = npre == NST ? 0 : npre;
             uint32_t ph = npre == NST ? 1u : 0u;
+            if constexpr (PAGED) if (pref.valid) load_tile_blocks<TT>(p, pref, ent);
             while (pref.valid) {
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err)) break;
                 // a tile that holds a stream's new token waits for the fused append's writes
                 if (fused && pref.t + pref.n() == pref.it.L &&
                     !mbar_wait(append_bar, 0u, abort_flag, p.err))
                     break;
-                issue_tile_tc5<C, TT>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf);
+                issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf,
+                                      TILE_ALL, ent);
                 issued[s] += 1;
                 pref.advance();
+                // the next tile's blocks load while this thread waits for a free stage
+                if constexpr (PAGED) if (pref.valid) load_tile_blocks<TT>(p, pref, ent);
                 if (++s == NST) { s = 0; ph ^= 1u; }
             }
         }
@@ -466,9 +504,17 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             SegIter it;
             it.init(prefix, B, H_kv, r0, r1);
             while (it.valid) {
+                int64_t arow = -1;
                 if (it.t1 == it.L) {
+                    if constexpr (PAGED)
+                        arow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max, it.b,
+                                         it.h, it.L - 1, p.err);
+                    else
+                        arow = ((int64_t)it.b * H_kv + it.h) * p.T_max + (it.L - 1);
+                }
+                if (arow >= 0) {
                     const size_t unit = (size_t)it.b * H_kv + it.h;
-                    const size_t dst = (unit * p.T_max + (size_t)(it.L - 1)) * C::ROWB;
+                    const size_t dst = (size_t)arow * C::ROWB;
                     const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + unit * C::ROWB);
                     const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + unit * C::ROWB);
                     uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + dst);
@@ -590,7 +636,8 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 }
             }
             // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2)
-            const int loaded = ((n + C::BOX_ROWS - 1) / C::BOX_ROWS) * C::BOX_ROWS;
+            const int br = paged ? p.box_rows : C::BOX_ROWS;
+            const int loaded = ((n + br - 1) / br) * br;
             if (row >= loaded) {
                 unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + row * 128;
 #pragma unroll

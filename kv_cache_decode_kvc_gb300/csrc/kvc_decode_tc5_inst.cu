@@ -1,6 +1,17 @@
 // kvc_decode_tc5_inst.cu -- instantiates the tcgen05 decode kernel (bf16 cache, D = 128); the
-// query-head group G is dispatched at run time.
+// query-head group G is dispatched at run time.  Compiled twice: KVC_TC5_PAGED = 0 for
+// contiguous caches (launch_decode_tc5_d128), 1 for paged pools (launch_decode_tc5p_d128), so
+// neither kernel carries the other's code.
 #include "kvc_decode_tc5.cuh"
+
+#ifndef KVC_TC5_PAGED
+#define KVC_TC5_PAGED 0
+#endif
+#if KVC_TC5_PAGED
+#define KVC_TC5_LAUNCHER launch_decode_tc5p_d128
+#else
+#define KVC_TC5_LAUNCHER launch_decode_tc5_d128
+#endif
 
 namespace kvc {
 
@@ -10,7 +21,7 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
     using C = Tc5Cfg<G>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G>,
+        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G, (bool)KVC_TC5_PAGED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return (int)e;
         attr_set = true;
@@ -29,12 +40,12 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc5_kernel<G>, p, maps[0], maps[1], maps[2], maps[3]);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc5_kernel<G, (bool)KVC_TC5_PAGED>, p, maps[0], maps[1], maps[2], maps[3]);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 
-int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+int KVC_TC5_LAUNCHER(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                            int* smem_out) {
     switch (G) {
         case 1: return launch_tc5_g<1>(p, maps, s, smem_out);

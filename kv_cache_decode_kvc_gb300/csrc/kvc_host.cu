@@ -27,7 +27,10 @@ struct kvc_cache {
     int math;                        // 0 automatic, 1 CUDA cores, 2 warp MMA, 3 tcgen05
     int overlap;                     // 1: early history reads before the preceding grid ends
     bool tc_ok;                      // tensor maps built (bf16 cache, rows < 2^31)
-    std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes)
+    std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes);
+                                     // paged: K, V, K, V with min(bs, 128)-row boxes
+    bool paged;                      // K / V of a layer are pools [num_blocks, H_kv, bs, D]
+    int bs, max_blocks, num_blocks;  // paged geometry (T_max = max_blocks * bs)
 };
 
 namespace {
@@ -95,7 +98,8 @@ int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cud
     int e;
     const int path = kvc_math_path(h);
     if (path == 3) {
-        e = kvc::launch_decode_tc5_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem);
+        e = h->paged ? kvc::launch_decode_tc5p_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem)
+                     : kvc::launch_decode_tc5_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem);
     } else if (path == 2) {
         const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
         const CUtensorMap& tv = h->tmaps[4 * (size_t)layer + 1];
@@ -129,11 +133,12 @@ int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cud
 }
 
 int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new, void* out,
-                const int32_t* lens, void* stream) {
+                const int32_t* table, const int32_t* lens, void* stream) {
     if (!h || !q || !out || !lens) return KVC_EINVAL;
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVC_EINVAL;
-    kvc::DecodeParams p;
+    if (h->paged != (table != nullptr)) return KVC_EINVAL;  // paged calls on paged handles only
+    kvc::DecodeParams p{};
     p.K = h->slab + (size_t)(2 * layer) * h->layer_bytes;
     p.V = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
     p.q = q;
@@ -150,6 +155,11 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.T_max = h->T_max;
     p.P = h->ctas > 0 ? h->ctas : h->sms;
     p.min_tokens = h->ctas > 0 ? 1 : 256;
+    p.table = table;
+    p.bs = h->paged ? h->bs : 1;
+    p.max_blocks = h->max_blocks;
+    p.num_blocks = h->num_blocks;
+    p.box_rows = h->paged ? (h->bs < kvc::TC_FULL_ROWS ? h->bs : kvc::TC_FULL_ROWS) : 0;
     const int U = h->B * h->H_kv;
     int mode = h->combine_mode;
     if (mode < 0) {
@@ -196,7 +206,49 @@ int kvc_plan_cta_of(int64_t x, int64_t W, int P) {
     return (int)kvc::cta_of(x, W, P);
 }
 
-int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
+namespace {
+// prefix[b] = sum of the valid lengths before b (host copy of the kernels' first step)
+int64_t plan_prefix(const int32_t* lens, int B, int T_max, std::vector<int64_t>& prefix) {
+    prefix.assign((size_t)B + 1, 0);
+    for (int b = 0; b < B; ++b)
+        prefix[b + 1] = prefix[b] + ((lens[b] >= 1 && lens[b] <= T_max) ? lens[b] : 0);
+    return prefix[B];
+}
+}  // namespace
+
+int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+                  int min_tokens, int64_t* cuts) {
+    if (!lens_host || !cuts || B < 1 || B > kvc::MAX_B || H_kv < 1 || P < 1 || min_tokens < 1 ||
+        block_size < 1)
+        return -1;
+    std::vector<int64_t> prefix;
+    const int64_t W = (int64_t)H_kv * plan_prefix(lens_host, B, T_max, prefix);
+    if (W == 0) return 0;
+    const int64_t Pu = kvc::plan_ctas(W, P, min_tokens, block_size);
+    for (int64_t i = 0; i <= Pu; ++i)
+        cuts[i] = kvc::cta_cut(i, prefix.data(), B, H_kv, W, Pu, block_size);
+    return (int)Pu;
+}
+
+int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+                         int min_tokens, int b, int h, int* first, int* last) {
+    if (!lens_host || !first || !last || B < 1 || B > kvc::MAX_B || b < 0 || b >= B || h < 0 ||
+        h >= H_kv || P < 1 || min_tokens < 1 || block_size < 1)
+        return KVC_EINVAL;
+    std::vector<int64_t> prefix;
+    const int64_t W = (int64_t)H_kv * plan_prefix(lens_host, B, T_max, prefix);
+    const int64_t L = prefix[b + 1] - prefix[b];
+    if (W == 0 || L == 0) return KVC_EINVAL;
+    const int64_t Pu = kvc::plan_ctas(W, P, min_tokens, block_size);
+    const int64_t us = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
+    *first = (int)kvc::cta_first_of_stream(us, L, W, Pu, block_size);
+    *last = (int)kvc::cta_of(us + L - 1, W, Pu);
+    return KVC_OK;
+}
+
+static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max,
+                         int dtype, int bs, int max_blocks, int num_blocks) {
+    const bool paged = bs > 0;
     if (!out) return KVC_EINVAL;
     *out = nullptr;
     if (layers < 1 || B < 1 || H_q < 1 || H_kv < 1 || D < 1 || T_max < 1) return KVC_EINVAL;
@@ -208,8 +260,13 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
     const int es = dtype == KVC_BF16 ? 2 : 4;
     // partition positions: B * H_kv * T_max < 2^50
     if ((double)B * H_kv * (double)T_max >= 1125899906842624.0) return KVC_ERANGE;
-    const uint64_t total = kvc_bytes_formula(layers, B, H_kv, D, T_max, es);
-    if (total == 0) return KVC_ERANGE;
+    // rows of one layer's K (or V): streams x T_max, or the pool's blocks x heads x bs
+    uint64_t rows = 0;
+    if (!mul_ok(paged ? (uint64_t)num_blocks : (uint64_t)B, (uint64_t)H_kv, &rows) ||
+        !mul_ok(rows, paged ? (uint64_t)bs : (uint64_t)T_max, &rows))
+        return KVC_ERANGE;
+    uint64_t total = 0;
+    if (!mul_ok(rows, 2ull * (uint64_t)layers * (uint64_t)D * (uint64_t)es, &total)) return KVC_ERANGE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ECUDA;
@@ -227,8 +284,12 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
     h->overlap = 0;
     h->math = 0;
     h->tc_ok = false;
+    h->paged = paged;
+    h->bs = paged ? bs : 1;
+    h->max_blocks = paged ? max_blocks : 0;
+    h->num_blocks = paged ? num_blocks : 0;
     h->max_ctas = 4 * h->sms;
-    h->layer_bytes = (size_t)B * H_kv * (size_t)T_max * D * es;
+    h->layer_bytes = (size_t)rows * D * es;
 
     const size_t U = (size_t)B * H_kv;
     const size_t slots = (size_t)h->max_ctas + U;
@@ -256,8 +317,10 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
         delete h;
         return KVC_ECUDA;
     }
-    // tensor maps for the tensor-core kernel (bf16 caches whose rows fit the map's coordinates)
-    const uint64_t rows = (uint64_t)B * H_kv * (uint64_t)T_max;
+    // tensor maps for the tensor-core kernels (bf16 caches whose rows fit the map's coordinates);
+    // a paged pool is copied one block (at most 128 rows) per box
+    const int box_small = paged ? (bs < kvc::TC_FULL_ROWS ? bs : kvc::TC_FULL_ROWS) : kvc::TC_BOX_ROWS;
+    const int box_full = paged ? box_small : kvc::TC_FULL_ROWS;
     if (dtype == KVC_BF16 && rows < (1ull << 31)) {
         h->tmaps.resize(4 * (size_t)layers);
         bool ok = true;
@@ -265,16 +328,33 @@ int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_ma
             void* kb = h->slab + (size_t)(2 * l) * h->layer_bytes;
             void* vb = h->slab + (size_t)(2 * l + 1) * h->layer_bytes;
             CUtensorMap* m4 = &h->tmaps[4 * (size_t)l];
-            ok = make_kv_tensor_map(&m4[0], kb, rows, D, kvc::TC_BOX_ROWS) &&
-                 make_kv_tensor_map(&m4[1], vb, rows, D, kvc::TC_BOX_ROWS) &&
-                 make_kv_tensor_map(&m4[2], kb, rows, D, kvc::TC_FULL_ROWS) &&
-                 make_kv_tensor_map(&m4[3], vb, rows, D, kvc::TC_FULL_ROWS);
+            ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
+                 make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
+                 make_kv_tensor_map(&m4[2], kb, rows, D, box_full) &&
+                 make_kv_tensor_map(&m4[3], vb, rows, D, box_full);
         }
         h->tc_ok = ok;
         if (!ok) h->tmaps.clear();
     }
     *out = h;
     return KVC_OK;
+}
+
+int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
+    return create_common(out, layers, B, H_q, H_kv, D, T_max, dtype, 0, 0, 0);
+}
+
+int kvc_create_paged(kvc_t* out, int layers, int num_blocks, int block_size, int B, int max_blocks,
+                     int H_q, int H_kv, int D, int dtype) {
+    if (!out) return KVC_EINVAL;
+    *out = nullptr;
+    if (num_blocks < 1 || max_blocks < 1) return KVC_EINVAL;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 &&
+        block_size != 256)
+        return KVC_EUNSUPPORTED;
+    if ((int64_t)max_blocks * block_size >= (1ll << 31)) return KVC_ERANGE;
+    return create_common(out, layers, B, H_q, H_kv, D, max_blocks * block_size, dtype, block_size,
+                         max_blocks, num_blocks);
 }
 
 int kvc_destroy(kvc_t h) {
@@ -289,7 +369,7 @@ int kvc_destroy(kvc_t h) {
 
 uint64_t kvc_bytes(kvc_t h) {
     if (!h) return 0;
-    return kvc_bytes_formula(h->layers, h->B, h->H_kv, h->D, h->T_max, h->es);
+    return 2ull * (uint64_t)h->layers * h->layer_bytes;  // paged: the whole block pool
 }
 
 uint64_t kvc_payload_bytes(kvc_t h, const int32_t* lens_host) {
@@ -334,6 +414,7 @@ int kvc_set_math(kvc_t h, int mode) {
     if (!h || mode < 0 || mode > 3) return KVC_EINVAL;
     if (mode >= 2 && !h->tc_ok) return KVC_EUNSUPPORTED;
     if (mode == 3 && h->D != 128) return KVC_EUNSUPPORTED;
+    if (mode == 2 && h->paged) return KVC_EUNSUPPORTED;  // the warp-MMA kernel reads contiguous caches
     h->math = mode;
     return KVC_OK;
 }
@@ -365,7 +446,8 @@ int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in
     if (!h || !K || !V || !lens) return KVC_EINVAL;
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
     if (T_in < 1 || T_in > h->T_max) return KVC_ERANGE;
-    kvc::CopyParams p;
+    if (h->paged) return KVC_EINVAL;
+    kvc::CopyParams p{};
     p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
     p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
     p.K = K;
@@ -381,7 +463,8 @@ int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const i
                void* stream) {
     if (!h || !k_new || !v_new || !lens) return KVC_EINVAL;
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
-    kvc::CopyParams p;
+    if (h->paged) return KVC_EINVAL;
+    kvc::CopyParams p{};
     p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
     p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
     p.K = k_new;
@@ -395,13 +478,68 @@ int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const i
 
 int kvc_decode_attn(kvc_t h, int layer, const void* q, void* out, const int32_t* lens,
                     void* stream) {
-    return attn_common(h, layer, q, nullptr, nullptr, out, lens, stream);
+    return attn_common(h, layer, q, nullptr, nullptr, out, nullptr, lens, stream);
 }
 
 int kvc_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
                     void* out, const int32_t* lens, void* stream) {
     if (!k_new || !v_new) return KVC_EINVAL;
-    return attn_common(h, layer, q, k_new, v_new, out, lens, stream);
+    return attn_common(h, layer, q, k_new, v_new, out, nullptr, lens, stream);
+}
+
+int kvc_paged_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in,
+                            const int32_t* block_table, const int32_t* lens, void* stream) {
+    if (!h || !K || !V || !lens || !block_table) return KVC_EINVAL;
+    if (!h->paged || layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    if (T_in < 1 || T_in > h->T_max) return KVC_ERANGE;
+    kvc::CopyParams p{};
+    p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.K = K;
+    p.V = V;
+    p.lens = lens;
+    p.err = h->err;
+    p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = T_in;
+    p.row_bytes = h->D * h->es;
+    p.table = block_table; p.bs = h->bs; p.max_blocks = h->max_blocks; p.num_blocks = h->num_blocks;
+    return kvc::launch_prefill(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
+}
+
+int kvc_paged_append(kvc_t h, int layer, const void* k_new, const void* v_new,
+                     const int32_t* block_table, const int32_t* lens, void* stream) {
+    if (!h || !k_new || !v_new || !lens || !block_table) return KVC_EINVAL;
+    if (!h->paged || layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    kvc::CopyParams p{};
+    p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.K = k_new;
+    p.V = v_new;
+    p.lens = lens;
+    p.err = h->err;
+    p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = 1;
+    p.row_bytes = h->D * h->es;
+    p.table = block_table; p.bs = h->bs; p.max_blocks = h->max_blocks; p.num_blocks = h->num_blocks;
+    return kvc::launch_append(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
+}
+
+int kvc_paged_decode_attn(kvc_t h, int layer, const void* q, void* out, const int32_t* block_table,
+                          const int32_t* lens, void* stream) {
+    if (!block_table) return KVC_EINVAL;
+    return attn_common(h, layer, q, nullptr, nullptr, out, block_table, lens, stream);
+}
+
+int kvc_paged_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                          void* out, const int32_t* block_table, const int32_t* lens, void* stream) {
+    if (!k_new || !v_new || !block_table) return KVC_EINVAL;
+    return attn_common(h, layer, q, k_new, v_new, out, block_table, lens, stream);
+}
+
+int kvc_get_paged_shape(kvc_t h, int* num_blocks, int* block_size, int* max_blocks) {
+    if (!h || !h->paged) return KVC_EINVAL;
+    if (num_blocks) *num_blocks = h->num_blocks;
+    if (block_size) *block_size = h->bs;
+    if (max_blocks) *max_blocks = h->max_blocks;
+    return KVC_OK;
 }
 
 int kvc_last_error(kvc_t h, void* stream, uint32_t* detail) {

@@ -11,6 +11,7 @@ namespace kvc {
 
 constexpr uint32_t DEV_BAD_LENS = 1u;      // mirrors KVC_DEV_BAD_LENS
 constexpr uint32_t DEV_WAIT_TIMEOUT = 2u;  // mirrors KVC_DEV_WAIT_TIMEOUT
+constexpr uint32_t DEV_BAD_BLOCK = 4u;     // mirrors KVC_DEV_BAD_BLOCK
 constexpr int MAX_B = 1024;
 // An in-kernel wait that has not completed after this long gives up, flags
 // DEV_WAIT_TIMEOUT and lets the kernel run to its end (no hang, output marked invalid).
@@ -26,6 +27,41 @@ __host__ __device__ inline int64_t cta_begin(int64_t i, int64_t W, int64_t P) {
 // CTA owning position x: the largest i with cta_begin(i) <= x.
 __host__ __device__ inline int64_t cta_of(int64_t x, int64_t W, int64_t P) {
     return ((x + 1) * P - 1) / W;
+}
+
+// Paged caches (block size bs > 1) round every cut down to a block boundary of the stream it
+// falls in, so each segment starts on a block and a 128-token tile covers whole blocks.
+// prefix[b] = sum_{b' < b} L_b' (B + 1 entries).  With W / P >= bs the rounded cuts stay
+// strictly increasing, so no CTA range is empty.  bs <= 1: the plain cut.
+__host__ __device__ inline int64_t cta_cut(int64_t i, const int64_t* prefix, int B, int H_kv,
+                                           int64_t W, int64_t P, int bs) {
+    const int64_t x = cta_begin(i, W, P);
+    if (bs <= 1 || x >= W) return x;
+    int lo = 0, hi = B - 1;  // largest b with H_kv * prefix[b] <= x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)H_kv * prefix[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int64_t L = prefix[lo + 1] - prefix[lo];
+    const int64_t base = (int64_t)H_kv * prefix[lo];
+    const int64_t ustart = base + ((x - base) / L) * L;
+    return ustart + ((x - ustart) / bs) * bs;
+}
+// CTAs actually used for W positions: at most P, at least min_tokens positions each, and for
+// a paged cache at least bs positions each (so rounded cuts never collide).
+__host__ __device__ inline int64_t plan_ctas(int64_t W, int64_t P, int min_tokens, int bs) {
+    int64_t want = (W + min_tokens - 1) / min_tokens;
+    if (bs > 1) {
+        const int64_t cap = W / bs > 1 ? W / bs : 1;
+        if (cap < want) want = cap;
+    }
+    return want < P ? want : P;
+}
+// First CTA holding stream tokens [ustart, ustart + L) under the rounded cuts.
+__host__ __device__ inline int64_t cta_first_of_stream(int64_t ustart, int64_t L, int64_t W,
+                                                       int64_t P, int bs) {
+    const int64_t reach = bs > 1 ? (L < bs ? L : (int64_t)bs) : 1;
+    return cta_of(ustart + reach - 1, W, P);
 }
 
 // ------------------------------------------------------------------ launch parameters
@@ -47,6 +83,12 @@ struct DecodeParams {
     int combine_mode;     // 0: the last CTA of a split stream merges it; 1: combine kernel
     float qscale;         // log2(e) / sqrt(D), folded into q
     int overlap;          // 1: lens and history rows may be read before the preceding grid ends
+    // paged cache (table == nullptr: contiguous [B, H_kv, T_max, D] layer)
+    const int32_t* table; // [B, max_blocks] physical block of each logical block
+    int bs;               // tokens per block (1 for a contiguous cache)
+    int max_blocks;
+    int num_blocks;       // K / V are pools [num_blocks, H_kv, bs, D]; T_max = max_blocks * bs
+    int box_rows;         // tcgen05 path: rows per tensor-copy box of a paged tile (min(bs, 128))
 };
 
 struct CopyParams {
@@ -58,6 +100,8 @@ struct CopyParams {
     uint32_t* err;
     int B, H_kv, T_max, T_in;
     int row_bytes;        // D * element bytes (a multiple of 16)
+    const int32_t* table; // paged cache: [B, max_blocks] block table, else nullptr
+    int bs, max_blocks, num_blocks;
 };
 
 // One launcher per (dtype, D) translation unit; G selects the instantiation.  Each returns
@@ -84,6 +128,9 @@ int launch_decode_tc_d256(int G, const DecodeParams& p, const CUtensorMap& tmK,
 // K and V with TC_FULL_ROWS-row boxes (whole 128-token tiles).
 int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                            int* smem_out);
+// the same kernel for a paged pool (p.table set; maps with min(bs, 128)-row boxes)
+int launch_decode_tc5p_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                            int* smem_out);
 constexpr int TC_BOX_ROWS = 32;
 constexpr int TC_FULL_ROWS = 128;
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s);
@@ -92,6 +139,28 @@ int launch_prefill(const CopyParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ device primitives
 #ifdef __CUDACC__
+// Cache row of token t of stream (b, h): contiguous [B, H_kv, T_max] rows, or through the block
+// table of a paged pool [num_blocks, H_kv, bs].  A table entry outside [0, num_blocks) flags
+// DEV_BAD_BLOCK and gives -1: readers then load row 0 instead (in bounds; that sequence's
+// output is unspecified), writers skip the row.
+__device__ __forceinline__ int64_t cache_row(const int32_t* table, int bs, int max_blocks,
+                                             int num_blocks, int H_kv, int T_max, int b, int h, int t,
+                                             uint32_t* err) {
+    if (table == nullptr) return ((int64_t)b * H_kv + h) * T_max + t;
+    const int e = __ldg(table + (size_t)b * max_blocks + t / bs);
+    if ((unsigned)e >= (unsigned)num_blocks) {
+        atomicOr(err, DEV_BAD_BLOCK);
+        return -1;
+    }
+    return ((int64_t)e * H_kv + h) * bs + (t % bs);
+}
+__device__ __forceinline__ int64_t cache_row_rd(const int32_t* table, int bs, int max_blocks,
+                                                int num_blocks, int H_kv, int T_max, int b, int h,
+                                                int t, uint32_t* err) {
+    const int64_t r = cache_row(table, bs, max_blocks, num_blocks, H_kv, T_max, b, h, t, err);
+    return r < 0 ? 0 : r;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -88,7 +88,7 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     // the counters must start at zero; the error word too when the kernel writes it here
     if (cudaMemsetAsync(base, 0, off_ml, s) != cudaSuccess) return KVC_ECUDA;
 
-    kvc::DecodeParams p;
+    kvc::DecodeParams p{};  // contiguous cache, no overlap
     p.K = K;
     p.V = V;
     p.q = q;
@@ -105,6 +105,7 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     p.T_max = T_max;
     p.P = sms;
     p.min_tokens = 256;
+    p.bs = 1;
     const long long nseg = ((long long)sms + (long long)U - 1) / (long long)U + 1;
     p.combine_mode = (nseg * G * D * 4 > 65536) ? 1 : 0;
     p.qscale = (float)(1.4426950408889634 / sqrt((double)D));

@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "kvc.h")
 
 KVC_BF16, KVC_F32 = 0, 1
 KVC_OK, KVC_EINVAL, KVC_ENOMEM, KVC_ECUDA, KVC_ERANGE, KVC_EDEVICE, KVC_EUNSUPPORTED = range(7)
-KVC_DEV_BAD_LENS, KVC_DEV_WAIT_TIMEOUT = 1, 2
+KVC_DEV_BAD_LENS, KVC_DEV_WAIT_TIMEOUT, KVC_DEV_BAD_BLOCK = 1, 2, 4
 
 _lib = None
 
@@ -63,8 +63,16 @@ def load() -> ctypes.CDLL:
         "kvc_get_launch_overlap": (I, [P]),
         "kvc_get_shape": (I, [P] + [ctypes.POINTER(I)] * 7),
         "kvc_plan_cta_of": (I, [I64, I64, I]),
+        "kvc_plan_cuts": (I, [P, I, I, I, I, I, I, P]),
+        "kvc_plan_stream_ctas": (I, [P, I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
         "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
+        "kvc_create_paged": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I, I, I]),
+        "kvc_paged_prefill_write": (I, [P, I, P, P, I, P, P, P]),
+        "kvc_paged_append": (I, [P, I, P, P, P, P, P]),
+        "kvc_paged_decode_attn": (I, [P, I, P, P, P, P, P]),
+        "kvc_paged_decode_step": (I, [P, I, P, P, P, P, P, P, P]),
+        "kvc_get_paged_shape": (I, [P] + [ctypes.POINTER(I)] * 3),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -133,6 +141,40 @@ def kvc_decode_attn(h, layer, q, out, lens, stream=None) -> None:
 def kvc_decode_step(h, layer, q, k_new, v_new, out, lens, stream=None) -> None:
     _check(load().kvc_decode_step(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                   _ptr(lens), _stream(stream)), "kvc_decode_step")
+
+
+def kvc_create_paged(layers, num_blocks, block_size, B, max_blocks, H_q, H_kv, D, dtype) -> int:
+    h = ctypes.c_void_p()
+    _check(load().kvc_create_paged(ctypes.byref(h), layers, num_blocks, block_size, B, max_blocks,
+                                   H_q, H_kv, D, dtype), "kvc_create_paged")
+    return h.value
+
+
+def kvc_paged_prefill_write(h, layer, K, V, T_in, block_table, lens, stream=None) -> None:
+    _check(load().kvc_paged_prefill_write(h, layer, _ptr(K), _ptr(V), T_in, _ptr(block_table),
+                                          _ptr(lens), _stream(stream)), "kvc_paged_prefill_write")
+
+
+def kvc_paged_append(h, layer, k_new, v_new, block_table, lens, stream=None) -> None:
+    _check(load().kvc_paged_append(h, layer, _ptr(k_new), _ptr(v_new), _ptr(block_table), _ptr(lens),
+                                   _stream(stream)), "kvc_paged_append")
+
+
+def kvc_paged_decode_attn(h, layer, q, out, block_table, lens, stream=None) -> None:
+    _check(load().kvc_paged_decode_attn(h, layer, _ptr(q), _ptr(out), _ptr(block_table), _ptr(lens),
+                                        _stream(stream)), "kvc_paged_decode_attn")
+
+
+def kvc_paged_decode_step(h, layer, q, k_new, v_new, out, block_table, lens, stream=None) -> None:
+    _check(load().kvc_paged_decode_step(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                        _ptr(block_table), _ptr(lens), _stream(stream)),
+           "kvc_paged_decode_step")
+
+
+def kvc_get_paged_shape(h) -> dict:
+    vals = [ctypes.c_int() for _ in range(3)]
+    _check(load().kvc_get_paged_shape(h, *[ctypes.byref(v) for v in vals]), "kvc_get_paged_shape")
+    return dict(zip(("num_blocks", "block_size", "max_blocks"), (v.value for v in vals)))
 
 
 def kvc_bytes(h) -> int:
@@ -295,3 +337,34 @@ def _wrap_device(ptr: int, shape, dtype):
     if dtype == torch.bfloat16:
         t = t.view(torch.bfloat16)
     return t
+
+
+class PagedKVCache(KVCache):
+    """Owns one paged kvc handle: per layer, K and V block pools [num_blocks, H_kv, block_size, D]
+    reached through a caller-owned block table [B, max_blocks] (int32, device)."""
+
+    def __init__(self, layers, num_blocks, block_size, B, max_blocks, H_q, H_kv, D, dtype="bf16"):
+        self.dtype_code = {"bf16": KVC_BF16, "f32": KVC_F32, KVC_BF16: KVC_BF16, KVC_F32: KVC_F32}[dtype]
+        self.layers, self.B, self.H_q, self.H_kv, self.D = layers, B, H_q, H_kv, D
+        self.num_blocks, self.block_size, self.max_blocks = num_blocks, block_size, max_blocks
+        self.T_max = max_blocks * block_size
+        self.h = kvc_create_paged(layers, num_blocks, block_size, B, max_blocks, H_q, H_kv, D,
+                                  self.dtype_code)
+
+    def layer_views(self, layer):
+        """torch views (no copy) of layer `layer`'s K and V block pools."""
+        kp, vp = kvc_layer_ptrs(self.h, layer)
+        shape = (self.num_blocks, self.H_kv, self.block_size, self.D)
+        return _wrap_device(kp, shape, self.torch_dtype), _wrap_device(vp, shape, self.torch_dtype)
+
+    def prefill_write(self, layer, K, V, block_table, lens, stream=None):
+        kvc_paged_prefill_write(self.h, layer, K, V, K.shape[2], block_table, lens, stream)
+
+    def append(self, layer, k_new, v_new, block_table, lens, stream=None):
+        kvc_paged_append(self.h, layer, k_new, v_new, block_table, lens, stream)
+
+    def decode_attn(self, layer, q, out, block_table, lens, stream=None):
+        kvc_paged_decode_attn(self.h, layer, q, out, block_table, lens, stream)
+
+    def decode_step(self, layer, q, k_new, v_new, out, block_table, lens, stream=None):
+        kvc_paged_decode_step(self.h, layer, q, k_new, v_new, out, block_table, lens, stream)
