@@ -163,10 +163,11 @@ def run_reference(args, w):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def traffic_from_profiles(kernel_src_hash: str):
+def traffic_from_profiles(kernel_src_hash: str, paged: int = 0):
     """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_gqa8b_b24.md")
+    name = f"decode_kernel_gqa8b_b24_paged{paged}.md" if paged else "decode_kernel_gqa8b_b24.md"
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     vals = {}
@@ -197,7 +198,7 @@ def run_ours(args, w):
 
     from kv_cache_decode_kvc_gb300 import kvc
     from kv_cache_decode_kvc_gb300.replicas import env_rank, max_over_ranks, replica_seed, whole_job_rate
-    from kv_cache_decode_kvc_gb300.workloads import fill_layer, step_inputs
+    from kv_cache_decode_kvc_gb300.workloads import fill_layer, paged_table, step_inputs
 
     rank, local, world = env_rank()
     torch.cuda.set_device(local)
@@ -212,13 +213,20 @@ def run_ours(args, w):
 
     seed = replica_seed(w.seed, rank)  # each replica decodes its own batch (weak scaling)
     L = w.layers
-    cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
+    table_d = None
+    if args.paged:
+        # the same sequences in a paged pool: block_size-token blocks at shuffled pool positions
+        table, num_blocks, max_blocks = paged_table(w, args.paged, spare=w.B)
+        cache = kvc.PagedKVCache(L, num_blocks, args.paged, w.B, max_blocks, w.H_q, w.H_kv, w.D, w.dtype)
+        table_d = table.to(dev)
+    else:
+        cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
     # the launch preceding each decode launch is the previous layer's decode step, which writes
     # neither lens nor this layer's history rows: early history loads are allowed
     cache.set_launch_overlap(0 if args.no_overlap else 1)
     t_fill = time.perf_counter()
     for layer in range(L):
-        fill_layer(cache, layer, w, seed=seed)
+        fill_layer(cache, layer, w, seed=seed, table=table_d)
     ins = [step_inputs(w, layer, seed=seed) for layer in range(L)]
     outs = [torch.empty(w.B, w.H_q, w.D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
     lens_d = w.lens().to(dev)
@@ -227,10 +235,16 @@ def run_ours(args, w):
     stream = torch.cuda.Stream(device=dev)
     sptr = stream.cuda_stream
 
+    def decode(layer, q, kn, vn, out, lens):
+        if table_d is None:
+            kvc.kvc_decode_step(cache.h, layer, q, kn, vn, out, lens, sptr)
+        else:
+            kvc.kvc_paged_decode_step(cache.h, layer, q, kn, vn, out, table_d, lens, sptr)
+
     def step():
         for layer in range(L):
             q, kn, vn = ins[layer]
-            kvc.kvc_decode_step(cache.h, layer, q, kn, vn, outs[layer], lens_d, sptr)
+            decode(layer, q, kn, vn, outs[layer], lens_d)
 
     # the automatic merge path adds a combine kernel per layer when streams are few and long
     # (same rule as the library: segments per stream x group outputs above 64 KB)
@@ -293,7 +307,7 @@ def run_ours(args, w):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 q, kn, vn = ins[layer]
-                kvc.kvc_decode_step(cache.h, layer, q, kn, vn, outs[layer], lens_d, sptr)
+                decode(layer, q, kn, vn, outs[layer], lens_d)
                 b.record(stream)
                 evs.append((a, b))
     torch.cuda.synchronize()
@@ -302,14 +316,16 @@ def run_ours(args, w):
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
     alg_bytes_launch = (w.kv_read_bytes_per_layer() + 2 * B * Hq * D * s  # q read, out written
                         + 4 * B * Hkv * D * s + 4 * B)                    # k/v new read + written, lens
+    if args.paged:  # each block-table entry a sequence uses, read once
+        alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
     # average launch duration over the timed region (graph replay, gaps included)
     region_launch_ms = ms_local / launches_per_step
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
-    traffic = traffic_from_profiles(kernel_source_hash())
+    traffic = traffic_from_profiles(kernel_source_hash(), args.paged)
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
-                   3: f"decode_tc5_kernel<{w.G}> (tcgen05)"}[path]
+                   3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'contiguous'}> (tcgen05)"}[path]
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     h_q = [i[0].cpu().pin_memory() for i in ins]
@@ -330,7 +346,7 @@ def run_ours(args, w):
             d_q[layer].copy_(h_q[layer], non_blocking=True)
             d_kn[layer].copy_(h_kn[layer], non_blocking=True)
             d_vn[layer].copy_(h_vn[layer], non_blocking=True)
-            kvc.kvc_decode_step(cache.h, layer, d_q[layer], d_kn[layer], d_vn[layer], outs[layer], d_lens, sptr)
+            decode(layer, d_q[layer], d_kn[layer], d_vn[layer], outs[layer], d_lens)
             h_out[layer].copy_(outs[layer], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -370,7 +386,8 @@ def run_ours(args, w):
             "attn_tokens_per_s": round(world * w.B / (ms * 1e-3), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (counter-based generator, bf16)",
-            "config": {"workload": w.name, "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
+            "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else ""),
+                       "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
                        "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
                        "kv_bytes_per_step": kv_bytes_step,
                        "l2": "inputs larger than L2 (each layer has its own cache; "
@@ -405,6 +422,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128, 256],
+                    help="run the workload from a paged cache with this block size (0: contiguous)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch overlap off: nothing is read before the preceding launch ends")
     ap.add_argument("--no-cpu-baseline", action="store_true")

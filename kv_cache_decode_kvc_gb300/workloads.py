@@ -73,9 +73,22 @@ WORKLOADS = {
 HEADLINE = "gqa8b_b24_ragged3000_6000"
 
 
+def paged_table(w: Workload, block_size: int, spare: int = 0):
+    """Block table for a paged copy of the workload: every sequence gets ceil(T_max / block_size)
+    logical blocks, mapped to a seeded random permutation of a pool with `spare` unused blocks,
+    so logically adjacent blocks are never adjacent in memory.  Returns (table int32 [B,
+    max_blocks] on the CPU, num_blocks, max_blocks)."""
+    max_blocks = -(-w.T_max() // block_size)
+    num_blocks = w.B * max_blocks + spare
+    g = torch.Generator().manual_seed(w.seed + 101 * block_size)
+    table = torch.randperm(num_blocks, generator=g)[: w.B * max_blocks].to(torch.int32)
+    return table.view(w.B, max_blocks).contiguous(), num_blocks, max_blocks
+
+
 def fill_layer(cache, layer: int, w: Workload, seed: int | None = None, device="cuda",
-               chunk_elems: int = 1 << 26):
-    """Write the layer's seeded history (slots [0, T_b)) through kvc_prefill_write."""
+               chunk_elems: int = 1 << 26, table=None):
+    """Write the layer's seeded history (slots [0, T_b)) through kvc_prefill_write (through
+    kvc_paged_prefill_write with `table`, a device block table, for a paged cache)."""
     seed = w.seed if seed is None else seed
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     lp = w.lens_pre()
@@ -88,7 +101,10 @@ def fill_layer(cache, layer: int, w: Workload, seed: int | None = None, device="
         b1 = min(w.B, b0 + step)
         K[b0:b1] = synth.block(seed, layer, "K", b0, b1, w.H_kv, 0, T_in, w.D, w.B, dt, device)
         V[b0:b1] = synth.block(seed, layer, "V", b0, b1, w.H_kv, 0, T_in, w.D, w.B, dt, device)
-    cache.prefill_write(layer, K, V, lp.to(device))
+    if table is None:
+        cache.prefill_write(layer, K, V, lp.to(device))
+    else:
+        cache.prefill_write(layer, K, V, table, lp.to(device))
     del K, V
 
 
