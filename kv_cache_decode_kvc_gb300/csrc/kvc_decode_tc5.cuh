@@ -132,24 +132,44 @@ __device__ __forceinline__ void tc5_ld16(uint32_t taddr, float (&v)[16]) {
 // stage's barrier without arriving and starts the K/V copies; TILE_Q then adds q (first tile
 // of a segment) and arrives, so the stage cannot complete before q is in.
 enum { TILE_ALL = 0, TILE_KV = 1, TILE_Q = 2 };
-// Paged cache: the tile's blocks are table[b][t / bs + i] for i < ceil(n / bs) (one block when
-// bs >= 128); loaded ahead by the producer so the lookup latency hides behind a stage wait.
-constexpr int TC5_MAX_BLK = 8;  // 128-token tile / smallest block (16)
-template <int TT>
-__device__ __forceinline__ void load_tile_blocks(const DecodeParams& p, const TileCursor<TT>& c,
-                                                 int (&ent)[TC5_MAX_BLK]) {
-    const int nb = p.bs >= TT ? 1 : (c.n() + p.bs - 1) / p.bs;
-    const int32_t* row = p.table + (size_t)c.it.b * p.max_blocks + c.t / p.bs;
-#pragma unroll
-    for (int i = 0; i < TC5_MAX_BLK; ++i) ent[i] = i < nb ? __ldg(row + i) : 0;
+// 4-D tensor copy for a paged pool: the map views the pool's rows as (64 columns, 8 rows, 2
+// column blocks, row groups of 8) with strides (2, 256, 128, 2048) bytes, so one box of `groups`
+// row groups arrives as [group][column block][8 rows x 128 B]: 8-row swizzle atoms of the two
+// column blocks interleaved (column-block stride 1024 B, group stride 2048 B).  `group` is the
+// first row / 8 (block rows start at multiples of 16).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int group, int groups,
+                                            uint64_t* bar, uint64_t policy) {
+    (void)groups;  // fixed by the map's box
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+        "cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(group), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
 }
+// Shared-memory layout of a K / V tile: contiguous caches [column block][128 rows][128 B]
+// (2-D copies); paged pools [8-row group][column block][8 rows][128 B] (4-D copies above).
+template <class C, bool PAGED>
+struct Tc5Layout {
+    static constexpr uint32_t HSTR = PAGED ? 1024u : (uint32_t)C::HALF_BYTES;  // column-block stride
+    static constexpr uint32_t GSTR = PAGED ? 2048u : 1024u;                    // 8-row group stride
+};
+// Paged cache: the tile's blocks are table[b][t / bs + i] for i < ceil(n / bs) (one block when
+// bs >= 128).  The whole producer warp runs a paged tile: lane i looks up block i (ahead, so the
+// lookup latency hides behind a stage wait) and issues its copies.
+template <int TT>
+__device__ __forceinline__ int tile_block(const DecodeParams& p, const TileCursor<TT>& c, int lane) {
+    const int nb = p.bs >= TT ? 1 : (c.n() + p.bs - 1) / p.bs;
+    return lane < nb ? __ldg(p.table + (size_t)c.it.b * p.max_blocks + c.t / p.bs + lane) : 0;
+}
+// Run by lane 0 of the producer warp (contiguous) or by the whole warp (paged, lane = block).
 template <class C, int TT, bool PAGED>
 __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const TileCursor<TT>& c,
                                                uint32_t ring, uint64_t* full_bar, int stage,
                                                uint64_t pol, const CUtensorMap* tmK,
                                                const CUtensorMap* tmV, const CUtensorMap* tmKf,
-                                               const CUtensorMap* tmVf, int part,
-                                               const int (&ent)[TC5_MAX_BLK]) {
+                                               const CUtensorMap* tmVf, int part, int ent,
+                                               int lane) {
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
@@ -162,35 +182,34 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     const bool with_q = c.first();
     const uint32_t kv_bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
     const uint32_t q_bytes = with_q ? (uint32_t)(C::G * C::ROWB) : 0u;
-    if (part == TILE_Q) {
-        if (with_q) mbar_arrive_expect_tx(&full_bar[stage], q_bytes);
-        else mbar_arrive(&full_bar[stage]);
-    } else if (part == TILE_KV) {
-        mbar_expect_tx(&full_bar[stage], kv_bytes);
-    } else {
-        mbar_arrive_expect_tx(&full_bar[stage], kv_bytes + q_bytes);
+    if (lane == 0) {
+        if (part == TILE_Q) {
+            if (with_q) mbar_arrive_expect_tx(&full_bar[stage], q_bytes);
+            else mbar_arrive(&full_bar[stage]);
+        } else if (part == TILE_KV) {
+            mbar_expect_tx(&full_bar[stage], kv_bytes);
+        } else {
+            mbar_arrive_expect_tx(&full_bar[stage], kv_bytes + q_bytes);
+        }
     }
     if constexpr (PAGED) {
-      if (part != TILE_Q) {
-        // one box per block (or per 128-row piece of a larger block), from the block's rows
-#pragma unroll
-        for (int bx = 0; bx < TC5_MAX_BLK; ++bx) {
-            if (bx >= nbox) break;
-            int e = ent[bx];
-            if ((unsigned)e >= (unsigned)p.num_blocks) {
-                atomicOr(p.err, DEV_BAD_BLOCK);
-                e = 0;
-            }
-            const int tt = c.t + bx * rows;
-            const int row = (int)(((int64_t)e * p.H_kv + c.it.h) * p.bs + tt % p.bs);
-#pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf) {
-                const uint32_t off = hf * C::HALF_BYTES + bx * rows * 128;
-                tma_load_2d(ks + off, tmK, hf * 64, row, &full_bar[stage], pol);
-                tma_load_2d(vs + off, tmV, hf * 64, row, &full_bar[stage], pol);
+        if (part != TILE_Q) {
+            __syncwarp();  // the stage's expected bytes are registered before any copy lands
+            // lane bx: box bx = block bx (or the 128-row piece of a larger block)
+            if (lane < nbox) {
+                int e = ent;
+                if ((unsigned)e >= (unsigned)p.num_blocks) {
+                    atomicOr(p.err, DEV_BAD_BLOCK);
+                    e = 0;
+                }
+                const int tt = c.t + lane * rows;
+                const int row = (int)(((int64_t)e * p.H_kv + c.it.h) * p.bs + tt % p.bs);
+                // both column blocks in one copy: the 4-D map lands [8-row group][half][8 rows][128 B]
+                const uint32_t off = (uint32_t)(lane * rows * C::ROWB);
+                tma_load_4d(ks + off, tmK, row >> 3, rows >> 3, &full_bar[stage], pol);
+                tma_load_4d(vs + off, tmV, row >> 3, rows >> 3, &full_bar[stage], pol);
             }
         }
-      }
     } else if (part != TILE_Q) {
         const int row0 = (int)(unit * p.T_max + c.t);
         const CUtensorMap* mk = full ? tmKf : tmK;
@@ -203,7 +222,7 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                 tma_load_2d(vs + off, mv, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
             }
     }
-    if (with_q && part != TILE_KV) {
+    if (with_q && part != TILE_KV && lane == 0) {
         asm volatile(
             "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
             "[%1], %2, [%3], %4;" ::"r"(qs),
@@ -339,17 +358,17 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     const uint32_t ring_s = smem_addr(ring);
     const uint64_t pol = policy_evict_first();
     constexpr bool paged = PAGED;  // paged pool through the block table (separate instantiation)
-    TileCursor<TT> pref;       // producer's cursor (thread 0)
-    int ent[TC5_MAX_BLK] = {};  // paged: physical blocks of the tile at pref
-    int npre = 0;              // tiles whose K/V copies started before the grid dependency wait
-    if (tid == 0 && work) {
+    TileCursor<TT> pref;  // producer's cursor (thread 0; the whole warp 0 when paged)
+    int ent = 0;          // paged: this lane's block of the tile at pref
+    int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
+    if (work && (PAGED ? warp == 0 : tid == 0)) {
         pref.init(prefix, B, H_kv, r0, r1);
         if (early)
             while (pref.valid && npre < NST && pref.t + pref.n() < pref.it.L) {
-                if constexpr (PAGED) load_tile_blocks<TT>(p, pref, ent);
+                if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
                 issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                      TILE_KV, ent);
-                issued[npre] += 1;
+                                             TILE_KV, ent, lane);
+                if (lane == 0) issued[npre] += 1;
                 pref.advance();
                 ++npre;
             }
@@ -369,30 +388,35 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        if (lane == 0) {
+        if (PAGED || lane == 0) {
             // finish the tiles started early: q (segment's first tile) and the arrival
             TileCursor<TT> c0;
             c0.init(prefix, B, H_kv, r0, r1);
             for (int i = 0; i < npre; ++i) {
-                issue_tile_tc5<C, TT, PAGED>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf, TILE_Q,
-                                      ent);
+                issue_tile_tc5<C, TT, PAGED>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf,
+                                             TILE_Q, ent, lane);
                 c0.advance();
             }
             int s = npre == NST ? 0 : npre;
             uint32_t ph = npre == NST ? 1u : 0u;
-            if constexpr (PAGED) if (pref.valid) load_tile_blocks<TT>(p, pref, ent);
+            if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
             while (pref.valid) {
-                if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err)) break;
-                // a tile that holds a stream's new token waits for the fused append's writes
-                if (fused && pref.t + pref.n() == pref.it.L &&
-                    !mbar_wait(append_bar, 0u, abort_flag, p.err))
-                    break;
+                // lane 0 waits; the warp follows its verdict (paged: every lane issues a block)
+                bool ok = true;
+                if (lane == 0) {
+                    ok = mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err);
+                    // a tile that holds a stream's new token waits for the fused append's writes
+                    if (ok && fused && pref.t + pref.n() == pref.it.L)
+                        ok = mbar_wait(append_bar, 0u, abort_flag, p.err);
+                }
+                if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
                 issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                      TILE_ALL, ent);
-                issued[s] += 1;
+                                             TILE_ALL, ent, lane);
+                if (lane == 0) issued[s] += 1;
                 pref.advance();
-                // the next tile's blocks load while this thread waits for a free stage
-                if constexpr (PAGED) if (pref.valid) load_tile_blocks<TT>(p, pref, ent);
+                // the next tile's blocks load while lane 0 waits for a free stage
+                if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
                 if (++s == NST) { s = 0; ph ^= 1u; }
             }
         }
@@ -411,8 +435,9 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
         constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, 0);  // V read MN-major x [P_hi; P_lo]
         const uint32_t qsw_s = smem_addr(qsw), pbuf_s = smem_addr(pbuf);
-        const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, 1024u);                    // + stage, block, k-step
-        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, (uint32_t)C::HALF_BYTES, 1024u);
+        using LY = Tc5Layout<C, PAGED>;
+        const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);                  // + stage, block, k-step
+        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
         const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
         const uint64_t dP0 = smem_desc_sw128(pbuf_s, 16u, 1024u);
         TileCursor<TT> cur;
@@ -433,7 +458,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                     const uint32_t pb = (uint32_t)((j & 1) * C::PBUF);
 #pragma unroll
                     for (int kk = 0; kk < TS; ++kk) {
-                        const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2048);
+                        const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2 * LY::GSTR);
                         const uint32_t poff = pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
                         tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
                     }
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 const uint32_t tS = tmem + (uint32_t)((k & 1) * N);
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
-                    const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32);
+                    const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * LY::HSTR + (kk & 3) * 32);
                     const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
                     tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
                 }
@@ -639,12 +664,13 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             const int br = paged ? p.box_rows : C::BOX_ROWS;
             const int loaded = ((n + br - 1) / br) * br;
             if (row >= loaded) {
-                unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + row * 128;
+                using LY = Tc5Layout<C, PAGED>;
+                unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + (row >> 3) * LY::GSTR + (row & 7) * 128;
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(vt + hf * C::HALF_BYTES + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vt + hf * LY::HSTR + c * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_async_smem();
             __syncwarp();

@@ -78,6 +78,22 @@ bool make_kv_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int D, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over a paged pool with D = 128 (rows of 256 bytes): dimensions (64 columns, 8 rows,
+// 2 column blocks, rows / 8 groups) with byte strides (256, 128, 2048) for dimensions 1..3, so
+// one box of box_rows / 8 groups lands in shared memory as [group][column block][8 rows][128 B]
+// (128-byte swizzle); both column blocks of a block's rows come in one copy.
+bool make_paged_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) || rows % 8 != 0) return false;
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+    const cuuint64_t strides[3] = {256, 128, 2048};
+    const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // a * b with overflow detection (all operands >= 0)
 bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
     if (a != 0 && b > UINT64_MAX / a) return false;
@@ -321,17 +337,23 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     // a paged pool is copied one block (at most 128 rows) per box
     const int box_small = paged ? (bs < kvc::TC_FULL_ROWS ? bs : kvc::TC_FULL_ROWS) : kvc::TC_BOX_ROWS;
     const int box_full = paged ? box_small : kvc::TC_FULL_ROWS;
-    if (dtype == KVC_BF16 && rows < (1ull << 31)) {
+    if (dtype == KVC_BF16 && rows < (1ull << 31) && (!paged || D == 128)) {
         h->tmaps.resize(4 * (size_t)layers);
         bool ok = true;
         for (int l = 0; l < layers && ok; ++l) {
             void* kb = h->slab + (size_t)(2 * l) * h->layer_bytes;
             void* vb = h->slab + (size_t)(2 * l + 1) * h->layer_bytes;
             CUtensorMap* m4 = &h->tmaps[4 * (size_t)l];
-            ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
-                 make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
-                 make_kv_tensor_map(&m4[2], kb, rows, D, box_full) &&
-                 make_kv_tensor_map(&m4[3], vb, rows, D, box_full);
+            if (paged)  // the tcgen05 kernel's paged variant (D = 128) reads 4-D boxes
+                ok = make_paged_tensor_map(&m4[0], kb, rows, box_small) &&
+                     make_paged_tensor_map(&m4[1], vb, rows, box_small) &&
+                     make_paged_tensor_map(&m4[2], kb, rows, box_full) &&
+                     make_paged_tensor_map(&m4[3], vb, rows, box_full);
+            else
+                ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
+                     make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
+                     make_kv_tensor_map(&m4[2], kb, rows, D, box_full) &&
+                     make_kv_tensor_map(&m4[3], vb, rows, D, box_full);
         }
         h->tc_ok = ok;
         if (!ok) h->tmaps.clear();
