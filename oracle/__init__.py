@@ -64,6 +64,12 @@ def lib() -> ctypes.CDLL:
         L.oracle_paged_prefill_write.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I]
         L.oracle_paged_decode_attn.restype = I
         L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P]
+        L.oracle_window_decode_attn.restype = I
+        L.oracle_window_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
+        L.oracle_rolling_append.restype = I
+        L.oracle_rolling_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
+        L.oracle_rolling_decode_attn.restype = I
+        L.oracle_rolling_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
         L.oracle_set_fault.restype = None
         L.oracle_set_fault.argtypes = [I]
         L.oracle_get_fault.restype = I
@@ -163,6 +169,38 @@ def paged_decode_attn(q, Kp, Vp, table, lens, return_bad: bool = False):
     return (out, bad) if return_bad else out
 
 
+def window_decode_attn(q, Kc, Vc, lens, W, return_bad: bool = False):
+    """Sliding-window decode over a full-history cache [B,H_kv,T_max,D]: positions
+    [max(0, L-W), L).  out [B,H_q,D] float64."""
+    B, H_q, D = q.shape
+    _, H_kv, T_max, _ = Kc.shape
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros((B, H_q, D), dtype=np.float64)
+    bad = lib().oracle_window_decode_attn(_ptr(q), _ptr(Kc), _ptr(Vc), _ptr(lens), B, H_q, H_kv,
+                                          T_max, D, W, _dtype_code(q), _ptr(out))
+    return (out, bad) if return_bad else out
+
+
+def rolling_append(Kr, Vr, k_new, v_new, lens) -> int:
+    """In place: position lens[b]-1 into slot (lens[b]-1) mod W of the rolling cache [B,H_kv,W,D]."""
+    B, H_kv, W, D = Kr.shape
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_rolling_append(_ptr(Kr), _ptr(Vr), _ptr(k_new), _ptr(v_new), _ptr(lens), B,
+                                       H_kv, W, D, _dtype_code(Kr))
+
+
+def rolling_decode_attn(q, Kr, Vr, lens, return_bad: bool = False):
+    """Decode over a rolling cache [B,H_kv,W,D]: positions [max(0, L-W), L), position p in slot
+    p mod W.  out [B,H_q,D] float64."""
+    B, H_q, D = q.shape
+    _, H_kv, W, _ = Kr.shape
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros((B, H_q, D), dtype=np.float64)
+    bad = lib().oracle_rolling_decode_attn(_ptr(q), _ptr(Kr), _ptr(Vr), _ptr(lens), B, H_q, H_kv, W,
+                                           D, _dtype_code(q), _ptr(out))
+    return (out, bad) if return_bad else out
+
+
 def layer_full(x, WQ, WK, WV, WO, H_q, H_kv, D):
     """Path A (dense causal layer).  Returns (out[B,T,hidden], K[B,H_kv,T,D], V[...])."""
     x = np.ascontiguousarray(x, dtype=np.float64)
@@ -194,7 +232,8 @@ class planted_fault:
     """Context manager that plants a known mistake in the oracle (tests only).
 
     1 = interleaved GQA map (j mod H_kv), 2 = score scale 1/D, 3 = append one slot late,
-    4 = the new token left out of the attention, 5 = paged block stored token-major."""
+    4 = the new token left out of the attention, 5 = paged block stored token-major,
+    6 = sliding window one position too wide."""
 
     def __init__(self, which: int):
         self.which = which

@@ -342,6 +342,116 @@ int oracle_paged_decode_attn(const void* q, const void* Kp, const void* Vp, cons
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Sliding window and rolling cache.  With a window of W tokens the query of the newest token
+ * (position L-1) attends to the W most recent positions [max(0, L-W), L), and the cache only
+ * needs W slots: position p lives in slot p mod W, the oldest entry being overwritten
+ * ([W1D4] §2.7 and §1.6, the rolling cache of a sliding-window model; [M11] §8).
+ * ------------------------------------------------------------------------------------- */
+
+/* First position of the window of a sequence of length L. */
+static int window_start(int L, int W) {
+    int t0 = L - W;
+    if (g_fault == 6) t0 = L - W - 1; /* planted: one position too many */
+    return t0 > 0 ? t0 : 0;
+}
+
+/* Sliding-window decode over a full-history cache [B, H_kv, T_max, D]: positions
+ * [max(0, L-W), L).  out [B, H_q, D] double.  Returns the number of invalid rows. */
+int oracle_window_decode_attn(const void* q, const void* Kc, const void* Vc, const int32_t* lens,
+                              int B, int H_q, int H_kv, int T_max, int D, int W, int dtype,
+                              double* out) {
+    int bad = 0;
+    for (int r = 0; r < B * H_q; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (L < 1 || L > T_max || W < 1) {
+            if (j == 0) ++bad;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        int t0 = window_start(L, W), n = L - t0;
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)n);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        size_t base = (((size_t)b * H_kv + h) * (size_t)T_max + (size_t)t0) * D;
+        for (size_t i = 0; i < (size_t)n * D; ++i) {
+            Kd[i] = load_elem(Kc, dtype, base + i);
+            Vd[i] = load_elem(Vc, dtype, base + i);
+        }
+        decode_row_f64(qd, Kd, Vd, n, D, (size_t)D, o, sc);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(sc);
+    }
+    return bad;
+}
+
+/* Rolling cache [B, H_kv, W, D]: writes k_new/v_new of position lens[b]-1 into slot
+ * (lens[b]-1) mod W.  Returns the number of rows with lens[b] < 1 (skipped). */
+int oracle_rolling_append(void* Kr, void* Vr, const void* k_new, const void* v_new,
+                          const int32_t* lens, int B, int H_kv, int W, int D, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 1 || W < 1) {
+            ++bad;
+            continue;
+        }
+        int slot = (L - 1) % W;
+        for (int h = 0; h < H_kv; ++h) {
+            size_t dst = (((size_t)b * H_kv + h) * W + slot) * row;
+            size_t src = ((size_t)b * H_kv + h) * row;
+            memcpy((char*)Kr + dst, (const char*)k_new + src, row);
+            memcpy((char*)Vr + dst, (const char*)v_new + src, row);
+        }
+    }
+    return bad;
+}
+
+/* Decode over a rolling cache: positions [max(0, L-W), L) in position order, position p read
+ * from slot p mod W.  Returns the number of rows with lens[b] < 1 (zero output). */
+int oracle_rolling_decode_attn(const void* q, const void* Kr, const void* Vr, const int32_t* lens,
+                               int B, int H_q, int H_kv, int W, int D, int dtype, double* out) {
+    int bad = 0;
+    for (int r = 0; r < B * H_q; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (L < 1 || W < 1) {
+            if (j == 0) ++bad;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        int t0 = window_start(L, W), n = L - t0;
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)n * D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)n);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        for (int i = 0; i < n; ++i) {
+            size_t base = (((size_t)b * H_kv + h) * (size_t)W + (size_t)((t0 + i) % W)) * D;
+            for (int d = 0; d < D; ++d) {
+                Kd[(size_t)i * D + d] = load_elem(Kr, dtype, base + d);
+                Vd[(size_t)i * D + d] = load_elem(Vr, dtype, base + d);
+            }
+        }
+        decode_row_f64(qd, Kd, Vd, n, D, (size_t)D, o, sc);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(sc);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
  * One attention layer, two ways ([KVG] "两条数学等价的 decode 路径"; [W1D4] §1.3).
  * x: [B, T, hidden]; W_Q [hidden, H_q*D], W_K / W_V [hidden, H_kv*D], W_O [H_q*D, hidden],
  * all double, row-major.  No RoPE, no norm: the pages' single-layer teaching setting.
