@@ -152,6 +152,22 @@ int kvc_set_launch_overlap(kvc_t h, int on);
 int kvc_get_launch_overlap(kvc_t h);
 
 /* ---------------------------------------------------------------------------------------
+ * Rolling cache for sliding-window attention.  With a window of W tokens the newest query
+ * attends to the W most recent positions, and the cache needs only W slots: position p lives
+ * in slot p mod W, overwriting position p - W ("第 1 周 · Day 4" §2.7 and §1.6, the rolling
+ * cache of a sliding-window model; "11.7 KV Cache" §8).  kvc_create_rolling makes a contiguous
+ * handle [B, H_kv, W, D] per layer (T_max = W) whose calls read lens as positions, unbounded:
+ *   - kvc_append / kvc_decode_step write position lens[b] - 1 into slot (lens[b] - 1) mod W;
+ *   - kvc_decode_attn / kvc_decode_step attend over positions [max(0, lens[b] - W), lens[b]),
+ *     i.e. slots [0, min(lens[b], W)) (softmax over a set: the slot order does not matter);
+ *   - kvc_prefill_write takes T_in >= lens[b] positions and keeps the last W of them.
+ * lens[b] < 1 is invalid (KVC_DEV_BAD_LENS).  Math paths 0, 1, 3 (2 is KVC_EUNSUPPORTED).
+ * kvc_get_window returns W (0 for a handle that does not roll). */
+int kvc_create_rolling(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int window,
+                       int dtype);
+int kvc_get_window(kvc_t h);
+
+/* ---------------------------------------------------------------------------------------
  * Paged cache.  The pages describe storage cut into fixed-size blocks that are handed out on
  * demand and found through a table, with the attention arithmetic unchanged ("第 1 周 · Day 4"
  * §1.6; "KV 缓存", "先把它放回推理链路" and "成本转移、失败场景与常见误解"; "11.7 KV Cache" §8).

@@ -28,8 +28,9 @@ def _units():
              ("kvc_noalloc", "kvc_noalloc.cu", [])]
     for d in (64, 128, 256):
         units.append((f"kvc_decode_tc_d{d}", "kvc_decode_tc_inst.cu", [f"-DKVC_INST_D={d}"]))
-    units.append(("kvc_decode_tc5_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_PAGED=0"]))
-    units.append(("kvc_decode_tc5p_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_PAGED=1"]))
+    units.append(("kvc_decode_tc5_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=0"]))
+    units.append(("kvc_decode_tc5p_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=1"]))
+    units.append(("kvc_decode_tc5r_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=2"]))
     for dt, d in DECODE_INST:
         units.append((f"kvc_decode_{dt}_d{d}", "kvc_decode_inst.cu",
                       [f"-DKVC_INST_BF16={1 if dt == 'bf16' else 0}", f"-DKVC_INST_D={d}"]))

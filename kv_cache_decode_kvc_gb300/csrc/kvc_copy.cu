@@ -18,12 +18,14 @@ __global__ void append_kernel(const CopyParams p) {
     if (gw >= p.B * p.H_kv) return;
     const int b = gw / p.H_kv, h = gw - b * p.H_kv;
     const int L = p.lens[b];
-    if (L < 1 || L > p.T_max) {
+    if (L < 1 || (!p.rolling && L > p.T_max)) {
         if (h == 0 && lane == 0) atomicOr(p.err, DEV_BAD_LENS);
         return;
     }
+    // slot L - 1, or (L - 1) mod T_max in a rolling cache
+    const int slot = p.rolling ? (L - 1) % p.T_max : L - 1;
     const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b, h,
-                                   L - 1, p.err);
+                                   slot, p.err);
     if (drow < 0) return;
     const size_t dst = (size_t)drow * p.row_bytes;
     const size_t src = (size_t)gw * p.row_bytes;
@@ -54,10 +56,13 @@ __global__ void prefill_kernel(const CopyParams p) {
             continue;
         }
         if (t >= L) continue;
+        // a rolling cache keeps the last T_max positions, position t in slot t mod T_max
+        if (p.rolling && t < L - p.T_max) continue;
         const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + row * p.row_bytes) + v);
         const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + row * p.row_bytes) + v);
         const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b,
-                                       (int)(bh - (size_t)b * p.H_kv), t, p.err);
+                                       (int)(bh - (size_t)b * p.H_kv), p.rolling ? t % p.T_max : t,
+                                       p.err);
         if (drow < 0) continue;
         reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + drow * p.row_bytes)[v] = kx;
         reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + drow * p.row_bytes)[v] = vx;

@@ -188,23 +188,30 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
     unsigned char* vs = ks + C::TILE_BYTES;
     unsigned char* qs = vs + C::TILE_BYTES;
     const bool with_q = c.first();
-    const bool last_here = p.k_new != nullptr && (c.t + n == c.it.L);
-    const int nc = last_here ? n - 1 : n;
+    // tile row of the stream's new token in the fused step (-1: not in this tile)
+    int ns = -1;
+    if (p.k_new != nullptr) {
+        const int slot = new_row_slot(p, c.it.b, c.it.L);
+        if (slot >= c.t && slot < c.t + n) ns = slot - c.t;
+    }
     uint32_t bytes = (uint32_t)(2 * n * C::ROWB);
     if (with_q) bytes += C::G * C::ROWB;
     mbar_arrive_expect_tx(&full_bar[stage], bytes);
-    if (p.table == nullptr) {
-        const char* Kg = static_cast<const char*>(p.K) + (unit * p.T_max + c.t) * C::ROWB;
-        const char* Vg = static_cast<const char*>(p.V) + (unit * p.T_max + c.t) * C::ROWB;
-        if (nc > 0) {
-            bulk_g2s(ks, Kg, nc * C::ROWB, &full_bar[stage], pol);
-            bulk_g2s(vs, Vg, nc * C::ROWB, &full_bar[stage], pol);
+    // cache rows [r0, r1) of the tile
+    auto copy_rows = [&](int r0, int r1) {
+        if (r1 <= r0) return;
+        if (p.table == nullptr) {
+            const size_t off = (unit * p.T_max + c.t + r0) * C::ROWB;
+            bulk_g2s(ks + r0 * C::ROWB, static_cast<const char*>(p.K) + off, (r1 - r0) * C::ROWB,
+                     &full_bar[stage], pol);
+            bulk_g2s(vs + r0 * C::ROWB, static_cast<const char*>(p.V) + off, (r1 - r0) * C::ROWB,
+                     &full_bar[stage], pol);
+            return;
         }
-    } else {
         // paged: one copy per block piece (the rows of one (block, head) are contiguous)
-        for (int r = 0; r < nc;) {
+        for (int r = r0; r < r1;) {
             const int t = c.t + r;
-            const int m = (p.bs - t % p.bs) < (nc - r) ? (p.bs - t % p.bs) : (nc - r);
+            const int m = (p.bs - t % p.bs) < (r1 - r) ? (p.bs - t % p.bs) : (r1 - r);
             const int64_t row = cache_row_rd(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv,
                                              p.T_max, c.it.b, c.it.h, t, p.err);
             bulk_g2s(ks + r * C::ROWB, static_cast<const char*>(p.K) + row * C::ROWB, m * C::ROWB,
@@ -213,12 +220,17 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
                      &full_bar[stage], pol);
             r += m;
         }
-    }
-    if (last_here) {
-        bulk_g2s(ks + nc * C::ROWB, static_cast<const char*>(p.k_new) + unit * C::ROWB, C::ROWB,
+    };
+    if (ns < 0) {
+        copy_rows(0, n);
+    } else {
+        // the new row comes straight from k_new / v_new, the rest from the cache
+        copy_rows(0, ns);
+        bulk_g2s(ks + ns * C::ROWB, static_cast<const char*>(p.k_new) + unit * C::ROWB, C::ROWB,
                  &full_bar[stage], pol);
-        bulk_g2s(vs + nc * C::ROWB, static_cast<const char*>(p.v_new) + unit * C::ROWB, C::ROWB,
+        bulk_g2s(vs + ns * C::ROWB, static_cast<const char*>(p.v_new) + unit * C::ROWB, C::ROWB,
                  &full_bar[stage], pol);
+        copy_rows(ns + 1, n);
     }
     if (with_q)
         bulk_g2s(qs, static_cast<const char*>(p.q) + unit * C::G * C::ROWB, C::G * C::ROWB,
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
             int64_t x = 0;
             if (b < B) {
                 const int L = p.lens[b];
-                x = (L >= 1 && L <= p.T_max) ? L : 0;
+                x = eff_len(L, p.T_max, p.rolling);
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -632,14 +644,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                 }
             }
             // fused append: warp 0 stores the new token's rows (now in the tile) into the cache
-            const int64_t arow = (fused && warp == 0 && cur.t + n == cur.it.L)
+            const int nslot = (fused && warp == 0) ? new_row_slot(p, cur.it.b, cur.it.L) : -1;
+            const int64_t arow = (nslot >= cur.t && nslot < cur.t + n)
                                      ? cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max,
-                                                 cur.it.b, cur.it.h, cur.it.L - 1, p.err)
+                                                 cur.it.b, cur.it.h, nslot, p.err)
                                      : -1;
             if (arow >= 0) {
                 const size_t dst = (size_t)arow * C::ROWB;
-                const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(Ks) + (n - 1) * C::ROWB;
-                const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(Vs) + (n - 1) * C::ROWB;
+                const int tr = nslot - cur.t;  // the new row's place in the tile
+                const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(Ks) + tr * C::ROWB;
+                const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(Vs) + tr * C::ROWB;
                 unsigned char* kd = static_cast<unsigned char*>(const_cast<void*>(p.K)) + dst;
                 unsigned char* vd = static_cast<unsigned char*>(const_cast<void*>(p.V)) + dst;
                 for (int v = lane; v < C::NVR; v += 32) {
@@ -777,15 +791,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     int64_t before = 0, all = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
         const int L = p.lens[i];
-        const int64_t v = (L >= 1 && L <= p.T_max) ? L : 0;
+        const int64_t v = eff_len(L, p.T_max, p.rolling);
         all += v;
         if (i < b) before += v;
     }
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[0]), (unsigned long long)before);
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[1]), (unsigned long long)all);
     __syncthreads();
-    const int Lb = p.lens[b];
-    if (Lb < 1 || Lb > p.T_max) return;
+    const int Lb = eff_len(p.lens[b], p.T_max, p.rolling);
+    if (Lb == 0) return;
     const int64_t W = (int64_t)p.H_kv * sh_sum[1];
     const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
     const int64_t us = (int64_t)p.H_kv * sh_sum[0] + (int64_t)h * Lb;

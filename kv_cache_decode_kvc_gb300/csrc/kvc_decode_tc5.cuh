@@ -252,7 +252,30 @@ __device__ __forceinline__ bool softmax_group_any(bool pred) {
 // segment this CTA completes) while the next segment streams.
 // Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
 // the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
-template <int G, bool PAGED>
+// Slot of a stream's new row in the fused step (the row a preceding append may just have
+// written): the last row, or for a rolling cache of W = T_max slots, (lens[b] - 1) mod W.  The
+// rolling slot comes from lens[b] (one load per stream, kept while the cursor stays on it).
+template <bool ROLL>
+struct NewRow {
+    int b = -1, slot = 0;
+    __device__ __forceinline__ bool in_tile(const DecodeParams& p, int sb, int L, int t, int n) {
+        if constexpr (!ROLL) {
+            (void)p; (void)sb;
+            return t + n == L;
+        } else {
+            if (sb != b) {
+                b = sb;
+                slot = (__ldg(p.lens + sb) - 1) % p.T_max;
+            }
+            return t <= slot && slot < t + n;
+        }
+    }
+};
+
+// MODE: 0 contiguous cache, 1 paged pool (block table), 2 rolling cache (T_max = window slots,
+// position p in slot p mod T_max; lens may exceed T_max and the attention covers
+// min(lens, T_max) slots).  Each mode is its own instantiation.
+template <int G, int MODE>
 __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     decode_tc5_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
@@ -260,6 +283,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tmVf) {
     using C = Tc5Cfg<G>;
     using T = __nv_bfloat16;
+    constexpr bool PAGED = MODE == 1, ROLL = MODE == 2;
     constexpr int D = C::D, N = C::N, TT = C::TT, NST = C::NST, KS = D / 16, TS = TT / 16;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -336,7 +360,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             int64_t x = 0;
             if (b < B) {
                 const int L = p.lens[b];
-                x = (L >= 1 && L <= p.T_max) ? L : 0;
+                if (L >= 1 && (ROLL || L <= p.T_max)) x = ROLL && L > p.T_max ? p.T_max : L;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -359,12 +383,13 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     const uint64_t pol = policy_evict_first();
     constexpr bool paged = PAGED;  // paged pool through the block table (separate instantiation)
     TileCursor<TT> pref;  // producer's cursor (thread 0; the whole warp 0 when paged)
+    NewRow<ROLL> nrow;    // producer: where the stream's new row is
     int ent = 0;          // paged: this lane's block of the tile at pref
     int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
     if (work && (PAGED ? warp == 0 : tid == 0)) {
         pref.init(prefix, B, H_kv, r0, r1);
         if (early)
-            while (pref.valid && npre < NST && pref.t + pref.n() < pref.it.L) {
+            while (pref.valid && npre < NST && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
                 if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
                 issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
                                              TILE_KV, ent, lane);
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 if (lane == 0) {
                     ok = mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err);
                     // a tile that holds a stream's new token waits for the fused append's writes
-                    if (ok && fused && pref.t + pref.n() == pref.it.L)
+                    if (ok && fused && nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n()))
                         ok = mbar_wait(append_bar, 0u, abort_flag, p.err);
                 }
                 if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
@@ -530,7 +555,10 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             it.init(prefix, B, H_kv, r0, r1);
             while (it.valid) {
                 int64_t arow = -1;
-                if (it.t1 == it.L) {
+                if constexpr (ROLL) {
+                    const int slot = (__ldg(p.lens + it.b) - 1) % p.T_max;
+                    if (it.t0 <= slot && slot < it.t1) arow = ((int64_t)it.b * H_kv + it.h) * p.T_max + slot;
+                } else if (it.t1 == it.L) {
                     if constexpr (PAGED)
                         arow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max, it.b,
                                          it.h, it.L - 1, p.err);

@@ -1,14 +1,16 @@
 // kvc_decode_tc5_inst.cu -- instantiates the tcgen05 decode kernel (bf16 cache, D = 128); the
-// query-head group G is dispatched at run time.  Compiled twice: KVC_TC5_PAGED = 0 for
-// contiguous caches (launch_decode_tc5_d128), 1 for paged pools (launch_decode_tc5p_d128), so
-// neither kernel carries the other's code.
+// query-head group G is dispatched at run time.  Compiled once per cache mode, so no kernel
+// carries another mode's code: KVC_TC5_MODE = 0 contiguous (launch_decode_tc5_d128), 1 paged
+// pool (launch_decode_tc5p_d128), 2 rolling cache (launch_decode_tc5r_d128).
 #include "kvc_decode_tc5.cuh"
 
-#ifndef KVC_TC5_PAGED
-#define KVC_TC5_PAGED 0
+#ifndef KVC_TC5_MODE
+#define KVC_TC5_MODE 0
 #endif
-#if KVC_TC5_PAGED
+#if KVC_TC5_MODE == 1
 #define KVC_TC5_LAUNCHER launch_decode_tc5p_d128
+#elif KVC_TC5_MODE == 2
+#define KVC_TC5_LAUNCHER launch_decode_tc5r_d128
 #else
 #define KVC_TC5_LAUNCHER launch_decode_tc5_d128
 #endif
@@ -21,7 +23,7 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
     using C = Tc5Cfg<G>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G, (bool)KVC_TC5_PAGED>,
+        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G, KVC_TC5_MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return (int)e;
         attr_set = true;
@@ -40,7 +42,7 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc5_kernel<G, (bool)KVC_TC5_PAGED>, p, maps[0], maps[1], maps[2], maps[3]);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc5_kernel<G, KVC_TC5_MODE>, p, maps[0], maps[1], maps[2], maps[3]);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

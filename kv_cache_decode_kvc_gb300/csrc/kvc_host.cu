@@ -30,6 +30,7 @@ struct kvc_cache {
     std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes);
                                      // paged: K, V, K, V with min(bs, 128)-row boxes
     bool paged;                      // K / V of a layer are pools [num_blocks, H_kv, bs, D]
+    bool rolling;                    // T_max = window slots, position p in slot p mod T_max
     int bs, max_blocks, num_blocks;  // paged geometry (T_max = max_blocks * bs)
 };
 
@@ -114,8 +115,10 @@ int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cud
     int e;
     const int path = kvc_math_path(h);
     if (path == 3) {
-        e = h->paged ? kvc::launch_decode_tc5p_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem)
-                     : kvc::launch_decode_tc5_d128(h->G, p, &h->tmaps[4 * (size_t)layer], s, &smem);
+        const CUtensorMap* maps = &h->tmaps[4 * (size_t)layer];
+        e = h->paged     ? kvc::launch_decode_tc5p_d128(h->G, p, maps, s, &smem)
+            : h->rolling ? kvc::launch_decode_tc5r_d128(h->G, p, maps, s, &smem)
+                         : kvc::launch_decode_tc5_d128(h->G, p, maps, s, &smem);
     } else if (path == 2) {
         const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
         const CUtensorMap& tv = h->tmaps[4 * (size_t)layer + 1];
@@ -176,6 +179,7 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.max_blocks = h->max_blocks;
     p.num_blocks = h->num_blocks;
     p.box_rows = h->paged ? (h->bs < kvc::TC_FULL_ROWS ? h->bs : kvc::TC_FULL_ROWS) : 0;
+    p.rolling = h->rolling ? 1 : 0;
     const int U = h->B * h->H_kv;
     int mode = h->combine_mode;
     if (mode < 0) {
@@ -301,6 +305,7 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     h->math = 0;
     h->tc_ok = false;
     h->paged = paged;
+    h->rolling = false;
     h->bs = paged ? bs : 1;
     h->max_blocks = paged ? max_blocks : 0;
     h->num_blocks = paged ? num_blocks : 0;
@@ -364,6 +369,18 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
 
 int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
     return create_common(out, layers, B, H_q, H_kv, D, T_max, dtype, 0, 0, 0);
+}
+
+int kvc_create_rolling(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int window,
+                       int dtype) {
+    const int rc = create_common(out, layers, B, H_q, H_kv, D, window, dtype, 0, 0, 0);
+    if (rc == KVC_OK) (*out)->rolling = true;
+    return rc;
+}
+
+int kvc_get_window(kvc_t h) {
+    if (!h) return -1;
+    return h->rolling ? h->T_max : 0;
 }
 
 int kvc_create_paged(kvc_t* out, int layers, int num_blocks, int block_size, int B, int max_blocks,
@@ -436,7 +453,7 @@ int kvc_set_math(kvc_t h, int mode) {
     if (!h || mode < 0 || mode > 3) return KVC_EINVAL;
     if (mode >= 2 && !h->tc_ok) return KVC_EUNSUPPORTED;
     if (mode == 3 && h->D != 128) return KVC_EUNSUPPORTED;
-    if (mode == 2 && h->paged) return KVC_EUNSUPPORTED;  // the warp-MMA kernel reads contiguous caches
+    if (mode == 2 && (h->paged || h->rolling)) return KVC_EUNSUPPORTED;  // warp MMA: plain caches only
     h->math = mode;
     return KVC_OK;
 }
@@ -467,7 +484,7 @@ int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in
                       const int32_t* lens, void* stream) {
     if (!h || !K || !V || !lens) return KVC_EINVAL;
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
-    if (T_in < 1 || T_in > h->T_max) return KVC_ERANGE;
+    if (T_in < 1 || (!h->rolling && T_in > h->T_max)) return KVC_ERANGE;
     if (h->paged) return KVC_EINVAL;
     kvc::CopyParams p{};
     p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
@@ -478,6 +495,7 @@ int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in
     p.err = h->err;
     p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = T_in;
     p.row_bytes = h->D * h->es;
+    p.rolling = h->rolling ? 1 : 0;
     return kvc::launch_prefill(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
 }
 
@@ -495,6 +513,7 @@ int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const i
     p.err = h->err;
     p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = 1;
     p.row_bytes = h->D * h->es;
+    p.rolling = h->rolling ? 1 : 0;
     return kvc::launch_append(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
 }
 

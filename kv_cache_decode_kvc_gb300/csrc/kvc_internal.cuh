@@ -89,6 +89,7 @@ struct DecodeParams {
     int max_blocks;
     int num_blocks;       // K / V are pools [num_blocks, H_kv, bs, D]; T_max = max_blocks * bs
     int box_rows;         // tcgen05 path: rows per tensor-copy box of a paged tile (min(bs, 128))
+    int rolling;          // 1: rolling cache, T_max = window slots, position p in slot p mod T_max
 };
 
 struct CopyParams {
@@ -102,6 +103,7 @@ struct CopyParams {
     int row_bytes;        // D * element bytes (a multiple of 16)
     const int32_t* table; // paged cache: [B, max_blocks] block table, else nullptr
     int bs, max_blocks, num_blocks;
+    int rolling;          // rolling cache: position p in slot p mod T_max (lens may exceed T_max)
 };
 
 // One launcher per (dtype, D) translation unit; G selects the instantiation.  Each returns
@@ -128,8 +130,11 @@ int launch_decode_tc_d256(int G, const DecodeParams& p, const CUtensorMap& tmK,
 // K and V with TC_FULL_ROWS-row boxes (whole 128-token tiles).
 int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                            int* smem_out);
-// the same kernel for a paged pool (p.table set; maps with min(bs, 128)-row boxes)
+// the same kernel for a paged pool (p.table set; maps with min(bs, 128)-row boxes) and for a
+// rolling cache (p.rolling set)
 int launch_decode_tc5p_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                            int* smem_out);
+int launch_decode_tc5r_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                             int* smem_out);
 constexpr int TC_BOX_ROWS = 32;
 constexpr int TC_FULL_ROWS = 128;
@@ -139,6 +144,19 @@ int launch_prefill(const CopyParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ device primitives
 #ifdef __CUDACC__
+// Attended length of a sequence with post-append length L: 0 if invalid (L < 1, or L > T_max
+// for a cache that does not roll), min(L, T_max) for a rolling cache, else L.
+__host__ __device__ __forceinline__ int eff_len(int L, int T_max, int rolling) {
+    if (L < 1 || (!rolling && L > T_max)) return 0;
+    return rolling && L > T_max ? T_max : L;
+}
+
+// Slot of a sequence's new row in the fused step (the row an append writes): L_eff - 1, or for a
+// rolling cache (lens[b] - 1) mod T_max.
+__device__ __forceinline__ int new_row_slot(const DecodeParams& p, int b, int L_eff) {
+    return p.rolling ? (__ldg(p.lens + b) - 1) % p.T_max : L_eff - 1;
+}
+
 // Cache row of token t of stream (b, h): contiguous [B, H_kv, T_max] rows, or through the block
 // table of a paged pool [num_blocks, H_kv, bs].  A table entry outside [0, num_blocks) flags
 // DEV_BAD_BLOCK and gives -1: readers then load row 0 instead (in bounds; that sequence's

@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
         "kvc_status_str": (ctypes.c_char_p, [I]),
         "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
         "kvc_create_paged": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I, I, I]),
+        "kvc_create_rolling": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
+        "kvc_get_window": (I, [P]),
         "kvc_paged_prefill_write": (I, [P, I, P, P, I, P, P, P]),
         "kvc_paged_append": (I, [P, I, P, P, P, P, P]),
         "kvc_paged_decode_attn": (I, [P, I, P, P, P, P, P]),
@@ -141,6 +143,17 @@ def kvc_decode_attn(h, layer, q, out, lens, stream=None) -> None:
 def kvc_decode_step(h, layer, q, k_new, v_new, out, lens, stream=None) -> None:
     _check(load().kvc_decode_step(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                   _ptr(lens), _stream(stream)), "kvc_decode_step")
+
+
+def kvc_create_rolling(layers, B, H_q, H_kv, D, window, dtype) -> int:
+    h = ctypes.c_void_p()
+    _check(load().kvc_create_rolling(ctypes.byref(h), layers, B, H_q, H_kv, D, window, dtype),
+           "kvc_create_rolling")
+    return h.value
+
+
+def kvc_get_window(h) -> int:
+    return int(load().kvc_get_window(h))
 
 
 def kvc_create_paged(layers, num_blocks, block_size, B, max_blocks, H_q, H_kv, D, dtype) -> int:
@@ -368,3 +381,14 @@ class PagedKVCache(KVCache):
 
     def decode_step(self, layer, q, k_new, v_new, out, block_table, lens, stream=None):
         kvc_paged_decode_step(self.h, layer, q, k_new, v_new, out, block_table, lens, stream)
+
+
+class RollingKVCache(KVCache):
+    """Owns one rolling kvc handle: per layer a [B, H_kv, window, D] cache, position p in slot
+    p mod window; lens count positions and may exceed the window."""
+
+    def __init__(self, layers, B, H_q, H_kv, D, window, dtype="bf16"):
+        self.dtype_code = {"bf16": KVC_BF16, "f32": KVC_F32, KVC_BF16: KVC_BF16, KVC_F32: KVC_F32}[dtype]
+        self.layers, self.B, self.H_q, self.H_kv, self.D = layers, B, H_q, H_kv, D
+        self.window = self.T_max = window
+        self.h = kvc_create_rolling(layers, B, H_q, H_kv, D, window, self.dtype_code)
