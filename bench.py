@@ -219,6 +219,9 @@ def run_ours(args, w):
         table, num_blocks, max_blocks = paged_table(w, args.paged, spare=w.B)
         cache = kvc.PagedKVCache(L, num_blocks, args.paged, w.B, max_blocks, w.H_q, w.H_kv, w.D, w.dtype)
         table_d = table.to(dev)
+    elif args.window:
+        # sliding-window attention: a rolling cache of `window` slots per sequence
+        cache = kvc.RollingKVCache(L, w.B, w.H_q, w.H_kv, w.D, args.window, w.dtype)
     else:
         cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
     # the launch preceding each decode launch is the previous layer's decode step, which writes
@@ -294,7 +297,7 @@ def run_ours(args, w):
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
 
-    kv_bytes_step = L * w.kv_read_bytes_per_layer()
+    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window)
     gbs = whole_job_rate(world, kv_bytes_step, ms)
     peak, peak_kind = measured_peaks()
 
@@ -314,14 +317,14 @@ def run_ours(args, w):
     per_launch = [a.elapsed_time(b) for a, b in evs]
     launch_ms = statistics.mean(per_launch)
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
-    alg_bytes_launch = (w.kv_read_bytes_per_layer() + 2 * B * Hq * D * s  # q read, out written
+    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window) + 2 * B * Hq * D * s  # q read, out written
                         + 4 * B * Hkv * D * s + 4 * B)                    # k/v new read + written, lens
     if args.paged:  # each block-table entry a sequence uses, read once
         alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
     # average launch duration over the timed region (graph replay, gaps included)
     region_launch_ms = ms_local / launches_per_step
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
-    traffic = traffic_from_profiles(kernel_source_hash(), args.paged)
+    traffic = None if args.window else traffic_from_profiles(kernel_source_hash(), args.paged)
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
@@ -386,7 +389,8 @@ def run_ours(args, w):
             "attn_tokens_per_s": round(world * w.B / (ms * 1e-3), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (counter-based generator, bf16)",
-            "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else ""),
+            "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else "")
+                                   + (f", rolling cache, window {args.window}" if args.window else ""),
                        "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
                        "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
                        "kv_bytes_per_step": kv_bytes_step,
@@ -424,6 +428,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128, 256],
                     help="run the workload from a paged cache with this block size (0: contiguous)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window attention over a rolling cache of this many slots (0: off)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch overlap off: nothing is read before the preceding launch ends")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -433,6 +439,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.paged and args.window:
+        ap.error("--paged and --window are separate cache kinds")
     from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
     if args.layers:

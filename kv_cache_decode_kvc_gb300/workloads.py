@@ -48,9 +48,13 @@ class Workload:
     def T_max(self) -> int:
         return int(self.lens().max())
 
-    def kv_read_bytes_per_layer(self) -> int:
-        """Algorithmic KV bytes one decode step reads per layer: 2 H_kv D s sum_b L_b."""
-        return 2 * self.H_kv * self.D * self.elem_bytes * int(self.lens().sum())
+    def kv_read_bytes_per_layer(self, window: int = 0) -> int:
+        """Algorithmic KV bytes one decode step reads per layer: 2 H_kv D s sum_b L_b, with
+        L_b capped at the window for sliding-window attention (window > 0)."""
+        lens = self.lens()
+        if window > 0:
+            lens = lens.clamp(max=window)
+        return 2 * self.H_kv * self.D * self.elem_bytes * int(lens.sum())
 
 
 WORKLOADS = {
