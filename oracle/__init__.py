@@ -70,6 +70,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_rolling_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
         L.oracle_rolling_decode_attn.restype = I
         L.oracle_rolling_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+        L.oracle_append_multi.restype = I
+        L.oracle_append_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
+        L.oracle_decode_multi.restype = I
+        L.oracle_decode_multi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
         L.oracle_set_fault.restype = None
         L.oracle_set_fault.argtypes = [I]
         L.oracle_get_fault.restype = I
@@ -169,6 +173,26 @@ def paged_decode_attn(q, Kp, Vp, table, lens, return_bad: bool = False):
     return (out, bad) if return_bad else out
 
 
+def append_multi(Kc, Vc, k_new, v_new, lens) -> int:
+    """In place: the T_q rows of k_new/v_new [B,H_kv,T_q,D] into slots [lens[b]-T_q, lens[b])."""
+    B, H_kv, T_max, D = Kc.shape
+    T_q = k_new.shape[2]
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return lib().oracle_append_multi(_ptr(Kc), _ptr(Vc), _ptr(k_new), _ptr(v_new), _ptr(lens), B, H_kv,
+                                     T_max, D, T_q, _dtype_code(Kc))
+
+
+def decode_multi(q, Kc, Vc, lens, return_bad: bool = False):
+    """out[B,H_q,T_q,D] (float64): new query i of sequence b sees keys 0 .. lens[b]-T_q+i."""
+    B, H_q, T_q, D = q.shape
+    _, H_kv, T_max, _ = Kc.shape
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros((B, H_q, T_q, D), dtype=np.float64)
+    bad = lib().oracle_decode_multi(_ptr(q), _ptr(Kc), _ptr(Vc), _ptr(lens), B, H_q, H_kv, T_max, D,
+                                    T_q, _dtype_code(q), _ptr(out))
+    return (out, bad) if return_bad else out
+
+
 def window_decode_attn(q, Kc, Vc, lens, W, return_bad: bool = False):
     """Sliding-window decode over a full-history cache [B,H_kv,T_max,D]: positions
     [max(0, L-W), L).  out [B,H_q,D] float64."""
@@ -233,7 +257,8 @@ class planted_fault:
 
     1 = interleaved GQA map (j mod H_kv), 2 = score scale 1/D, 3 = append one slot late,
     4 = the new token left out of the attention, 5 = paged block stored token-major,
-    6 = sliding window one position too wide."""
+    6 = sliding window one position too wide,
+    7 = several-query causal mask aligned to the upper left."""
 
     def __init__(self, which: int):
         self.which = which

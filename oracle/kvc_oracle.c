@@ -342,6 +342,79 @@ int oracle_paged_decode_attn(const void* q, const void* Kp, const void* Vp, cons
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Several new tokens per step (chunked prefill, speculative decoding).  With a cache holding
+ * S keys after appending T new tokens, new query i (absolute position S - T + i) sees keys
+ * 0 .. S - T + i: the causal mask aligned to the lower right of the T x S score matrix
+ * ([W1D4] §3.3, third case; the upper-left alignment is the pitfall the same section names).
+ *   q, out  [B, H_q, T_q, D]      k_new, v_new  [B, H_kv, T_q, D]
+ * lens[b] is the post-append length S; a row is invalid unless T_q <= lens[b] <= T_max.
+ * ------------------------------------------------------------------------------------- */
+
+/* Writes the T_q new rows of every (b, h) into slots [lens[b] - T_q, lens[b]).  Returns the
+ * number of invalid rows (skipped). */
+int oracle_append_multi(void* Kc, void* Vc, const void* k_new, const void* v_new,
+                        const int32_t* lens, int B, int H_kv, int T_max, int D, int T_q, int dtype) {
+    const size_t row = (size_t)D * elem_bytes_of(dtype);
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (T_q < 1 || L < T_q || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h)
+            for (int i = 0; i < T_q; ++i) {
+                size_t dst = (((size_t)b * H_kv + h) * T_max + (size_t)(L - T_q + i)) * row;
+                size_t src = (((size_t)b * H_kv + h) * T_q + i) * row;
+                memcpy((char*)Kc + dst, (const char*)k_new + src, row);
+                memcpy((char*)Vc + dst, (const char*)v_new + src, row);
+            }
+    }
+    return bad;
+}
+
+/* Decode attention of T_q new queries per head over the cache [B, H_kv, T_max, D].
+ * out [B, H_q, T_q, D] double; invalid rows are zero.  Returns the number of invalid rows. */
+int oracle_decode_multi(const void* q, const void* Kc, const void* Vc, const int32_t* lens, int B,
+                        int H_q, int H_kv, int T_max, int D, int T_q, int dtype, double* out) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        if (T_q < 1 || lens[b] < T_q || lens[b] > T_max) ++bad;
+    const int rows = B * H_q * T_q;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) if (g_threads > 1)
+#endif
+    for (int r = 0; r < rows; ++r) {
+        int b = r / (H_q * T_q), j = (r / T_q) % H_q, i = r % T_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (T_q < 1 || L < T_q || L > T_max) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int visible = L - T_q + i + 1; /* keys 0 .. L - T_q + i */
+        if (g_fault == 7) visible = i + 1; /* planted: upper-left aligned causal mask */
+        int h = kv_head_of(j, H_q, H_kv);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)visible * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)visible * D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)visible);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        size_t base = ((size_t)b * H_kv + h) * (size_t)T_max * D;
+        for (size_t e = 0; e < (size_t)visible * D; ++e) {
+            Kd[e] = load_elem(Kc, dtype, base + e);
+            Vd[e] = load_elem(Vc, dtype, base + e);
+        }
+        decode_row_f64(qd, Kd, Vd, visible, D, (size_t)D, o, sc);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(sc);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Sliding window and rolling cache.  With a window of W tokens the query of the newest token
  * (position L-1) attends to the W most recent positions [max(0, L-W), L), and the cache only
  * needs W slots: position p lives in slot p mod W, the oldest entry being overwritten
