@@ -68,7 +68,9 @@ def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what="", tight=True):
     assert mx <= 2e-2 and rel <= 1e-2, f"{what}: max abs {mx:.3e} rel {rel:.3e}"
     if not tight:
         return mx, rel
-    tight = np.abs(ref) * 2.0 ** -8 + 1e-6
+    # one bf16 ulp of the exact value: |ref| = m 2^e with m in [0.5, 1) has ulp 2^(e - 8)
+    _, e = np.frexp(np.abs(ref))
+    tight = np.ldexp(1.0, e - 8) + 1e-6
     bad = np.argwhere(err > tight)
     assert bad.size == 0, f"{what}: {len(bad)} outputs beyond one bf16 ulp, first {bad[:3].tolist()}"
     return mx, rel
