@@ -152,6 +152,23 @@ int kvc_set_launch_overlap(kvc_t h, int on);
 int kvc_get_launch_overlap(kvc_t h);
 
 /* ---------------------------------------------------------------------------------------
+ * Several new tokens per step (chunked prefill, speculative decoding).  After T_q new tokens
+ * are appended to a sequence of S = lens[b] positions, new query i sits at position S - T_q + i
+ * and attends to positions 0 .. S - T_q + i: the causal mask aligned to the lower right of the
+ * T_q x S score matrix ("第 1 周 · Day 4" §3.3, third case).  Layouts:
+ *   q, out        [B, H_q, T_q, D]   (per head, the T_q new tokens in order)
+ *   k_new, v_new  [B, H_kv, T_q, D]  written to slots [S - T_q, S)
+ * lens[b] < T_q or > T_max is invalid (KVC_DEV_BAD_LENS, zero output rows).  Supported when T_q
+ * is a power of two with (H_q / H_kv) * T_q <= 32, on contiguous handles, math paths 0, 1, 3;
+ * else KVC_EUNSUPPORTED.  T_q = 1 is kvc_append / kvc_decode_attn / kvc_decode_step. */
+int kvc_append_multi(kvc_t h, int layer, const void* k_new, const void* v_new, const int32_t* lens,
+                     int T_q, void* stream);
+int kvc_decode_attn_multi(kvc_t h, int layer, const void* q, void* out, const int32_t* lens, int T_q,
+                          void* stream);
+int kvc_decode_step_multi(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                          void* out, const int32_t* lens, int T_q, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Rolling cache for sliding-window attention.  With a window of W tokens the newest query
  * attends to the W most recent positions, and the cache needs only W slots: position p lives
  * in slot p mod W, overwriting position p - W ("第 1 周 · Day 4" §2.7 and §1.6, the rolling

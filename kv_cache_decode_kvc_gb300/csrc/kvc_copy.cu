@@ -11,30 +11,35 @@
 
 namespace kvc {
 
-// One warp per (b, h) row pair; 16-byte vectors.
+// One warp per (b, h): the T_in new rows (T_in = T_q new tokens, source [B, H_kv, T_q, D])
+// go to slots [L - T_q, L) (a rolling cache: T_q = 1, slot (L - 1) mod T_max); 16-byte vectors.
 __global__ void append_kernel(const CopyParams p) {
     const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= p.B * p.H_kv) return;
     const int b = gw / p.H_kv, h = gw - b * p.H_kv;
     const int L = p.lens[b];
-    if (L < 1 || (!p.rolling && L > p.T_max)) {
+    const int T_q = p.T_in;
+    if (L < T_q || L < 1 || (!p.rolling && L > p.T_max)) {
         if (h == 0 && lane == 0) atomicOr(p.err, DEV_BAD_LENS);
         return;
     }
-    // slot L - 1, or (L - 1) mod T_max in a rolling cache
-    const int slot = p.rolling ? (L - 1) % p.T_max : L - 1;
-    const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b, h,
-                                   slot, p.err);
-    if (drow < 0) return;
-    const size_t dst = (size_t)drow * p.row_bytes;
-    const size_t src = (size_t)gw * p.row_bytes;
     const int nvec = p.row_bytes >> 4;
-    for (int v = lane; v < nvec; v += 32) {
-        const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + src) + v);
-        const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + src) + v);
-        reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + dst)[v] = kx;
-        reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + dst)[v] = vx;
+    for (int i = 0; i < T_q; ++i) {
+        // position L - T_q + i; a rolling cache stores it at slot position mod T_max
+        const int pos = L - T_q + i;
+        const int slot = p.rolling ? pos % p.T_max : pos;
+        const int64_t drow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, p.H_kv, p.T_max, b,
+                                       h, slot, p.err);
+        if (drow < 0) continue;
+        const size_t dst = (size_t)drow * p.row_bytes;
+        const size_t src = ((size_t)gw * T_q + i) * p.row_bytes;
+        for (int v = lane; v < nvec; v += 32) {
+            const uint4 kx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.K) + src) + v);
+            const uint4 vx = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(p.V) + src) + v);
+            reinterpret_cast<uint4*>(static_cast<char*>(p.Kc) + dst)[v] = kx;
+            reinterpret_cast<uint4*>(static_cast<char*>(p.Vc) + dst)[v] = vx;
+        }
     }
 }
 

@@ -188,11 +188,18 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
     unsigned char* vs = ks + C::TILE_BYTES;
     unsigned char* qs = vs + C::TILE_BYTES;
     const bool with_q = c.first();
-    // tile row of the stream's new token in the fused step (-1: not in this tile)
-    int ns = -1;
+    // tile rows [ns, ne) hold the step's new tokens (k_new rows from i0) in the fused step
+    int ns = -1, ne = -1, i0 = 0;
     if (p.k_new != nullptr) {
-        const int slot = new_row_slot(p, c.it.b, c.it.L);
-        if (slot >= c.t && slot < c.t + n) ns = slot - c.t;
+        if (p.rolling) {
+            const int slot = new_row_slot(p, c.it.b, c.it.L);
+            if (slot >= c.t && slot < c.t + n) { ns = slot - c.t; ne = ns + 1; }
+        } else if (c.t + n > c.it.L - p.T_q) {  // the stream's last T_q rows
+            const int first = c.it.L - p.T_q;
+            ns = first > c.t ? first - c.t : 0;
+            ne = n;
+            i0 = c.t + ns - first;
+        }
     }
     uint32_t bytes = (uint32_t)(2 * n * C::ROWB);
     if (with_q) bytes += C::G * C::ROWB;
@@ -224,13 +231,14 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const TileCurs
     if (ns < 0) {
         copy_rows(0, n);
     } else {
-        // the new row comes straight from k_new / v_new, the rest from the cache
+        // the new rows come straight from k_new / v_new [B, H_kv, T_q, D], the rest from the cache
         copy_rows(0, ns);
-        bulk_g2s(ks + ns * C::ROWB, static_cast<const char*>(p.k_new) + unit * C::ROWB, C::ROWB,
+        const size_t src = (unit * p.T_q + i0) * C::ROWB;
+        bulk_g2s(ks + ns * C::ROWB, static_cast<const char*>(p.k_new) + src, (ne - ns) * C::ROWB,
                  &full_bar[stage], pol);
-        bulk_g2s(vs + ns * C::ROWB, static_cast<const char*>(p.v_new) + unit * C::ROWB, C::ROWB,
+        bulk_g2s(vs + ns * C::ROWB, static_cast<const char*>(p.v_new) + src, (ne - ns) * C::ROWB,
                  &full_bar[stage], pol);
-        copy_rows(ns + 1, n);
+        copy_rows(ne, n);
     }
     if (with_q)
         bulk_g2s(qs, static_cast<const char*>(p.q) + unit * C::G * C::ROWB, C::G * C::ROWB,
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
             int64_t x = 0;
             if (b < B) {
                 const int L = p.lens[b];
-                x = eff_len(L, p.T_max, p.rolling);
+                x = eff_len(L, p.T_max, p.rolling, p.T_q);
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -573,13 +581,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 #pragma unroll
                 for (int j = 0; j < TPI * HS; ++j) acc[j] = acc2[j].x + acc2[j].y;
                 float s2[R];
+                // query row c = sl * HS + hh of the group is new token c mod T_q (T_q a power of
+                // two), which sees tile rows up to lim + (c mod T_q)
+                const int lim = cur.it.L - p.T_q - cur.t, tq1 = p.T_q - 1;
                 if constexpr (LPT == 1) {
                     const bool v0 = base < n;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) s2[r] = v0 ? acc[r] : -INFINITY;
+                    for (int r = 0; r < R; ++r)
+                        s2[r] = (v0 && base <= lim + ((sl * HS + r) & tq1)) ? acc[r] : -INFINITY;
                 } else {
                     reduce_scatter<LPT, LPT>(acc, lig);
-                    s2[0] = (base + lig / HS) < n ? acc[0] : -INFINITY;
+                    const int tok = base + lig / HS;
+                    s2[0] = (tok < n && tok <= lim + ((sl * HS + lig % HS) & tq1)) ? acc[0] : -INFINITY;
                 }
                 // online softmax with a lazily raised reference max
                 bool need = false;
@@ -644,14 +657,23 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
                 }
             }
             // fused append: warp 0 stores the new token's rows (now in the tile) into the cache
-            const int nslot = (fused && warp == 0) ? new_row_slot(p, cur.it.b, cur.it.L) : -1;
-            const int64_t arow = (nslot >= cur.t && nslot < cur.t + n)
-                                     ? cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max,
-                                                 cur.it.b, cur.it.h, nslot, p.err)
-                                     : -1;
-            if (arow >= 0) {
+            // the tile rows [ns, ne) that hold the step's new tokens (now in shared memory)
+            int ns = -1, ne = -1;
+            if (fused && warp == 0) {
+                if (p.rolling) {
+                    const int slot = new_row_slot(p, cur.it.b, cur.it.L);
+                    if (slot >= cur.t && slot < cur.t + n) { ns = slot - cur.t; ne = ns + 1; }
+                } else if (cur.t + n > cur.it.L - p.T_q) {
+                    const int first = cur.it.L - p.T_q;
+                    ns = first > cur.t ? first - cur.t : 0;
+                    ne = n;
+                }
+            }
+            for (int tr = ns; tr >= 0 && tr < ne; ++tr) {
+                const int64_t arow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max,
+                                               cur.it.b, cur.it.h, cur.t + tr, p.err);
+                if (arow < 0) continue;
                 const size_t dst = (size_t)arow * C::ROWB;
-                const int tr = nslot - cur.t;  // the new row's place in the tile
                 const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(Ks) + tr * C::ROWB;
                 const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(Vs) + tr * C::ROWB;
                 unsigned char* kd = static_cast<unsigned char*>(const_cast<void*>(p.K)) + dst;
@@ -791,14 +813,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     int64_t before = 0, all = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
         const int L = p.lens[i];
-        const int64_t v = eff_len(L, p.T_max, p.rolling);
+        const int64_t v = eff_len(L, p.T_max, p.rolling, p.T_q);
         all += v;
         if (i < b) before += v;
     }
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[0]), (unsigned long long)before);
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[1]), (unsigned long long)all);
     __syncthreads();
-    const int Lb = eff_len(p.lens[b], p.T_max, p.rolling);
+    const int Lb = eff_len(p.lens[b], p.T_max, p.rolling, p.T_q);
     if (Lb == 0) return;
     const int64_t W = (int64_t)p.H_kv * sh_sum[1];
     const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);

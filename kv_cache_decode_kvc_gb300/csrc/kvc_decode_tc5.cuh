@@ -258,10 +258,11 @@ __device__ __forceinline__ bool softmax_group_any(bool pred) {
 template <bool ROLL>
 struct NewRow {
     int b = -1, slot = 0;
+    // does tile [t, t + n) hold a new row (one of the last T_q rows, or the rolling slot)?
     __device__ __forceinline__ bool in_tile(const DecodeParams& p, int sb, int L, int t, int n) {
         if constexpr (!ROLL) {
-            (void)p; (void)sb;
-            return t + n == L;
+            (void)sb;
+            return t + n > L - p.T_q;
         } else {
             if (sb != b) {
                 b = sb;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             int64_t x = 0;
             if (b < B) {
                 const int L = p.lens[b];
-                if (L >= 1 && (ROLL || L <= p.T_max)) x = ROLL && L > p.T_max ? p.T_max : L;
+                x = eff_len(L, p.T_max, ROLL ? 1 : 0, p.T_q);
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -554,24 +555,31 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             SegIter it;
             it.init(prefix, B, H_kv, r0, r1);
             while (it.valid) {
-                int64_t arow = -1;
+                // the new rows inside this segment: slots [r0, r1), k_new rows from i0
+                int r0 = 0, r1 = 0, i0 = 0;
                 if constexpr (ROLL) {
                     const int slot = (__ldg(p.lens + it.b) - 1) % p.T_max;
-                    if (it.t0 <= slot && slot < it.t1) arow = ((int64_t)it.b * H_kv + it.h) * p.T_max + slot;
-                } else if (it.t1 == it.L) {
+                    if (it.t0 <= slot && slot < it.t1) { r0 = slot; r1 = slot + 1; }
+                } else {
+                    const int first = it.L - p.T_q;  // the step's first new position
+                    r0 = first > it.t0 ? first : it.t0;
+                    r1 = it.t1;
+                    i0 = r0 - first;
+                }
+                const size_t unit = (size_t)it.b * H_kv + it.h;
+                for (int r = r0; r < r1; ++r) {
+                    int64_t arow;
                     if constexpr (PAGED)
                         arow = cache_row(p.table, p.bs, p.max_blocks, p.num_blocks, H_kv, p.T_max, it.b,
-                                         it.h, it.L - 1, p.err);
+                                         it.h, r, p.err);
                     else
-                        arow = ((int64_t)it.b * H_kv + it.h) * p.T_max + (it.L - 1);
-                }
-                if (arow >= 0) {
-                    const size_t unit = (size_t)it.b * H_kv + it.h;
-                    const size_t dst = (size_t)arow * C::ROWB;
-                    const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + unit * C::ROWB);
-                    const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + unit * C::ROWB);
-                    uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + dst);
-                    uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.V)) + dst);
+                        arow = ((int64_t)it.b * H_kv + it.h) * p.T_max + r;
+                    if (arow < 0) continue;
+                    const size_t src = (unit * p.T_q + (size_t)(i0 + r - r0)) * C::ROWB;
+                    const uint4* ksrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.k_new) + src);
+                    const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.v_new) + src);
+                    uint4* kd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.K)) + (size_t)arow * C::ROWB);
+                    uint4* vd = reinterpret_cast<uint4*>(static_cast<char*>(const_cast<void*>(p.V)) + (size_t)arow * C::ROWB);
                     for (int v = lane; v < C::ROWB / 16; v += 32) {
                         kd[v] = __ldg(ksrc + v);
                         vd[v] = __ldg(vsrc + v);
@@ -643,11 +651,23 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[k & 1]);
             const bool valid = row < n;
+            // query row h is new token h mod T_q (T_q a power of two), which sees positions up
+            // to L - T_q + (h mod T_q): this row is visible to new token i iff i >= dmask
+            const int dmask = row - (cur.it.L - p.T_q - cur.t);
             bool need = false;
+            if (dmask <= 0) {  // visible to every query row (always with one new token)
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                x[h] = valid ? x[h] * qscale : -INFINITY;
-                need |= x[h] > m[h] + TAU;
+                for (int h = 0; h < G; ++h) {
+                    x[h] = valid ? x[h] * qscale : -INFINITY;
+                    need |= x[h] > m[h] + TAU;
+                }
+            } else {
+                const int tq1 = p.T_q - 1;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    x[h] = (valid && (h & tq1) >= dmask) ? x[h] * qscale : -INFINITY;
+                    need |= x[h] > m[h] + TAU;
+                }
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) alpha[h] = 1.f;

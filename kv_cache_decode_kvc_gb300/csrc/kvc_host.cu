@@ -113,47 +113,55 @@ int kvc_math_path(const kvc_cache* h) {
 int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cudaStream_t s) {
     int smem = 0;
     int e;
+    const int Gq = h->G * p.T_q;  // query rows per KV head: G heads x T_q new tokens
     const int path = kvc_math_path(h);
     if (path == 3) {
         const CUtensorMap* maps = &h->tmaps[4 * (size_t)layer];
-        e = h->paged     ? kvc::launch_decode_tc5p_d128(h->G, p, maps, s, &smem)
-            : h->rolling ? kvc::launch_decode_tc5r_d128(h->G, p, maps, s, &smem)
-                         : kvc::launch_decode_tc5_d128(h->G, p, maps, s, &smem);
+        e = h->paged     ? kvc::launch_decode_tc5p_d128(Gq, p, maps, s, &smem)
+            : h->rolling ? kvc::launch_decode_tc5r_d128(Gq, p, maps, s, &smem)
+                         : kvc::launch_decode_tc5_d128(Gq, p, maps, s, &smem);
     } else if (path == 2) {
         const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
         const CUtensorMap& tv = h->tmaps[4 * (size_t)layer + 1];
         switch (h->D) {
-            case 64: e = kvc::launch_decode_tc_d64(h->G, p, tk, tv, s, &smem); break;
-            case 128: e = kvc::launch_decode_tc_d128(h->G, p, tk, tv, s, &smem); break;
-            case 256: e = kvc::launch_decode_tc_d256(h->G, p, tk, tv, s, &smem); break;
+            case 64: e = kvc::launch_decode_tc_d64(Gq, p, tk, tv, s, &smem); break;
+            case 128: e = kvc::launch_decode_tc_d128(Gq, p, tk, tv, s, &smem); break;
+            case 256: e = kvc::launch_decode_tc_d256(Gq, p, tk, tv, s, &smem); break;
             default: return KVC_EUNSUPPORTED;
         }
     } else if (h->dtype == KVC_BF16) {
         switch (h->D) {
-            case 64: e = kvc::launch_decode_bf16_d64(h->G, p, s, &smem); break;
-            case 128: e = kvc::launch_decode_bf16_d128(h->G, p, s, &smem); break;
-            case 256: e = kvc::launch_decode_bf16_d256(h->G, p, s, &smem); break;
+            case 64: e = kvc::launch_decode_bf16_d64(Gq, p, s, &smem); break;
+            case 128: e = kvc::launch_decode_bf16_d128(Gq, p, s, &smem); break;
+            case 256: e = kvc::launch_decode_bf16_d256(Gq, p, s, &smem); break;
             default: return KVC_EUNSUPPORTED;
         }
     } else {
         switch (h->D) {
-            case 4: e = kvc::launch_decode_f32_d4(h->G, p, s, &smem); break;
-            case 64: e = kvc::launch_decode_f32_d64(h->G, p, s, &smem); break;
-            case 128: e = kvc::launch_decode_f32_d128(h->G, p, s, &smem); break;
-            case 256: e = kvc::launch_decode_f32_d256(h->G, p, s, &smem); break;
+            case 4: e = kvc::launch_decode_f32_d4(Gq, p, s, &smem); break;
+            case 64: e = kvc::launch_decode_f32_d64(Gq, p, s, &smem); break;
+            case 128: e = kvc::launch_decode_f32_d128(Gq, p, s, &smem); break;
+            case 256: e = kvc::launch_decode_f32_d256(Gq, p, s, &smem); break;
             default: return KVC_EUNSUPPORTED;
         }
     }
     if (e != 0) return KVC_ECUDA;
     if (p.combine_mode == 1) {
-        if (kvc::launch_combine(h->dtype, h->D, h->G, p, s) != 0) return KVC_ECUDA;
+        if (kvc::launch_combine(h->dtype, h->D, Gq, p, s) != 0) return KVC_ECUDA;
     }
     return KVC_OK;
 }
 
 int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new, void* out,
-                const int32_t* table, const int32_t* lens, void* stream) {
+                const int32_t* table, const int32_t* lens, void* stream, int T_q = 1) {
     if (!h || !q || !out || !lens) return KVC_EINVAL;
+    if (T_q < 1) return KVC_EINVAL;
+    if (T_q > 1) {
+        // several new tokens: the group's G * T_q query rows must be a supported row count, on a
+        // plain contiguous cache, with a kernel that masks per query row
+        if ((T_q & (T_q - 1)) != 0 || h->G * T_q > 32) return KVC_EUNSUPPORTED;
+        if (h->paged || h->rolling || kvc_math_path(h) == 2) return KVC_EUNSUPPORTED;
+    }
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVC_EINVAL;
     if (h->paged != (table != nullptr)) return KVC_EINVAL;  // paged calls on paged handles only
@@ -180,13 +188,14 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.num_blocks = h->num_blocks;
     p.box_rows = h->paged ? (h->bs < kvc::TC_FULL_ROWS ? h->bs : kvc::TC_FULL_ROWS) : 0;
     p.rolling = h->rolling ? 1 : 0;
+    p.T_q = T_q;
     const int U = h->B * h->H_kv;
     int mode = h->combine_mode;
     if (mode < 0) {
         // Merge cost of the last-arriving CTA grows with the segments per stream times the
         // group's outputs; when streams are few and long, hand the merge to a wide kernel.
         const long long nseg = (p.P + U - 1) / U + 1;
-        mode = (nseg * h->G * h->D * 4 > 65536) ? 1 : 0;
+        mode = (nseg * h->G * T_q * h->D * 4 > 65536) ? 1 : 0;
     }
     p.combine_mode = mode;
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
@@ -314,7 +323,9 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
 
     const size_t U = (size_t)B * H_kv;
     const size_t slots = (size_t)h->max_ctas + U;
-    const size_t ws_bytes = slots * G * (size_t)D * 4 + slots * G * 2 * 4 + U * 4 + 256;
+    // partial states for up to 32 query rows per KV head (G heads x T_q new tokens)
+    const size_t GW = G > 32 ? (size_t)G : 32;
+    const size_t ws_bytes = slots * GW * (size_t)D * 4 + slots * GW * 2 * 4 + U * 4 + 256;
     size_t free_b = 0, total_b = 0;
     if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) { delete h; return KVC_ECUDA; }
     if (total + ws_bytes > free_b) { delete h; return KVC_ENOMEM; }
@@ -328,8 +339,8 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
         return KVC_ENOMEM;
     }
     h->part_o = reinterpret_cast<float*>(ws);
-    h->part_ml = h->part_o + slots * G * D;
-    h->counters = reinterpret_cast<int*>(h->part_ml + slots * G * 2);
+    h->part_ml = h->part_o + slots * GW * D;
+    h->counters = reinterpret_cast<int*>(h->part_ml + slots * GW * 2);
     h->err = reinterpret_cast<uint32_t*>(h->counters + U);
     if (cudaMemset(h->slab, 0, total) != cudaSuccess || cudaMemset(ws, 0, ws_bytes) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -526,6 +537,36 @@ int kvc_decode_step(kvc_t h, int layer, const void* q, const void* k_new, const 
                     void* out, const int32_t* lens, void* stream) {
     if (!k_new || !v_new) return KVC_EINVAL;
     return attn_common(h, layer, q, k_new, v_new, out, nullptr, lens, stream);
+}
+
+int kvc_append_multi(kvc_t h, int layer, const void* k_new, const void* v_new, const int32_t* lens,
+                     int T_q, void* stream) {
+    if (!h || !k_new || !v_new || !lens || T_q < 1) return KVC_EINVAL;
+    if (layer < 0 || layer >= h->layers || h->paged) return KVC_EINVAL;
+    if (T_q > 1 && h->rolling) return KVC_EUNSUPPORTED;
+    if (T_q > h->T_max) return KVC_ERANGE;
+    kvc::CopyParams p{};
+    p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;
+    p.Vc = h->slab + (size_t)(2 * layer + 1) * h->layer_bytes;
+    p.K = k_new;
+    p.V = v_new;
+    p.lens = lens;
+    p.err = h->err;
+    p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = T_q;
+    p.row_bytes = h->D * h->es;
+    p.rolling = h->rolling ? 1 : 0;
+    return kvc::launch_append(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
+}
+
+int kvc_decode_attn_multi(kvc_t h, int layer, const void* q, void* out, const int32_t* lens, int T_q,
+                          void* stream) {
+    return attn_common(h, layer, q, nullptr, nullptr, out, nullptr, lens, stream, T_q);
+}
+
+int kvc_decode_step_multi(kvc_t h, int layer, const void* q, const void* k_new, const void* v_new,
+                          void* out, const int32_t* lens, int T_q, void* stream) {
+    if (!k_new || !v_new) return KVC_EINVAL;
+    return attn_common(h, layer, q, k_new, v_new, out, nullptr, lens, stream, T_q);
 }
 
 int kvc_paged_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in,

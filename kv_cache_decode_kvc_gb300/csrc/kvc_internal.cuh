@@ -90,6 +90,8 @@ struct DecodeParams {
     int num_blocks;       // K / V are pools [num_blocks, H_kv, bs, D]; T_max = max_blocks * bs
     int box_rows;         // tcgen05 path: rows per tensor-copy box of a paged tile (min(bs, 128))
     int rolling;          // 1: rolling cache, T_max = window slots, position p in slot p mod T_max
+    int T_q;              // new tokens per sequence (>= 1); the group's G query rows are
+                          // [head][token], token i seeing positions up to lens[b] - T_q + i
 };
 
 struct CopyParams {
@@ -144,10 +146,11 @@ int launch_prefill(const CopyParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ device primitives
 #ifdef __CUDACC__
-// Attended length of a sequence with post-append length L: 0 if invalid (L < 1, or L > T_max
-// for a cache that does not roll), min(L, T_max) for a rolling cache, else L.
-__host__ __device__ __forceinline__ int eff_len(int L, int T_max, int rolling) {
-    if (L < 1 || (!rolling && L > T_max)) return 0;
+// Attended length of a sequence with post-append length L: 0 if invalid (L < T_q, i.e. fewer
+// positions than the step's new tokens, or L > T_max for a cache that does not roll),
+// min(L, T_max) for a rolling cache, else L.
+__host__ __device__ __forceinline__ int eff_len(int L, int T_max, int rolling, int T_q = 1) {
+    if (L < (T_q > 1 ? T_q : 1) || (!rolling && L > T_max)) return 0;
     return rolling && L > T_max ? T_max : L;
 }
 

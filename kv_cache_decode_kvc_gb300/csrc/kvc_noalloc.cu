@@ -106,6 +106,7 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     p.P = sms;
     p.min_tokens = 256;
     p.bs = 1;
+    p.T_q = 1;
     const long long nseg = ((long long)sms + (long long)U - 1) / (long long)U + 1;
     p.combine_mode = (nseg * G * D * 4 > 65536) ? 1 : 0;
     p.qscale = (float)(1.4426950408889634 / sqrt((double)D));

@@ -69,6 +69,9 @@ def load() -> ctypes.CDLL:
         "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
         "kvc_create_paged": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I, I, I]),
         "kvc_create_rolling": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
+        "kvc_append_multi": (I, [P, I, P, P, P, I, P]),
+        "kvc_decode_attn_multi": (I, [P, I, P, P, P, I, P]),
+        "kvc_decode_step_multi": (I, [P, I, P, P, P, P, P, I, P]),
         "kvc_get_window": (I, [P]),
         "kvc_paged_prefill_write": (I, [P, I, P, P, I, P, P, P]),
         "kvc_paged_append": (I, [P, I, P, P, P, P, P]),
@@ -143,6 +146,21 @@ def kvc_decode_attn(h, layer, q, out, lens, stream=None) -> None:
 def kvc_decode_step(h, layer, q, k_new, v_new, out, lens, stream=None) -> None:
     _check(load().kvc_decode_step(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                   _ptr(lens), _stream(stream)), "kvc_decode_step")
+
+
+def kvc_append_multi(h, layer, k_new, v_new, lens, T_q, stream=None) -> None:
+    _check(load().kvc_append_multi(h, layer, _ptr(k_new), _ptr(v_new), _ptr(lens), T_q, _stream(stream)),
+           "kvc_append_multi")
+
+
+def kvc_decode_attn_multi(h, layer, q, out, lens, T_q, stream=None) -> None:
+    _check(load().kvc_decode_attn_multi(h, layer, _ptr(q), _ptr(out), _ptr(lens), T_q, _stream(stream)),
+           "kvc_decode_attn_multi")
+
+
+def kvc_decode_step_multi(h, layer, q, k_new, v_new, out, lens, T_q, stream=None) -> None:
+    _check(load().kvc_decode_step_multi(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                        _ptr(lens), T_q, _stream(stream)), "kvc_decode_step_multi")
 
 
 def kvc_create_rolling(layers, B, H_q, H_kv, D, window, dtype) -> int:
@@ -326,6 +344,17 @@ class KVCache:
 
     def math(self) -> int:
         return kvc_get_math(self.h)
+
+    def append_multi(self, layer, k_new, v_new, lens, stream=None):
+        """k_new / v_new [B, H_kv, T_q, D] into slots [lens[b] - T_q, lens[b])."""
+        kvc_append_multi(self.h, layer, k_new, v_new, lens, k_new.shape[2], stream)
+
+    def decode_attn_multi(self, layer, q, out, lens, stream=None):
+        """q, out [B, H_q, T_q, D]; new token i sees positions up to lens[b] - T_q + i."""
+        kvc_decode_attn_multi(self.h, layer, q, out, lens, q.shape[2], stream)
+
+    def decode_step_multi(self, layer, q, k_new, v_new, out, lens, stream=None):
+        kvc_decode_step_multi(self.h, layer, q, k_new, v_new, out, lens, q.shape[2], stream)
 
     def set_launch_overlap(self, on):
         kvc_set_launch_overlap(self.h, on)
