@@ -198,7 +198,7 @@ def run_ours(args, w):
 
     from kv_cache_decode_kvc_gb300 import kvc
     from kv_cache_decode_kvc_gb300.replicas import env_rank, max_over_ranks, replica_seed, whole_job_rate
-    from kv_cache_decode_kvc_gb300.workloads import fill_layer, paged_table, step_inputs
+    from kv_cache_decode_kvc_gb300.workloads import fill_layer, paged_table, step_inputs, step_inputs_multi
 
     rank, local, world = env_rank()
     torch.cuda.set_device(local)
@@ -223,23 +223,30 @@ def run_ours(args, w):
         # sliding-window attention: a rolling cache of `window` slots per sequence
         cache = kvc.RollingKVCache(L, w.B, w.H_q, w.H_kv, w.D, args.window, w.dtype)
     else:
-        cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), w.dtype)
+        # room for the step's new tokens (one, or --tq of them)
+        cache = kvc.KVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max() + args.tq - 1, w.dtype)
     # the launch preceding each decode launch is the previous layer's decode step, which writes
     # neither lens nor this layer's history rows: early history loads are allowed
     cache.set_launch_overlap(0 if args.no_overlap else 1)
     t_fill = time.perf_counter()
     for layer in range(L):
         fill_layer(cache, layer, w, seed=seed, table=table_d)
-    ins = [step_inputs(w, layer, seed=seed) for layer in range(L)]
-    outs = [torch.empty(w.B, w.H_q, w.D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
-    lens_d = w.lens().to(dev)
+    if args.tq > 1:  # several new tokens per sequence and step (speculative decoding)
+        ins = [step_inputs_multi(w, layer, args.tq, seed=seed) for layer in range(L)]
+        outs = [torch.empty(w.B, w.H_q, args.tq, w.D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    else:
+        ins = [step_inputs(w, layer, seed=seed) for layer in range(L)]
+        outs = [torch.empty(w.B, w.H_q, w.D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    lens_d = (w.lens_pre() + args.tq).to(dev)
     torch.cuda.synchronize()
     t_fill = time.perf_counter() - t_fill
     stream = torch.cuda.Stream(device=dev)
     sptr = stream.cuda_stream
 
     def decode(layer, q, kn, vn, out, lens):
-        if table_d is None:
+        if args.tq > 1:
+            kvc.kvc_decode_step_multi(cache.h, layer, q, kn, vn, out, lens, args.tq, sptr)
+        elif table_d is None:
             kvc.kvc_decode_step(cache.h, layer, q, kn, vn, out, lens, sptr)
         else:
             kvc.kvc_paged_decode_step(cache.h, layer, q, kn, vn, out, table_d, lens, sptr)
@@ -297,7 +304,7 @@ def run_ours(args, w):
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
 
-    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window)
+    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window, args.tq)
     gbs = whole_job_rate(world, kv_bytes_step, ms)
     peak, peak_kind = measured_peaks()
 
@@ -317,14 +324,15 @@ def run_ours(args, w):
     per_launch = [a.elapsed_time(b) for a, b in evs]
     launch_ms = statistics.mean(per_launch)
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
-    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window) + 2 * B * Hq * D * s  # q read, out written
-                        + 4 * B * Hkv * D * s + 4 * B)                    # k/v new read + written, lens
+    T_q = args.tq
+    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window, T_q) + 2 * B * Hq * T_q * D * s  # q, out
+                        + 4 * B * Hkv * T_q * D * s + 4 * B)  # k/v new read + written, lens
     if args.paged:  # each block-table entry a sequence uses, read once
         alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
     # average launch duration over the timed region (graph replay, gaps included)
     region_launch_ms = ms_local / launches_per_step
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
-    traffic = None if args.window else traffic_from_profiles(kernel_source_hash(), args.paged)
+    traffic = None if (args.window or args.tq > 1) else traffic_from_profiles(kernel_source_hash(), args.paged)
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
@@ -334,8 +342,8 @@ def run_ours(args, w):
     h_q = [i[0].cpu().pin_memory() for i in ins]
     h_kn = [i[1].cpu().pin_memory() for i in ins]
     h_vn = [i[2].cpu().pin_memory() for i in ins]
-    h_lens = w.lens().pin_memory()
-    h_out = [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    h_lens = lens_d.cpu().pin_memory()
+    h_out = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for o in outs]
     d_q = [torch.empty_like(i[0]) for i in ins]
     d_kn = [torch.empty_like(i[1]) for i in ins]
     d_vn = [torch.empty_like(i[2]) for i in ins]
@@ -390,7 +398,8 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (counter-based generator, bf16)",
             "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else "")
-                                   + (f", rolling cache, window {args.window}" if args.window else ""),
+                                   + (f", rolling cache, window {args.window}" if args.window else "")
+                                   + (f", {args.tq} new tokens per step" if args.tq > 1 else ""),
                        "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
                        "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
                        "kv_bytes_per_step": kv_bytes_step,
@@ -428,6 +437,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128, 256],
                     help="run the workload from a paged cache with this block size (0: contiguous)")
+    ap.add_argument("--tq", type=int, default=1, choices=[1, 2, 4, 8],
+                    help="new tokens per sequence and step (speculative decoding; 1: plain decode)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window attention over a rolling cache of this many slots (0: off)")
     ap.add_argument("--no-overlap", action="store_true",
@@ -441,6 +452,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.paged and args.window:
         ap.error("--paged and --window are separate cache kinds")
+    if args.tq > 1 and (args.paged or args.window):
+        ap.error("--tq runs on the contiguous cache")
     from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
     if args.layers:

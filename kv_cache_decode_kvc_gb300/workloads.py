@@ -48,10 +48,11 @@ class Workload:
     def T_max(self) -> int:
         return int(self.lens().max())
 
-    def kv_read_bytes_per_layer(self, window: int = 0) -> int:
+    def kv_read_bytes_per_layer(self, window: int = 0, new_tokens: int = 1) -> int:
         """Algorithmic KV bytes one decode step reads per layer: 2 H_kv D s sum_b L_b, with
-        L_b capped at the window for sliding-window attention (window > 0)."""
-        lens = self.lens()
+        L_b capped at the window for sliding-window attention (window > 0), and L_b = T_b +
+        new_tokens when a step appends several tokens (the keys are read once for all of them)."""
+        lens = self.lens_pre() + new_tokens
         if window > 0:
             lens = lens.clamp(max=window)
         return 2 * self.H_kv * self.D * self.elem_bytes * int(lens.sum())
@@ -126,4 +127,20 @@ def step_inputs(w: Workload, layer: int, seed: int | None = None, device="cuda")
         for b in idx:
             kn[b] = synth.block(seed, layer, "K", b, b + 1, w.H_kv, T_b, T_b + 1, w.D, w.B, dt, device)[0, :, 0]
             vn[b] = synth.block(seed, layer, "V", b, b + 1, w.H_kv, T_b, T_b + 1, w.D, w.B, dt, device)[0, :, 0]
+    return q, kn, vn
+
+
+def step_inputs_multi(w: Workload, layer: int, T_q: int, seed: int | None = None, device="cuda"):
+    """A step with T_q new tokens per sequence: q [B,H_q,T_q,D] (rows 0..T_q-1 of tensor 'Q'),
+    k_new / v_new [B,H_kv,T_q,D] (the generator's rows T_b .. T_b + T_q - 1 of each stream)."""
+    seed = w.seed if seed is None else seed
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    lp = w.lens_pre()
+    q = synth.block(seed, layer, "Q", 0, w.B, w.H_q, 0, T_q, w.D, w.B, dt, device).contiguous()
+    kn = torch.empty(w.B, w.H_kv, T_q, w.D, dtype=dt, device=device)
+    vn = torch.empty_like(kn)
+    for b in range(w.B):
+        t0 = int(lp[b])
+        kn[b] = synth.block(seed, layer, "K", b, b + 1, w.H_kv, t0, t0 + T_q, w.D, w.B, dt, device)[0]
+        vn[b] = synth.block(seed, layer, "V", b, b + 1, w.H_kv, t0, t0 + T_q, w.D, w.B, dt, device)[0]
     return q, kn, vn
