@@ -74,6 +74,14 @@ def lib() -> ctypes.CDLL:
         L.oracle_append_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
         L.oracle_decode_multi.restype = I
         L.oracle_decode_multi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
+        L.oracle_quantize_rows.restype = None
+        L.oracle_quantize_rows.argtypes = [P, I, I, I, P, P]
+        L.oracle_quant_append.restype = I
+        L.oracle_quant_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+        L.oracle_quant_prefill_write.restype = I
+        L.oracle_quant_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
+        L.oracle_quant_decode_attn.restype = I
+        L.oracle_quant_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
         L.oracle_set_fault.restype = None
         L.oracle_set_fault.argtypes = [I]
         L.oracle_get_fault.restype = I
@@ -173,6 +181,52 @@ def paged_decode_attn(q, Kp, Vp, table, lens, return_bad: bool = False):
     return (out, bad) if return_bad else out
 
 
+def quantize_rows(x):
+    """int8 codes and fp32 scales of the rows of x [..., D] (bf16 bits or float32)."""
+    x = np.ascontiguousarray(x)
+    D = x.shape[-1]
+    n = x.size // D
+    codes = np.zeros(x.shape, np.int8)
+    scales = np.zeros(x.shape[:-1], np.float32)
+    lib().oracle_quantize_rows(_ptr(x), n, D, _dtype_code(x), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+class QuantCache:
+    """One layer of a quantized cache: int8 codes [B,H_kv,T_max,D] and fp32 scales [B,H_kv,T_max]
+    for K and for V."""
+
+    def __init__(self, B, H_kv, T_max, D):
+        self.Kq = np.zeros((B, H_kv, T_max, D), np.int8)
+        self.Vq = np.zeros_like(self.Kq)
+        self.Ks = np.zeros((B, H_kv, T_max), np.float32)
+        self.Vs = np.zeros_like(self.Ks)
+
+    def _args(self):
+        return _ptr(self.Kq), _ptr(self.Ks), _ptr(self.Vq), _ptr(self.Vs)
+
+    def append(self, k_new, v_new, lens) -> int:
+        B, H_kv, T_max, D = self.Kq.shape
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        return lib().oracle_quant_append(*self._args(), _ptr(k_new), _ptr(v_new), _ptr(lens), B, H_kv,
+                                         T_max, D, _dtype_code(k_new))
+
+    def prefill_write(self, K, V, lens) -> int:
+        B, H_kv, T_max, D = self.Kq.shape
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        return lib().oracle_quant_prefill_write(*self._args(), _ptr(K), _ptr(V), K.shape[2], _ptr(lens), B,
+                                                H_kv, T_max, D, _dtype_code(K))
+
+    def decode_attn(self, q, lens, return_bad: bool = False):
+        B, H_kv, T_max, D = self.Kq.shape
+        H_q = q.shape[1]
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        out = np.zeros((B, H_q, D), dtype=np.float64)
+        bad = lib().oracle_quant_decode_attn(_ptr(q), *self._args(), _ptr(lens), B, H_q, H_kv, T_max, D,
+                                             _dtype_code(q), _ptr(out))
+        return (out, bad) if return_bad else out
+
+
 def append_multi(Kc, Vc, k_new, v_new, lens) -> int:
     """In place: the T_q rows of k_new/v_new [B,H_kv,T_q,D] into slots [lens[b]-T_q, lens[b])."""
     B, H_kv, T_max, D = Kc.shape
@@ -258,7 +312,8 @@ class planted_fault:
     1 = interleaved GQA map (j mod H_kv), 2 = score scale 1/D, 3 = append one slot late,
     4 = the new token left out of the attention, 5 = paged block stored token-major,
     6 = sliding window one position too wide,
-    7 = several-query causal mask aligned to the upper left."""
+    7 = several-query causal mask aligned to the upper left,
+    8 = quantization scale max/128 instead of max/127."""
 
     def __init__(self, which: int):
         self.which = which

@@ -342,6 +342,135 @@ int oracle_paged_decode_attn(const void* q, const void* Kp, const void* Vp, cons
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Quantized cache.  The pages list int8 / fp8 caches as a way to read fewer bytes, with the
+ * softmax accumulated in higher precision, and name per-token / per-head scales among the
+ * formats ([KVG] "MHA、GQA、MLA 与量化如何改变容量"; [M11] §3.1 and §8; [W1D4] §1.5).  Reading
+ * taken: symmetric int8, one fp32 scale per (sequence, KV head, token) row, no zero point:
+ *   scale = max_d |x_d| / 127           (fp32)
+ *   code_d = round_half_even(x_d / scale), clamped to [-127, 127]   (fp32 division)
+ *   x_d ~ code_d * scale                 (the attention reads these values)
+ * A row of zeros has scale 0 and codes 0.  Layout per layer: codes [B, H_kv, T_max, D] int8,
+ * scales [B, H_kv, T_max] fp32, for K and for V.
+ * ------------------------------------------------------------------------------------- */
+
+static float load_f32(const void* base, int dtype, size_t idx) {
+    if (dtype == OR_F32) return ((const float*)base)[idx];
+    return (float)load_elem(base, dtype, idx); /* bf16 -> float is exact */
+}
+
+static void quant_row(const void* x, int dtype, size_t off, int D, int8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(load_f32(x, dtype, off + d));
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    if (g_fault == 8) s = amax / 128.0f; /* planted: scale off by one level */
+    *scale = s;
+    for (int d = 0; d < D; ++d) {
+        float c = 0.0f;
+        if (s > 0.0f) c = rintf(load_f32(x, dtype, off + d) / s);
+        if (c > 127.0f) c = 127.0f;
+        if (c < -127.0f) c = -127.0f;
+        codes[d] = (int8_t)c;
+    }
+}
+
+/* Quantizes rows of a [n_rows, D] array (dtype) into codes [n_rows, D] and scales [n_rows]. */
+void oracle_quantize_rows(const void* x, int n_rows, int D, int dtype, int8_t* codes, float* scales) {
+    for (int r = 0; r < n_rows; ++r)
+        quant_row(x, dtype, (size_t)r * D, D, codes + (size_t)r * D, scales + r);
+}
+
+/* Appends k_new/v_new [B, H_kv, D] (dtype), quantized, at slot lens[b]-1.  Returns the number of
+ * invalid rows (lens out of [1, T_max]; skipped). */
+int oracle_quant_append(int8_t* Kq, float* Ks, int8_t* Vq, float* Vs, const void* k_new,
+                        const void* v_new, const int32_t* lens, int B, int H_kv, int T_max, int D,
+                        int dtype) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 1 || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            size_t row = ((size_t)b * H_kv + h) * T_max + (size_t)(L - 1);
+            size_t src = ((size_t)b * H_kv + h) * D;
+            quant_row(k_new, dtype, src, D, Kq + row * D, Ks + row);
+            quant_row(v_new, dtype, src, D, Vq + row * D, Vs + row);
+        }
+    }
+    return bad;
+}
+
+/* Writes K/V [B, H_kv, T_in, D] (dtype) rows [0, lens[b]), quantized.  Returns the number of
+ * invalid rows (lens out of [0, min(T_in, T_max)]). */
+int oracle_quant_prefill_write(int8_t* Kq, float* Ks, int8_t* Vq, float* Vs, const void* K,
+                               const void* V, int T_in, const int32_t* lens, int B, int H_kv,
+                               int T_max, int D, int dtype) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 0 || L > T_in || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h)
+            for (int t = 0; t < L; ++t) {
+                size_t row = ((size_t)b * H_kv + h) * T_max + (size_t)t;
+                size_t src = (((size_t)b * H_kv + h) * T_in + t) * D;
+                quant_row(K, dtype, src, D, Kq + row * D, Ks + row);
+                quant_row(V, dtype, src, D, Vq + row * D, Vs + row);
+            }
+    }
+    return bad;
+}
+
+/* Decode attention over a quantized cache: the same arithmetic as oracle_decode_attn on the
+ * values code * scale (formed in double).  out [B, H_q, D] double. */
+int oracle_quant_decode_attn(const void* q, const int8_t* Kq, const float* Ks, const int8_t* Vq,
+                             const float* Vs, const int32_t* lens, int B, int H_q, int H_kv,
+                             int T_max, int D, int dtype, double* out) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        if (lens[b] < 1 || lens[b] > T_max) ++bad;
+    const int rows = B * H_q;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) if (g_threads > 1)
+#endif
+    for (int r = 0; r < rows; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (L < 1 || L > T_max) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)L);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        size_t row0 = ((size_t)b * H_kv + h) * (size_t)T_max;
+        for (int t = 0; t < L; ++t) {
+            double sk = (double)Ks[row0 + t], sv = (double)Vs[row0 + t];
+            for (int d = 0; d < D; ++d) {
+                Kd[(size_t)t * D + d] = (double)Kq[(row0 + t) * D + d] * sk;
+                Vd[(size_t)t * D + d] = (double)Vq[(row0 + t) * D + d] * sv;
+            }
+        }
+        decode_row_f64(qd, Kd, Vd, L, D, (size_t)D, o, sc);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(sc);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Several new tokens per step (chunked prefill, speculative decoding).  With a cache holding
  * S keys after appending T new tokens, new query i (absolute position S - T + i) sees keys
  * 0 .. S - T + i: the causal mask aligned to the lower right of the T x S score matrix
