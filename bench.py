@@ -219,6 +219,9 @@ def run_ours(args, w):
         table, num_blocks, max_blocks = paged_table(w, args.paged, spare=w.B)
         cache = kvc.PagedKVCache(L, num_blocks, args.paged, w.B, max_blocks, w.H_q, w.H_kv, w.D, w.dtype)
         table_d = table.to(dev)
+    elif args.int8:
+        # int8 cache with one fp32 scale per (sequence, head, token) row; q / out / new rows bf16
+        cache = kvc.QuantKVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max())
     elif args.window:
         # sliding-window attention: a rolling cache of `window` slots per sequence
         cache = kvc.RollingKVCache(L, w.B, w.H_q, w.H_kv, w.D, args.window, w.dtype)
@@ -304,7 +307,7 @@ def run_ours(args, w):
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
 
-    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window, args.tq)
+    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window, args.tq, args.int8)
     gbs = whole_job_rate(world, kv_bytes_step, ms)
     peak, peak_kind = measured_peaks()
 
@@ -325,18 +328,19 @@ def run_ours(args, w):
     launch_ms = statistics.mean(per_launch)
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
     T_q = args.tq
-    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window, T_q) + 2 * B * Hq * T_q * D * s  # q, out
-                        + 4 * B * Hkv * T_q * D * s + 4 * B)  # k/v new read + written, lens
+    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window, T_q, args.int8) + 2 * B * Hq * T_q * D * s
+                        + 2 * B * Hkv * T_q * D * s  # k/v new read
+                        + 2 * B * Hkv * T_q * (D + 4 if args.int8 else D * s) + 4 * B)  # written, lens
     if args.paged:  # each block-table entry a sequence uses, read once
         alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
     # average launch duration over the timed region (graph replay, gaps included)
     region_launch_ms = ms_local / launches_per_step
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
-    traffic = None if (args.window or args.tq > 1) else traffic_from_profiles(kernel_source_hash(), args.paged)
+    traffic = None if (args.window or args.tq > 1 or args.int8) else traffic_from_profiles(kernel_source_hash(), args.paged)
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
-                   3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'contiguous'}> (tcgen05)"}[path]
+                   3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'int8' if args.int8 else 'rolling' if args.window else 'contiguous'}> (tcgen05)"}[path]
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
     h_q = [i[0].cpu().pin_memory() for i in ins]
@@ -399,7 +403,8 @@ def run_ours(args, w):
             "data": "synthetic (counter-based generator, bf16)",
             "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else "")
                                    + (f", rolling cache, window {args.window}" if args.window else "")
-                                   + (f", {args.tq} new tokens per step" if args.tq > 1 else ""),
+                                   + (f", {args.tq} new tokens per step" if args.tq > 1 else "")
+                                   + (", int8 cache with per-row fp32 scales" if args.int8 else ""),
                        "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
                        "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
                        "kv_bytes_per_step": kv_bytes_step,
@@ -437,6 +442,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128, 256],
                     help="run the workload from a paged cache with this block size (0: contiguous)")
+    ap.add_argument("--int8", action="store_true",
+                    help="int8 cache with per-row fp32 scales (quantized on write)")
     ap.add_argument("--tq", type=int, default=1, choices=[1, 2, 4, 8],
                     help="new tokens per sequence and step (speculative decoding; 1: plain decode)")
     ap.add_argument("--window", type=int, default=0,
@@ -454,6 +461,8 @@ def main():
         ap.error("--paged and --window are separate cache kinds")
     if args.tq > 1 and (args.paged or args.window):
         ap.error("--tq runs on the contiguous cache")
+    if args.int8 and (args.paged or args.window or args.tq > 1):
+        ap.error("--int8 runs on the contiguous cache with one new token")
     from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
     if args.layers:

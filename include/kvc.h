@@ -152,6 +152,23 @@ int kvc_set_launch_overlap(kvc_t h, int on);
 int kvc_get_launch_overlap(kvc_t h);
 
 /* ---------------------------------------------------------------------------------------
+ * Quantized cache.  The pages list int8 / fp8 caches with per-token or per-head scales as a
+ * way to read fewer bytes, with the softmax accumulated in higher precision ("KV 缓存",
+ * "MHA、GQA、MLA 与量化如何改变容量"; "11.7 KV Cache" §3.1 and §8).  kvc_create_quantized makes a
+ * contiguous handle whose cache is symmetric int8 with one fp32 scale per (sequence, KV head,
+ * token) row, for K and for V:
+ *     scale = max_d |x_d| / 127,   code_d = round-half-even(x_d / scale) in [-127, 127]
+ * (IEEE fp32 division; a zero row has scale 0), and the attention reads code * scale.  q, out,
+ * k_new, v_new and the prefill source stay bf16 (dtype must be KVC_BF16); the ordinary calls
+ * (kvc_prefill_write, kvc_append, kvc_decode_attn, kvc_decode_step) quantize on write.
+ * Per layer: codes [B, H_kv, T_max, D] int8 (kvc_layer_ptrs) and scales [B, H_kv, T_max] fp32
+ * (kvc_layer_scales).  Supported: D = 128, H_q / H_kv <= 8, one new token per step, the
+ * tcgen05 path (math 0 or 3); else KVC_EUNSUPPORTED. */
+int kvc_create_quantized(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max,
+                         int dtype);
+int kvc_layer_scales(kvc_t h, int layer, float** Ks, float** Vs);
+
+/* ---------------------------------------------------------------------------------------
  * Several new tokens per step (chunked prefill, speculative decoding).  After T_q new tokens
  * are appended to a sequence of S = lens[b] positions, new query i sits at position S - T_q + i
  * and attends to positions 0 .. S - T_q + i: the causal mask aligned to the lower right of the

@@ -74,7 +74,50 @@ __global__ void prefill_kernel(const CopyParams p) {
     }
 }
 
+// int8 cache (p.Ksc set; bf16 source rows, D = 128): one warp per (b, h, row) quantizes the
+// source row into codes and a row scale (q8_store_row).  Append: rows [L - T_in, L) from the
+// [B, H_kv, T_in, D] source; prefill: rows [0, L) from [B, H_kv, T_in, D].
+__global__ void quant_write_kernel(const CopyParams p, int prefill) {
+    const size_t gw = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const size_t rows = (size_t)p.B * p.H_kv * p.T_in;
+    if (gw >= rows) return;
+    const size_t bh = gw / p.T_in;
+    const int i = (int)(gw - bh * p.T_in);
+    const int b = (int)(bh / p.H_kv);
+    const int L = p.lens[b];
+    int t;
+    if (prefill) {
+        if (L < 0 || L > p.T_in || L > p.T_max) {
+            if (i == 0 && lane == 0 && bh % p.H_kv == 0) atomicOr(p.err, DEV_BAD_LENS);
+            return;
+        }
+        if (i >= L) return;
+        t = i;
+    } else {
+        if (L < p.T_in || L > p.T_max) {
+            if (i == 0 && lane == 0 && bh % p.H_kv == 0) atomicOr(p.err, DEV_BAD_LENS);
+            return;
+        }
+        t = L - p.T_in + i;
+    }
+    const size_t crow = bh * p.T_max + t;
+    const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(p.K) + gw * 128;
+    const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.V) + gw * 128;
+    q8_store_row(ks, static_cast<int8_t*>(p.Kc) + crow * 128, p.Ksc + crow, lane);
+    q8_store_row(vs, static_cast<int8_t*>(p.Vc) + crow * 128, p.Vsc + crow, lane);
+}
+
+static int launch_quant_write(const CopyParams& p, int prefill, cudaStream_t s) {
+    const size_t warps = (size_t)p.B * p.H_kv * p.T_in;
+    const int threads = 256;
+    const size_t blocks = (warps * 32 + threads - 1) / threads;
+    quant_write_kernel<<<(unsigned)blocks, threads, 0, s>>>(p, prefill);
+    return (int)cudaGetLastError();
+}
+
 int launch_append(const CopyParams& p, cudaStream_t s) {
+    if (p.Ksc != nullptr) return launch_quant_write(p, 0, s);
     const int warps = p.B * p.H_kv;
     const int threads = 256;
     const int blocks = (warps * 32 + threads - 1) / threads;
@@ -83,6 +126,7 @@ int launch_append(const CopyParams& p, cudaStream_t s) {
 }
 
 int launch_prefill(const CopyParams& p, cudaStream_t s) {
+    if (p.Ksc != nullptr) return launch_quant_write(p, 1, s);
     const size_t total = (size_t)p.B * p.H_kv * p.T_in * (p.row_bytes >> 4);
     const int threads = 256;
     size_t blocks = (total + threads - 1) / threads;

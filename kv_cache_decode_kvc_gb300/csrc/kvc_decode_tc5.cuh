@@ -35,6 +35,7 @@ struct Tc5Cfg {
     static constexpr int NW = 4;                        // softmax warps (+ producer + MMA warp)
     static constexpr int NEPI = 2;                      // segment-epilogue warps
     static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
+    static constexpr int NCONV = 4;                     // int8 -> bf16 converter warps (int8 cache)
     static constexpr int TT = 128;                      // tokens per tile = MMA M
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
     static constexpr int HALF_BYTES = TT * 128;         // one column block of a K or V tile
@@ -80,6 +81,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)2u << 61;
     return d;
 }
+// Threads of the kernel instantiation: a quantized cache adds the converter warps.
+template <int G, int MODE>
+__host__ __device__ constexpr int tc5_threads() {
+    return Tc5Cfg<G>::NTHREADS + (MODE == 3 ? Tc5Cfg<G>::NCONV * 32 : 0);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness (0 = K-major,
 // 1 = MN-major), N >> 3, M >> 4.
 __host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -163,7 +170,7 @@ __device__ __forceinline__ int tile_block(const DecodeParams& p, const TileCurso
     return lane < nb ? __ldg(p.table + (size_t)c.it.b * p.max_blocks + c.t / p.bs + lane) : 0;
 }
 // Run by lane 0 of the producer warp (contiguous) or by the whole warp (paged, lane = block).
-template <class C, int TT, bool PAGED>
+template <class C, int TT, int MODE>
 __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const TileCursor<TT>& c,
                                                uint32_t ring, uint64_t* full_bar, int stage,
                                                uint64_t pol, const CUtensorMap* tmK,
@@ -175,12 +182,14 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
     const uint32_t vs = ks + C::TILE_BYTES;
     const uint32_t qs = vs + C::TILE_BYTES;
+    constexpr bool PAGED = MODE == 1, QUANT = MODE == 3;
     constexpr bool paged = PAGED;
     const bool full = n == TT && !paged;
     const int rows = paged ? p.box_rows : (full ? TT : C::BOX_ROWS);
     const int nbox = full ? 1 : (n + rows - 1) / rows;
     const bool with_q = c.first();
-    const uint32_t kv_bytes = (uint32_t)(2 * C::HALVES * nbox * rows * 128);
+    // bf16 tiles: 2 x 128-byte column blocks per row; int8 tiles: one row of D bytes
+    const uint32_t kv_bytes = (uint32_t)(2 * nbox * rows * (QUANT ? C::D : C::HALVES * 128));
     const uint32_t q_bytes = with_q ? (uint32_t)(C::G * C::ROWB) : 0u;
     if (lane == 0) {
         if (part == TILE_Q) {
@@ -210,6 +219,16 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                 tma_load_4d(vs + off, tmV, row >> 3, rows >> 3, &full_bar[stage], pol);
             }
         }
+    } else if (QUANT && part != TILE_Q) {
+        // int8 rows (128 bytes) into the back column block of the tile area, widened in place later
+        const int row0 = (int)(unit * p.T_max + c.t);
+        const CUtensorMap* mk = full ? tmKf : tmK;
+        const CUtensorMap* mv = full ? tmVf : tmV;
+        for (int bx = 0; bx < nbox; ++bx) {
+            const uint32_t off = C::HALF_BYTES + bx * C::BOX_ROWS * C::D;
+            tma_load_2d(ks + off, mk, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+            tma_load_2d(vs + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+        }
     } else if (part != TILE_Q) {
         const int row0 = (int)(unit * p.T_max + c.t);
         const CUtensorMap* mk = full ? tmKf : tmK;
@@ -230,6 +249,27 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
             "r"(smem_addr(&full_bar[stage])), "l"(pol)
             : "memory");
     }
+}
+
+// 16 int8 values -> 16 bf16, exactly, with full-rate integer and bf16x2 operations: for the
+// byte x = l - 128 s (l its low 7 bits, s its sign bit), the bf16 with bits 0x43:l is 128 + l and
+// the one with bits 0x43:(s << 7) is 128 + 128 s; their difference is x, exactly representable.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void widen_i8x16(const uint4& v, uint4& o0, uint4& o1) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t r[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = w[j] & 0x7F7F7F7Fu, hi = w[j] & 0x80808080u;
+        r[2 * j] = bf16x2_sub(__byte_perm(lo, 0x43434343u, 0x4140), __byte_perm(hi, 0x43434343u, 0x4140));
+        r[2 * j + 1] = bf16x2_sub(__byte_perm(lo, 0x43434343u, 0x4342), __byte_perm(hi, 0x43434343u, 0x4342));
+    }
+    o0 = make_uint4(r[0], r[1], r[2], r[3]);
+    o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
 // Named barrier of the four softmax warps with an OR reduction of a predicate.
@@ -275,16 +315,18 @@ struct NewRow {
 
 // MODE: 0 contiguous cache, 1 paged pool (block table), 2 rolling cache (T_max = window slots,
 // position p in slot p mod T_max; lens may exceed T_max and the attention covers
-// min(lens, T_max) slots).  Each mode is its own instantiation.
+// min(lens, T_max) slots), 3 int8 cache with per-row scales (tiles arrive as int8 in the back
+// half of the stage's tile area and are widened in place to bf16 by the converter warps; the
+// row scales multiply the scores and the weights).  Each mode is its own instantiation.
 template <int G, int MODE>
-__global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
+__global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     decode_tc5_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKf,
                       const __grid_constant__ CUtensorMap tmVf) {
     using C = Tc5Cfg<G>;
     using T = __nv_bfloat16;
-    constexpr bool PAGED = MODE == 1, ROLL = MODE == 2;
+    constexpr bool PAGED = MODE == 1, ROLL = MODE == 2, QUANT = MODE == 3;
     constexpr int D = C::D, N = C::N, TT = C::TT, NST = C::NST, KS = D / 16, TS = TT / 16;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -317,6 +359,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
     const size_t row_elems_q = (size_t)H_kv * G * D;
     uint64_t* append_bar = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(mma_issued + 1) + 7) & ~uintptr_t(7));
+    uint64_t* conv_full = append_bar + 1;  // [NST] int8 cache: the stage's tiles are bf16 now
 
     // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
     // CTAs take SMs as ours exit) but waits in griddepcontrol.wait until this grid is complete.
@@ -337,6 +380,8 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
         mbar_init(m_full, C::NW * 32);
         mbar_init(m_empty, C::NEPI * 32);
         mbar_init(append_bar, 1);
+        if constexpr (QUANT)
+            for (int s = 0; s < NST; ++s) mbar_init(&conv_full[s], C::NCONV * 32);
         *abort_flag = 0;
         *last_flag = 0;
         *mma_issued = 0;
@@ -392,7 +437,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
         if (early)
             while (pref.valid && npre < NST && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
                 if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
-                issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
+                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
                                              TILE_KV, ent, lane);
                 if (lane == 0) issued[npre] += 1;
                 pref.advance();
@@ -419,7 +464,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             TileCursor<TT> c0;
             c0.init(prefix, B, H_kv, r0, r1);
             for (int i = 0; i < npre; ++i) {
-                issue_tile_tc5<C, TT, PAGED>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf,
+                issue_tile_tc5<C, TT, MODE>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf,
                                              TILE_Q, ent, lane);
                 c0.advance();
             }
@@ -437,7 +482,7 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 }
                 if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                issue_tile_tc5<C, TT, PAGED>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf,
+                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf,
                                              TILE_ALL, ent, lane);
                 if (lane == 0) issued[s] += 1;
                 pref.advance();
@@ -497,7 +542,8 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             const bool have = cur.valid && alive;
             if (!have) break;
             // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
-            alive = mbar_wait(&full_bar[s], ph, abort_flag, p.err);
+            // int8 cache: wait until the converter warps have widened the stage to bf16
+            alive = mbar_wait(QUANT ? &conv_full[s] : &full_bar[s], ph, abort_flag, p.err);
             if (alive && cur.first()) {
                 // the previous MMA1 read q_sw: let it finish before q is replaced
                 if (k > 0) alive = mbar_wait(&s_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err);
@@ -526,6 +572,65 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             __syncwarp();
             s_prev = s;
             cur.advance();
+            if (++s == NST) { s = 0; ph ^= 1u; }
+        }
+    } else if (QUANT && warp >= 2 + C::NW + C::NEPI) {
+        // ======================================================= int8 -> bf16 converters
+        // Per stage, in tile order: wait for the copies, widen the K and V tiles in place
+        // (int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of
+        // column blocks 0 and 1), publish to the tensor cores, arrive.  Column block 0 is
+        // written first (it does not overlap the int8 rows); after a barrier of the converter
+        // warps, each thread widens whole rows' second halves in place.
+        const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
+        TileCursor<TT> cc;
+        cc.init(prefix, B, H_kv, r0, r1);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        while (cc.valid) {
+            ok = ok && mbar_wait(&full_bar[s], ph, abort_flag, p.err);
+            unsigned char* st = ring + s * C::STAGE_BYTES;
+            // (the barriers run whatever ok is: a thread that gave up must not strand the others)
+            if (ok) {
+                // column block 0: unit = (tensor, row, 16-byte group g of columns 16g .. 16g+15)
+#pragma unroll 4
+                for (int u = ct; u < 2 * TT * 4; u += C::NCONV * 32) {
+                    unsigned char* tb = st + (u >> 9) * C::TILE_BYTES;
+                    const int r = (u >> 2) & (TT - 1), g = u & 3;
+                    const uint4 v = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + r * C::D + g * 16);
+                    uint4 o0, o1;
+                    widen_i8x16(v, o0, o1);
+                    unsigned char* row = tb + r * 128;
+                    *reinterpret_cast<uint4*>(row + (((2 * g) ^ (r & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ (r & 7)) << 4)) = o1;
+                }
+            }
+            named_bar_sync(4, C::NCONV * 32);
+            // column block 1, in place: a thread owns whole rows (it reads a row's last 64 bytes
+            // before writing the row's 128); the read order rotates with the row so that the
+            // threads of a quarter warp hit different banks
+            if (ok) {
+#pragma unroll 2
+                for (int u = ct; u < 2 * TT; u += C::NCONV * 32) {
+                    const int r = u & (TT - 1);
+                    unsigned char* row = st + (u >> 7) * C::TILE_BYTES + C::HALF_BYTES + r * 128;
+                    uint4 v[4];  // v[i] holds column group (i + r) mod 4
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v[i] = *reinterpret_cast<const uint4*>(row + 64 + ((i + r) & 3) * 16);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int g = (i + r) & 3;
+                        uint4 o0, o1;
+                        widen_i8x16(v[i], o0, o1);
+                        *reinterpret_cast<uint4*>(row + (((2 * g) ^ (r & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ (r & 7)) << 4)) = o1;
+                    }
+                }
+            }
+            fence_async_smem();  // generic-proxy writes before the tensor cores read them
+            mbar_arrive(&conv_full[s]);
+            cc.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
     } else if (warp >= 2 + C::NW) {
@@ -567,6 +672,19 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                     i0 = r0 - first;
                 }
                 const size_t unit = (size_t)it.b * H_kv + it.h;
+                if constexpr (QUANT) {
+                    // quantize the new row (one per stream: T_q = 1) into codes + scale
+                    for (int r = r0; r < r1; ++r) {
+                        const size_t crow = unit * p.T_max + r;
+                        q8_store_row(static_cast<const __nv_bfloat16*>(p.k_new) + unit * D,
+                                     static_cast<int8_t*>(const_cast<void*>(p.K)) + crow * D,
+                                     const_cast<float*>(p.Ksc) + crow, lane);
+                        q8_store_row(static_cast<const __nv_bfloat16*>(p.v_new) + unit * D,
+                                     static_cast<int8_t*>(const_cast<void*>(p.V)) + crow * D,
+                                     const_cast<float*>(p.Vsc) + crow, lane);
+                    }
+                    r1 = r0;  // nothing left for the plain copy below
+                }
                 for (int r = r0; r < r1; ++r) {
                     int64_t arow;
                     if constexpr (PAGED)
@@ -626,6 +744,26 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_empty[j & 1]);
         };
+        // int8 cache: the K and V scales of this thread's row of a tile; the new row of a fused
+        // step takes them from k_new / v_new, as its append computes them
+        auto load_scales = [&](const TileCursor<TT>& c, float& a, float& b) {
+            a = 1.f;
+            b = 1.f;
+            if (row < c.n()) {
+                const int t = c.t + row;
+                const size_t unit = (size_t)c.it.b * H_kv + c.it.h;
+                if (fused && t == c.it.L - 1) {
+                    a = q8_row_scale(static_cast<const __nv_bfloat16*>(p.k_new) + unit * D);
+                    b = q8_row_scale(static_cast<const __nv_bfloat16*>(p.v_new) + unit * D);
+                } else {
+                    a = __ldcg(p.Ksc + unit * p.T_max + t);
+                    b = __ldcg(p.Vsc + unit * p.T_max + t);
+                }
+            }
+        };
+        float sk_next = 1.f, sv_next = 1.f;
+        if constexpr (QUANT)
+            if (cur.valid) load_scales(cur, sk_next, sv_next);
         for (int k = 0; cur.valid; ++k) {
             const int n = cur.n();
             const bool first = cur.first(), last = cur.last();
@@ -633,6 +771,14 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
 #pragma unroll
                 for (int h = 0; h < G; ++h) { o[h] = 0.f; m[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f; }
             }
+            // int8 cache: this row's K and V scales, loaded one tile ahead
+            const float sk = sk_next, sv = sv_next;
+            if constexpr (QUANT) {
+                TileCursor<TT> nxt = cur;
+                nxt.advance();
+                if (nxt.valid) load_scales(nxt, sk_next, sv_next);
+            }
+            const float qk = QUANT ? qscale * sk : qscale;
             // ---- scores of tile k
             alive = alive && mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
@@ -658,14 +804,14 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
             if (dmask <= 0) {  // visible to every query row (always with one new token)
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    x[h] = valid ? x[h] * qscale : -INFINITY;
+                    x[h] = valid ? x[h] * qk : -INFINITY;
                     need |= x[h] > m[h] + TAU;
                 }
             } else {
                 const int tq1 = p.T_q - 1;
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    x[h] = (valid && (h & tq1) >= dmask) ? x[h] * qscale : -INFINITY;
+                    x[h] = (valid && (h & tq1) >= dmask) ? x[h] * qk : -INFINITY;
                     need |= x[h] > m[h] + TAU;
                 }
             }
@@ -701,8 +847,10 @@ __global__ void __launch_bounds__(Tc5Cfg<G>::NTHREADS, 1)
                 for (int h = 0; h < G; ++h) {
                     const float pv = (x[h] == -INFINITY) ? 0.f : fast_exp2(x[h] - m[h]);
                     l[h] += pv;
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+                    // int8 cache: the V row scale folds into the weight (MMA2 reads the codes)
+                    const float pw = QUANT ? pv * sv : pv;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pw);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(pw - __bfloat162float(hi));
                     const uint32_t off = (((chunk ^ (h & 7)) << 4) | (e << 1));  // N % 8 == 0
                     *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + off) = hi;
                     *reinterpret_cast<__nv_bfloat16*>(pb + (N + h) * 128 + off) = lo;

@@ -1,7 +1,8 @@
 // kvc_decode_tc5_inst.cu -- instantiates the tcgen05 decode kernel (bf16 cache, D = 128); the
 // query-head group G is dispatched at run time.  Compiled once per cache mode, so no kernel
 // carries another mode's code: KVC_TC5_MODE = 0 contiguous (launch_decode_tc5_d128), 1 paged
-// pool (launch_decode_tc5p_d128), 2 rolling cache (launch_decode_tc5r_d128).
+// pool (launch_decode_tc5p_d128), 2 rolling cache (launch_decode_tc5r_d128), 3 int8 cache
+// (launch_decode_tc5q_d128; group sizes up to 8, the converter warps leave fewer registers).
 #include "kvc_decode_tc5.cuh"
 
 #ifndef KVC_TC5_MODE
@@ -11,6 +12,8 @@
 #define KVC_TC5_LAUNCHER launch_decode_tc5p_d128
 #elif KVC_TC5_MODE == 2
 #define KVC_TC5_LAUNCHER launch_decode_tc5r_d128
+#elif KVC_TC5_MODE == 3
+#define KVC_TC5_LAUNCHER launch_decode_tc5q_d128
 #else
 #define KVC_TC5_LAUNCHER launch_decode_tc5_d128
 #endif
@@ -34,7 +37,7 @@ static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStre
     // until that kernel is complete and its writes are visible
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.P);
-    cfg.blockDim = dim3(C::NTHREADS);
+    cfg.blockDim = dim3(tc5_threads<G, KVC_TC5_MODE>());
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -54,8 +57,10 @@ int KVC_TC5_LAUNCHER(int G, const DecodeParams& p, const CUtensorMap* maps, cuda
         case 2: return launch_tc5_g<2>(p, maps, s, smem_out);
         case 4: return launch_tc5_g<4>(p, maps, s, smem_out);
         case 8: return launch_tc5_g<8>(p, maps, s, smem_out);
+#if KVC_TC5_MODE != 3
         case 16: return launch_tc5_g<16>(p, maps, s, smem_out);
         case 32: return launch_tc5_g<32>(p, maps, s, smem_out);
+#endif
         default: return (int)cudaErrorInvalidValue;
     }
 }

@@ -31,6 +31,9 @@ struct kvc_cache {
                                      // paged: K, V, K, V with min(bs, 128)-row boxes
     bool paged;                      // K / V of a layer are pools [num_blocks, H_kv, bs, D]
     bool rolling;                    // T_max = window slots, position p in slot p mod T_max
+    bool quant;                      // int8 codes + fp32 row scales (q, out, new rows in dtype)
+    float* scales;                   // int8 cache: K / V row scales of layer l at 2l, 2l + 1
+    size_t scale_stride;             // floats between consecutive scale arrays (256-byte aligned)
     int bs, max_blocks, num_blocks;  // paged geometry (T_max = max_blocks * bs)
 };
 
@@ -95,6 +98,20 @@ bool make_paged_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over an int8 cache with D = 128 (rows of 128 bytes): boxes of 128 bytes x box_rows rows,
+// no swizzle (the kernel widens them to bf16 itself).
+bool make_q8_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // a * b with overflow detection (all operands >= 0)
 bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
     if (a != 0 && b > UINT64_MAX / a) return false;
@@ -119,6 +136,7 @@ int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cud
         const CUtensorMap* maps = &h->tmaps[4 * (size_t)layer];
         e = h->paged     ? kvc::launch_decode_tc5p_d128(Gq, p, maps, s, &smem)
             : h->rolling ? kvc::launch_decode_tc5r_d128(Gq, p, maps, s, &smem)
+            : h->quant   ? kvc::launch_decode_tc5q_d128(Gq, p, maps, s, &smem)
                          : kvc::launch_decode_tc5_d128(Gq, p, maps, s, &smem);
     } else if (path == 2) {
         const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
@@ -160,8 +178,9 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
         // several new tokens: the group's G * T_q query rows must be a supported row count, on a
         // plain contiguous cache, with a kernel that masks per query row
         if ((T_q & (T_q - 1)) != 0 || h->G * T_q > 32) return KVC_EUNSUPPORTED;
-        if (h->paged || h->rolling || kvc_math_path(h) == 2) return KVC_EUNSUPPORTED;
+        if (h->paged || h->rolling || h->quant || kvc_math_path(h) == 2) return KVC_EUNSUPPORTED;
     }
+    if (h->quant && kvc_math_path(h) != 3) return KVC_EUNSUPPORTED;  // only tcgen05 reads int8
     if (layer < 0 || layer >= h->layers) return KVC_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr)) return KVC_EINVAL;
     if (h->paged != (table != nullptr)) return KVC_EINVAL;  // paged calls on paged handles only
@@ -189,6 +208,10 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.box_rows = h->paged ? (h->bs < kvc::TC_FULL_ROWS ? h->bs : kvc::TC_FULL_ROWS) : 0;
     p.rolling = h->rolling ? 1 : 0;
     p.T_q = T_q;
+    if (h->quant) {
+        p.Ksc = h->scales + (size_t)(2 * layer) * h->scale_stride;
+        p.Vsc = h->scales + (size_t)(2 * layer + 1) * h->scale_stride;
+    }
     const int U = h->B * h->H_kv;
     int mode = h->combine_mode;
     if (mode < 0) {
@@ -201,6 +224,13 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
     p.overlap = h->overlap;
     return launch_decode(h, layer, p, static_cast<cudaStream_t>(stream));
+}
+
+// int8 cache: the layer's row-scale arrays for the quantizing writes
+void set_quant_scales(const kvc_cache* h, int layer, kvc::CopyParams& p) {
+    if (!h->quant) return;
+    p.Ksc = h->scales + (size_t)(2 * layer) * h->scale_stride;
+    p.Vsc = h->scales + (size_t)(2 * layer + 1) * h->scale_stride;
 }
 
 }  // namespace
@@ -276,7 +306,7 @@ int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, i
 }
 
 static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max,
-                         int dtype, int bs, int max_blocks, int num_blocks) {
+                         int dtype, int bs, int max_blocks, int num_blocks, bool quant = false) {
     const bool paged = bs > 0;
     if (!out) return KVC_EINVAL;
     *out = nullptr;
@@ -294,8 +324,13 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     if (!mul_ok(paged ? (uint64_t)num_blocks : (uint64_t)B, (uint64_t)H_kv, &rows) ||
         !mul_ok(rows, paged ? (uint64_t)bs : (uint64_t)T_max, &rows))
         return KVC_ERANGE;
+    // cache element bytes: the dtype, or 1 for int8 codes (their fp32 row scales follow all codes)
+    const int ces = quant ? 1 : es;
     uint64_t total = 0;
-    if (!mul_ok(rows, 2ull * (uint64_t)layers * (uint64_t)D * (uint64_t)es, &total)) return KVC_ERANGE;
+    if (!mul_ok(rows, 2ull * (uint64_t)layers * (uint64_t)D * (uint64_t)ces, &total)) return KVC_ERANGE;
+    const size_t scale_stride = quant ? (size_t)((rows + 63) / 64 * 64) : 0;  // floats, 256-B aligned
+    const size_t codes_total = (size_t)total;
+    total += 2ull * (uint64_t)layers * scale_stride * 4;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ECUDA;
@@ -315,11 +350,13 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     h->tc_ok = false;
     h->paged = paged;
     h->rolling = false;
+    h->quant = quant;
+    h->scale_stride = scale_stride;
     h->bs = paged ? bs : 1;
     h->max_blocks = paged ? max_blocks : 0;
     h->num_blocks = paged ? num_blocks : 0;
     h->max_ctas = 4 * h->sms;
-    h->layer_bytes = (size_t)rows * D * es;
+    h->layer_bytes = (size_t)rows * D * ces;
 
     const size_t U = (size_t)B * H_kv;
     const size_t slots = (size_t)h->max_ctas + U;
@@ -331,6 +368,7 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     if (total + ws_bytes > free_b) { delete h; return KVC_ENOMEM; }
 
     if (cudaMalloc(&h->slab, total) != cudaSuccess) { cudaGetLastError(); delete h; return KVC_ENOMEM; }
+    h->scales = quant ? reinterpret_cast<float*>(h->slab + codes_total) : nullptr;
     char* ws = nullptr;
     if (cudaMalloc(&ws, ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -353,14 +391,19 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     // a paged pool is copied one block (at most 128 rows) per box
     const int box_small = paged ? (bs < kvc::TC_FULL_ROWS ? bs : kvc::TC_FULL_ROWS) : kvc::TC_BOX_ROWS;
     const int box_full = paged ? box_small : kvc::TC_FULL_ROWS;
-    if (dtype == KVC_BF16 && rows < (1ull << 31) && (!paged || D == 128)) {
+    if (dtype == KVC_BF16 && rows < (1ull << 31) && ((!paged && !quant) || D == 128)) {
         h->tmaps.resize(4 * (size_t)layers);
         bool ok = true;
         for (int l = 0; l < layers && ok; ++l) {
             void* kb = h->slab + (size_t)(2 * l) * h->layer_bytes;
             void* vb = h->slab + (size_t)(2 * l + 1) * h->layer_bytes;
             CUtensorMap* m4 = &h->tmaps[4 * (size_t)l];
-            if (paged)  // the tcgen05 kernel's paged variant (D = 128) reads 4-D boxes
+            if (quant)  // int8 rows of 128 bytes, unswizzled (widened to bf16 in the kernel)
+                ok = make_q8_tensor_map(&m4[0], kb, rows, box_small) &&
+                     make_q8_tensor_map(&m4[1], vb, rows, box_small) &&
+                     make_q8_tensor_map(&m4[2], kb, rows, box_full) &&
+                     make_q8_tensor_map(&m4[3], vb, rows, box_full);
+            else if (paged)  // the tcgen05 kernel's paged variant (D = 128) reads 4-D boxes
                 ok = make_paged_tensor_map(&m4[0], kb, rows, box_small) &&
                      make_paged_tensor_map(&m4[1], vb, rows, box_small) &&
                      make_paged_tensor_map(&m4[2], kb, rows, box_full) &&
@@ -380,6 +423,29 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
 
 int kvc_create(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
     return create_common(out, layers, B, H_q, H_kv, D, T_max, dtype, 0, 0, 0);
+}
+
+int kvc_create_quantized(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max,
+                         int dtype) {
+    if (!out) return KVC_EINVAL;
+    *out = nullptr;
+    // the tcgen05 kernel reads int8 tiles: bf16 queries, D = 128, up to 8 query heads per KV head
+    if (dtype != KVC_BF16 || D != 128 || H_kv < 1 || H_q % H_kv != 0 || H_q / H_kv > 8)
+        return KVC_EUNSUPPORTED;
+    const int rc = create_common(out, layers, B, H_q, H_kv, D, T_max, dtype, 0, 0, 0, true);
+    if (rc == KVC_OK && !(*out)->tc_ok) {  // no tensor maps: nothing can read this cache
+        kvc_destroy(*out);
+        *out = nullptr;
+        return KVC_EUNSUPPORTED;
+    }
+    return rc;
+}
+
+int kvc_layer_scales(kvc_t h, int layer, float** Ks, float** Vs) {
+    if (!h || !h->quant || layer < 0 || layer >= h->layers) return KVC_EINVAL;
+    if (Ks) *Ks = h->scales + (size_t)(2 * layer) * h->scale_stride;
+    if (Vs) *Vs = h->scales + (size_t)(2 * layer + 1) * h->scale_stride;
+    return KVC_OK;
 }
 
 int kvc_create_rolling(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int window,
@@ -419,14 +485,16 @@ int kvc_destroy(kvc_t h) {
 
 uint64_t kvc_bytes(kvc_t h) {
     if (!h) return 0;
-    return 2ull * (uint64_t)h->layers * h->layer_bytes;  // paged: the whole block pool
+    // paged: the whole block pool; int8: codes plus the fp32 row scales
+    return 2ull * (uint64_t)h->layers * (h->layer_bytes + h->scale_stride * 4);
 }
 
 uint64_t kvc_payload_bytes(kvc_t h, const int32_t* lens_host) {
     if (!h || !lens_host) return 0;
     uint64_t sum = 0;
     for (int b = 0; b < h->B; ++b) sum += (uint64_t)(lens_host[b] > 0 ? lens_host[b] : 0);
-    return 2ull * h->layers * h->H_kv * h->D * h->es * sum;
+    const uint64_t row = h->quant ? (uint64_t)h->D + 4 : (uint64_t)h->D * h->es;  // int8: + scale
+    return 2ull * h->layers * h->H_kv * row * sum;
 }
 
 int kvc_layer_ptrs(kvc_t h, int layer, void** K, void** V) {
@@ -465,6 +533,7 @@ int kvc_set_math(kvc_t h, int mode) {
     if (mode >= 2 && !h->tc_ok) return KVC_EUNSUPPORTED;
     if (mode == 3 && h->D != 128) return KVC_EUNSUPPORTED;
     if (mode == 2 && (h->paged || h->rolling)) return KVC_EUNSUPPORTED;  // warp MMA: plain caches only
+    if (h->quant && mode != 0 && mode != 3) return KVC_EUNSUPPORTED;     // int8: tcgen05 only
     h->math = mode;
     return KVC_OK;
 }
@@ -507,6 +576,7 @@ int kvc_prefill_write(kvc_t h, int layer, const void* K, const void* V, int T_in
     p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = T_in;
     p.row_bytes = h->D * h->es;
     p.rolling = h->rolling ? 1 : 0;
+    set_quant_scales(h, layer, p);
     return kvc::launch_prefill(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
 }
 
@@ -525,6 +595,7 @@ int kvc_append(kvc_t h, int layer, const void* k_new, const void* v_new, const i
     p.B = h->B; p.H_kv = h->H_kv; p.T_max = h->T_max; p.T_in = 1;
     p.row_bytes = h->D * h->es;
     p.rolling = h->rolling ? 1 : 0;
+    set_quant_scales(h, layer, p);
     return kvc::launch_append(p, static_cast<cudaStream_t>(stream)) == 0 ? KVC_OK : KVC_ECUDA;
 }
 
@@ -543,7 +614,7 @@ int kvc_append_multi(kvc_t h, int layer, const void* k_new, const void* v_new, c
                      int T_q, void* stream) {
     if (!h || !k_new || !v_new || !lens || T_q < 1) return KVC_EINVAL;
     if (layer < 0 || layer >= h->layers || h->paged) return KVC_EINVAL;
-    if (T_q > 1 && h->rolling) return KVC_EUNSUPPORTED;
+    if (T_q > 1 && (h->rolling || h->quant)) return KVC_EUNSUPPORTED;
     if (T_q > h->T_max) return KVC_ERANGE;
     kvc::CopyParams p{};
     p.Kc = h->slab + (size_t)(2 * layer) * h->layer_bytes;

@@ -92,6 +92,8 @@ struct DecodeParams {
     int rolling;          // 1: rolling cache, T_max = window slots, position p in slot p mod T_max
     int T_q;              // new tokens per sequence (>= 1); the group's G query rows are
                           // [head][token], token i seeing positions up to lens[b] - T_q + i
+    const float* Ksc;     // int8 cache: K / V are codes [B, H_kv, T_max, D] and these the row
+    const float* Vsc;     // scales [B, H_kv, T_max] (value = code * scale); else nullptr
 };
 
 struct CopyParams {
@@ -106,6 +108,8 @@ struct CopyParams {
     const int32_t* table; // paged cache: [B, max_blocks] block table, else nullptr
     int bs, max_blocks, num_blocks;
     int rolling;          // rolling cache: position p in slot p mod T_max (lens may exceed T_max)
+    float* Ksc;           // int8 cache: row scales of K / V; the rows are quantized on write
+    float* Vsc;
 };
 
 // One launcher per (dtype, D) translation unit; G selects the instantiation.  Each returns
@@ -137,6 +141,9 @@ int launch_decode_tc5_d128(int G, const DecodeParams& p, const CUtensorMap* maps
 int launch_decode_tc5p_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                             int* smem_out);
 int launch_decode_tc5r_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                            int* smem_out);
+// ... and for an int8 cache (p.Ksc / p.Vsc set; maps over the int8 rows, no swizzle)
+int launch_decode_tc5q_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                             int* smem_out);
 constexpr int TC_BOX_ROWS = 32;
 constexpr int TC_FULL_ROWS = 128;
@@ -210,6 +217,19 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Non-blocking probe of a phase (for a thread that polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -320,6 +340,42 @@ struct Elem<float> {
         reinterpret_cast<float*>(base)[idx] = x;
     }
 };
+// Symmetric int8 quantization of one bf16 row of D = 128 values, as the cache stores it:
+// scale = max |x| / 127, code = round-half-even(x / scale) clamped to [-127, 127] (IEEE fp32
+// division; a zero row gets scale 0 and codes 0).
+__device__ __forceinline__ float q8_row_scale(const __nv_bfloat16* x) {
+    float amax = 0.f;
+    const uint4* v = reinterpret_cast<const uint4*>(x);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const uint4 w = __ldg(v + i);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+    }
+    return __fdiv_rn(amax, 127.f);
+}
+// Warp-cooperative: lane l quantizes elements 4l .. 4l+3 of the row and stores their codes;
+// lane 0 stores the scale.
+__device__ __forceinline__ void q8_store_row(const __nv_bfloat16* x, int8_t* codes, float* scale,
+                                             int lane) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(x) + lane);
+    const float f[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float s = __fdiv_rn(amax, 127.f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int c = s > 0.f ? __float2int_rn(__fdiv_rn(f[j], s)) : 0;
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        packed |= (uint32_t)(c & 0xFF) << (8 * j);
+    }
+    reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+    if (lane == 0) *scale = s;
+}
+
 #endif  // __CUDACC__
 
 }  // namespace kvc

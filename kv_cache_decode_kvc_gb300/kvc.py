@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
         "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
         "kvc_create_paged": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I, I, I]),
         "kvc_create_rolling": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
+        "kvc_create_quantized": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
+        "kvc_layer_scales": (I, [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "kvc_append_multi": (I, [P, I, P, P, P, I, P]),
         "kvc_decode_attn_multi": (I, [P, I, P, P, P, I, P]),
         "kvc_decode_step_multi": (I, [P, I, P, P, P, P, P, I, P]),
@@ -161,6 +163,19 @@ def kvc_decode_attn_multi(h, layer, q, out, lens, T_q, stream=None) -> None:
 def kvc_decode_step_multi(h, layer, q, k_new, v_new, out, lens, T_q, stream=None) -> None:
     _check(load().kvc_decode_step_multi(h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                         _ptr(lens), T_q, _stream(stream)), "kvc_decode_step_multi")
+
+
+def kvc_create_quantized(layers, B, H_q, H_kv, D, T_max, dtype) -> int:
+    h = ctypes.c_void_p()
+    _check(load().kvc_create_quantized(ctypes.byref(h), layers, B, H_q, H_kv, D, T_max, dtype),
+           "kvc_create_quantized")
+    return h.value
+
+
+def kvc_layer_scales(h, layer):
+    k, v = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(load().kvc_layer_scales(h, layer, ctypes.byref(k), ctypes.byref(v)), "kvc_layer_scales")
+    return k.value, v.value
 
 
 def kvc_create_rolling(layers, B, H_q, H_kv, D, window, dtype) -> int:
@@ -369,7 +384,7 @@ def _wrap_device(ptr: int, shape, dtype):
 
     class _Iface:
         def __init__(self):
-            typestr = {torch.bfloat16: "<i2", torch.float32: "<f4"}[dtype]
+            typestr = {torch.bfloat16: "<i2", torch.float32: "<f4", torch.int8: "|i1"}[dtype]
             self.__cuda_array_interface__ = {
                 "shape": tuple(shape), "typestr": typestr, "data": (ptr, False), "version": 2,
                 "strides": None,
@@ -421,3 +436,22 @@ class RollingKVCache(KVCache):
         self.layers, self.B, self.H_q, self.H_kv, self.D = layers, B, H_q, H_kv, D
         self.window = self.T_max = window
         self.h = kvc_create_rolling(layers, B, H_q, H_kv, D, window, self.dtype_code)
+
+
+class QuantKVCache(KVCache):
+    """Owns one int8 kvc handle: per layer, codes [B, H_kv, T_max, D] (int8) and row scales
+    [B, H_kv, T_max] (fp32) for K and V; q, out and new rows stay bf16."""
+
+    def __init__(self, layers, B, H_q, H_kv, D, T_max, dtype="bf16"):
+        self.dtype_code = {"bf16": KVC_BF16, KVC_BF16: KVC_BF16}[dtype]
+        self.layers, self.B, self.H_q, self.H_kv, self.D, self.T_max = layers, B, H_q, H_kv, D, T_max
+        self.h = kvc_create_quantized(layers, B, H_q, H_kv, D, T_max, self.dtype_code)
+
+    def layer_views(self, layer):
+        """torch views (no copy): K codes, V codes (int8) and K scales, V scales (fp32)."""
+        import torch
+        kp, vp = kvc_layer_ptrs(self.h, layer)
+        ks, vs = kvc_layer_scales(self.h, layer)
+        shape = (self.B, self.H_kv, self.T_max, self.D)
+        return (_wrap_device(kp, shape, torch.int8), _wrap_device(vp, shape, torch.int8),
+                _wrap_device(ks, shape[:3], torch.float32), _wrap_device(vs, shape[:3], torch.float32))

@@ -48,14 +48,16 @@ class Workload:
     def T_max(self) -> int:
         return int(self.lens().max())
 
-    def kv_read_bytes_per_layer(self, window: int = 0, new_tokens: int = 1) -> int:
+    def kv_read_bytes_per_layer(self, window: int = 0, new_tokens: int = 1, int8: bool = False) -> int:
         """Algorithmic KV bytes one decode step reads per layer: 2 H_kv D s sum_b L_b, with
         L_b capped at the window for sliding-window attention (window > 0), and L_b = T_b +
-        new_tokens when a step appends several tokens (the keys are read once for all of them)."""
+        new_tokens when a step appends several tokens (the keys are read once for all of them).
+        An int8 cache reads D one-byte codes and one 4-byte scale per row instead of D s."""
         lens = self.lens_pre() + new_tokens
         if window > 0:
             lens = lens.clamp(max=window)
-        return 2 * self.H_kv * self.D * self.elem_bytes * int(lens.sum())
+        row = self.D + 4 if int8 else self.D * self.elem_bytes
+        return 2 * self.H_kv * row * int(lens.sum())
 
 
 WORKLOADS = {
