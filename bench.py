@@ -385,12 +385,16 @@ def run_ours(args, w):
 
     # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    plain = not (args.paged or args.window or args.tq > 1 or args.int8)  # the oracle arm's workload
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and plain:
         threads = os.cpu_count() or 1
         cgbs, layers_done, secs, used = oracle_sample(w, budget_s=args.cpu_budget, threads=threads)
+        one_gbs, _, one_secs, _ = oracle_sample(w, budget_s=0.0, threads=1, max_layers=1)
         cpu = {"value": round(cgbs, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
                "sample": f"{layers_done} whole layer(s) of {w.name} ({secs:.1f} s of oracle time, "
-                         f"{used} threads)"}
+                         f"{used} threads)",
+               "single_thread": {"value": round(one_gbs, 4), "unit": "GB/s",
+                                 "sample": f"layer 0 of {w.name} on 1 thread ({one_secs:.1f} s)"}}
 
     if rank == 0:
         line = {
