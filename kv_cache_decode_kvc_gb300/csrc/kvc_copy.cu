@@ -136,10 +136,21 @@ int launch_prefill(const CopyParams& p, cudaStream_t s) {
     return (int)cudaGetLastError();
 }
 
+// A programmatic dependent launch of the combine kernel behind the decode kernel.
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s) {
-    const int blocks = p.B * p.H_kv * G;
-    if (dtype == 0) combine_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(p, D, G);
-    else combine_kernel<float><<<blocks, 128, 0, s>>>(p, D, G);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.H_kv * G));
+    cfg.blockDim = dim3(COMBINE_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p, D, G)
+                                     : cudaLaunchKernelEx(&cfg, combine_kernel<float>, p, D, G);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 

@@ -798,16 +798,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 }
 
 // Merges the partial states of streams cut across CTAs (combine_mode 1): one block per
-// (stream, query head of its group); threads over the segments, then over D.  Recomputes the
-// same partition as the decode kernels.
+// (stream, query head of its group).  Recomputes the same partition as the decode kernels.
+// The block's threads form SP segment lanes x D/4 column groups: lane j of a column group
+// sums segments j, j + SP, j + 2 SP, ... of four columns (float4 loads, four segments in
+// flight), and the SP partial sums meet in shared memory.  Launched as a programmatic
+// dependent of the decode kernel: lens is read before the grid dependency wait (the decode
+// kernel does not write it) when launch overlap is on, the partials after it.
 constexpr int COMBINE_MAX_SEG = 1024;
+constexpr int COMBINE_THREADS = 256;
 template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int D, int G) {
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodeParams p, int D, int G) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int NWARP = COMBINE_THREADS / 32;
     const int u = blockIdx.x / G, hg = blockIdx.x % G;
     const int b = u / p.H_kv, h = u % p.H_kv;
     __shared__ int64_t sh_sum[2];
     __shared__ float sw[COMBINE_MAX_SEG];
-    __shared__ float sred[4];
+    __shared__ float sred[NWARP];
+    __shared__ float4 spart[COMBINE_THREADS];
     if (threadIdx.x < 2) sh_sum[threadIdx.x] = 0;
     __syncthreads();
     int64_t before = 0, all = 0;
@@ -820,6 +829,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[0]), (unsigned long long)before);
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[1]), (unsigned long long)all);
     __syncthreads();
+    if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int Lb = eff_len(p.lens[b], p.T_max, p.rolling, p.T_q);
     if (Lb == 0) return;
     const int64_t W = (int64_t)p.H_kv * sh_sum[1];
@@ -830,6 +840,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
     const int nseg = (int)(clast - cfirst + 1);
     if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs
     const size_t base = (size_t)(cfirst + u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // weights w_c = 2^(m_c - M) / sum_c 2^(m_c - M) l_c, formed once in shared memory
     float mx = -INFINITY;
     for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
@@ -838,9 +849,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
         mx = fmaxf(mx, mc);
     }
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-    if ((threadIdx.x & 31) == 0) sred[threadIdx.x >> 5] = mx;
+    if (lane == 0) sred[warp] = mx;
     __syncthreads();
-    const float M = fmaxf(fmaxf(sred[0], sred[1]), fmaxf(sred[2], sred[3]));
+    float M = sred[0];
+    for (int w = 1; w < NWARP; ++w) M = fmaxf(M, sred[w]);
     __syncthreads();
     float den = 0.f;
     for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
@@ -849,24 +861,56 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int 
         den = fmaf(w, p.part_ml[((base + c) * G + hg) * 2 + 1], den);
     }
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
-    if ((threadIdx.x & 31) == 0) sred[threadIdx.x >> 5] = den;
+    if (lane == 0) sred[warp] = den;
     __syncthreads();
-    const float inv = 1.f / (sred[0] + sred[1] + sred[2] + sred[3]);
-    const size_t stride = (size_t)G * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const float* po = p.part_o + base * stride + (size_t)hg * D + d;
-        float acc = 0.f;
-        int c = 0;
-        for (; c + 4 <= nseg; c += 4) {
-            const float v0 = po[(size_t)c * stride], v1 = po[(size_t)(c + 1) * stride];
-            const float v2 = po[(size_t)(c + 2) * stride], v3 = po[(size_t)(c + 3) * stride];
-            acc = fmaf(sw[c], v0, acc);
-            acc = fmaf(sw[c + 1], v1, acc);
-            acc = fmaf(sw[c + 2], v2, acc);
-            acc = fmaf(sw[c + 3], v3, acc);
+    float dsum = 0.f;
+    for (int w = 0; w < NWARP; ++w) dsum += sred[w];
+    const float inv = 1.f / dsum;
+    // D % 4 == 0 and D <= 4 * COMBINE_THREADS for every instantiated head dimension
+    const int D4 = D >> 2, SP = COMBINE_THREADS / D4;
+    const int d4 = threadIdx.x % D4, j = threadIdx.x / D4;
+    const size_t st4 = (size_t)G * D4;  // float4s between consecutive segments
+    const float4* po = reinterpret_cast<const float4*>(p.part_o) + base * st4 + (size_t)hg * D4 + d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < SP) {
+        int c = j;
+        for (; c + 3 * SP < nseg; c += 4 * SP) {
+            float4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = __ldcg(po + (size_t)(c + i * SP) * st4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float w = sw[c + i * SP];
+                acc.x = fmaf(w, v[i].x, acc.x);
+                acc.y = fmaf(w, v[i].y, acc.y);
+                acc.z = fmaf(w, v[i].z, acc.z);
+                acc.w = fmaf(w, v[i].w, acc.w);
+            }
         }
-        for (; c < nseg; ++c) acc = fmaf(sw[c], po[(size_t)c * stride], acc);
-        Elem<T>::store(p.out, ((size_t)u * G + hg) * D + d, acc * inv);
+        for (; c < nseg; c += SP) {
+            const float4 v = __ldcg(po + (size_t)c * st4);
+            const float w = sw[c];
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+    }
+    spart[threadIdx.x] = acc;
+    __syncthreads();
+    if (j == 0) {
+        for (int jj = 1; jj < SP; ++jj) {
+            const float4 v = spart[jj * D4 + d4];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const size_t o = ((size_t)u * G + hg) * D + (size_t)d4 * 4;
+        Elem<T>::store(p.out, o, acc.x * inv);
+        Elem<T>::store(p.out, o + 1, acc.y * inv);
+        Elem<T>::store(p.out, o + 2, acc.z * inv);
+        Elem<T>::store(p.out, o + 3, acc.w * inv);
     }
 }
 

@@ -32,7 +32,11 @@ struct Tc5Cfg {
     static constexpr int N = G < 16 ? 16 : G;           // MMA N (heads, padded)
     static constexpr int ROWB = D * 2;
     static constexpr int HALVES = D / 64;               // 128-byte column blocks
-    static constexpr int NW = 4;                        // softmax warps (+ producer + MMA warp)
+    // softmax warps (+ producer + MMA warp): HSPLIT per tensor-memory lane quadrant, each with
+    // GH = G / HSPLIT of the group's head columns (large groups: more warps, fewer registers each)
+    static constexpr int HSPLIT = G >= 16 ? 2 : 1;
+    static constexpr int GH = G / HSPLIT;
+    static constexpr int NW = 4 * HSPLIT;
     static constexpr int NEPI = 2;                      // segment-epilogue warps
     static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
     static constexpr int NCONV = 4;                     // int8 -> bf16 converter warps (int8 cache)
@@ -52,7 +56,7 @@ struct Tc5Cfg {
     static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
     static constexpr int MERGE_FLOATS = G * (D + 2);
     static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
-    static constexpr int RED_BYTES = NW * N * 4;        // cross-warp max reduction
+    static constexpr int RED_BYTES = 4 * N * 4;         // cross-warp reductions, [quadrant][N]
     // 4 tensor maps: K and V with 128-row boxes (full tiles) and 32-row boxes (partial tiles)
     static constexpr int MISC_BYTES = 256;
     static constexpr int ALIGN_PAD = 1024;
@@ -66,6 +70,7 @@ struct Tc5Cfg {
     static constexpr int TMEM_COLS = 6 * N <= 32 ? 32 : (6 * N <= 64 ? 64 : (6 * N <= 128 ? 128 : 256));
     static_assert(NST >= 2, "ring too shallow");
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
+    static_assert(HSPLIT == 1 || GH % 8 == 0, "head slices start on a swizzle row group");
     static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
 };
 
@@ -130,6 +135,25 @@ __device__ __forceinline__ void tc5_ld16(uint32_t taddr, float (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc5_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+// NC (8 or 16) consecutive columns.
+template <int NC>
+__device__ __forceinline__ void tc5_ld(uint32_t taddr, float (&v)[NC]) {
+    if constexpr (NC == 8) tc5_ld8(taddr, v);
+    else tc5_ld16(taddr, v);
 }
 
 // Issues one tile: a full tile is one 128-row box per column block of K and of V (maps tmKf /
@@ -272,16 +296,17 @@ __device__ __forceinline__ void widen_i8x16(const uint4& v, uint4& o0, uint4& o1
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// Named barrier of the four softmax warps with an OR reduction of a predicate.
+// Named barrier of the NT softmax threads with an OR reduction of a predicate.
+template <int NT>
 __device__ __forceinline__ bool softmax_group_any(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "n"(NT)
         : "memory");
     return r != 0;
 }
@@ -372,10 +397,10 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&s_empty[i], C::NW);
+            mbar_init(&p_full[i], C::NW);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_empty[i], 4);
+            mbar_init(&o_empty[i], C::NW);
         }
         mbar_init(m_full, C::NW * 32);
         mbar_init(m_empty, C::NEPI * 32);
@@ -500,7 +525,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         tc5_fence_before();
-        named_bar_sync(2, 160);
+        named_bar_sync(2, 32 + C::NW * 32);
         tc5_fence_after();
         tmem = *tmem_slot;
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
@@ -654,7 +679,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // ======================================================= softmax + accumulate
         // zero the padded q rows and the P rows of padded heads (they stay zero), and write the
         // fused append's new rows; then meet the MMA warp (named barrier 2) for the TMEM base
-        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += 128)
+        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += C::NW * 32)
             reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
         if (warp == 2 && fused) {
             SegIter it;
@@ -712,15 +737,17 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         }
         fence_async_smem();
         tc5_fence_before();
-        named_bar_sync(2, 160);
+        named_bar_sync(2, 32 + C::NW * 32);
         tc5_fence_after();
         tmem = *tmem_slot;
+        constexpr int GH = C::GH, NT = C::NW * 32;
+        constexpr int CH = GH <= 8 ? 8 : 16;  // tensor-memory columns per load
         const int q4 = warp & 3;            // tensor-memory lane quadrant of this warp
+        const int h0 = ((warp - 2) >> 2) * GH;  // this warp's head slice [h0, h0 + GH)
         const int row = q4 * 32 + lane;     // token of S^T rows / element d of O^T rows
-        const int gt = tid - 64;            // 0..127 within the group
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const float qscale = p.qscale;
-        float o[G], m[G], l[G], alpha[G], alpha_prev[G];
+        float o[GH], m[GH], l[GH], alpha[GH], alpha_prev[GH];
         TileCursor<TT> cur;
         cur.init(prefix, B, H_kv, r0, r1);
         int s = 0, sg = 0;
@@ -730,15 +757,15 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // O^T(j) into the accumulator: o = o * alpha_j + (O^T_hi + O^T_lo)(j)[row, :]
             alive = alive && mbar_wait(&o_full[j & 1], (j >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
-            const uint32_t ob = tmem + (uint32_t)(2 * N + (j & 1) * C::N2) + lane_off;
-            float hi[16], lo[16];
+            const uint32_t ob = tmem + (uint32_t)(2 * N + (j & 1) * C::N2 + h0) + lane_off;
+            float hi[CH], lo[CH];
 #pragma unroll
-            for (int c0 = 0; c0 < N && c0 < G; c0 += 16) {
-                tc5_ld16(ob + c0, hi);
-                tc5_ld16(ob + N + c0, lo);
+            for (int c0 = 0; c0 < GH; c0 += CH) {
+                tc5_ld<CH>(ob + c0, hi);
+                tc5_ld<CH>(ob + N + c0, lo);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (c0 + i < G) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], hi[i] + lo[i]) : o[c0 + i];
+                for (int i = 0; i < CH; ++i)
+                    if (c0 + i < GH) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], hi[i] + lo[i]) : o[c0 + i];
             }
             tc5_fence_before();
             __syncwarp();
@@ -769,7 +796,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             const bool first = cur.first(), last = cur.last();
             if (first) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) { o[h] = 0.f; m[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f; }
+                for (int h = 0; h < GH; ++h) { o[h] = 0.f; m[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f; }
             }
             // int8 cache: this row's K and V scales, loaded one tile ahead
             const float sk = sk_next, sv = sv_next;
@@ -782,15 +809,15 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // ---- scores of tile k
             alive = alive && mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
-            float x[G];
+            float x[GH];
             {
-                float v[16];
+                float v[CH];
 #pragma unroll
-                for (int c0 = 0; c0 < N && c0 < G; c0 += 16) {
-                    tc5_ld16(tmem + (uint32_t)((k & 1) * N + c0) + lane_off, v);
+                for (int c0 = 0; c0 < GH; c0 += CH) {
+                    tc5_ld<CH>(tmem + (uint32_t)((k & 1) * N + h0 + c0) + lane_off, v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (c0 + i < G) x[c0 + i] = v[i];
+                    for (int i = 0; i < CH; ++i)
+                        if (c0 + i < GH) x[c0 + i] = v[i];
                 }
             }
             tc5_fence_before();
@@ -803,48 +830,48 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             bool need = false;
             if (dmask <= 0) {  // visible to every query row (always with one new token)
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GH; ++h) {
                     x[h] = valid ? x[h] * qk : -INFINITY;
                     need |= x[h] > m[h] + TAU;
                 }
             } else {
                 const int tq1 = p.T_q - 1;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    x[h] = (valid && (h & tq1) >= dmask) ? x[h] * qk : -INFINITY;
+                for (int h = 0; h < GH; ++h) {
+                    x[h] = (valid && ((h0 + h) & tq1) >= dmask) ? x[h] * qk : -INFINITY;
                     need |= x[h] > m[h] + TAU;
                 }
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) alpha[h] = 1.f;
-            if (softmax_group_any(need)) {
+            for (int h = 0; h < GH; ++h) alpha[h] = 1.f;
+            if (softmax_group_any<NT>(need)) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GH; ++h) {
                     float mx = x[h];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
-                    if (lane == 0) red[q4 * N + h] = mx;
+                    if (lane == 0) red[q4 * N + h0 + h] = mx;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, NT);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float mx = red[h];
+                for (int h = 0; h < GH; ++h) {
+                    float mx = red[h0 + h];
 #pragma unroll
-                    for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[w * N + h]);
+                    for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[w * N + h0 + h]);
                     const float mn = fmaxf(m[h], mx);
                     alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
                     m[h] = mn;
                     l[h] *= alpha[h];
                 }
-                named_bar_sync(1, 128);  // red is reused
+                named_bar_sync(1, NT);  // red is reused
             }
             // ---- P(k) = P_hi + P_lo: rows h (hi) and N + h (lo) of the K-major swizzled operand,
-            // column = this thread's token
+            // column = this thread's token (h0 is a multiple of 8: the swizzle phase is h & 7)
             {
-                unsigned char* pb = pbuf + (k & 1) * C::PBUF + (row >> 6) * C::PBLOCK;
+                unsigned char* pb = pbuf + (k & 1) * C::PBUF + (row >> 6) * C::PBLOCK + h0 * 128;
                 const int chunk = (row & 63) >> 3, e = row & 7;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GH; ++h) {
                     const float pv = (x[h] == -INFINITY) ? 0.f : fast_exp2(x[h] - m[h]);
                     l[h] += pv;
                     // int8 cache: the V row scale folds into the weight (MMA2 reads the codes)
@@ -859,7 +886,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2)
             const int br = paged ? p.box_rows : C::BOX_ROWS;
             const int loaded = ((n + br - 1) / br) * br;
-            if (row >= loaded) {
+            if (h0 == 0 && row >= loaded) {
                 using LY = Tc5Layout<C, PAGED>;
                 unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + (row >> 3) * LY::GSTR + (row & 7) * 128;
 #pragma unroll
@@ -874,28 +901,32 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // ---- fold in O^T of the previous tile of this segment
             if (!first) absorb(k - 1, alpha_prev);
 #pragma unroll
-            for (int h = 0; h < G; ++h) alpha_prev[h] = alpha[h];
+            for (int h = 0; h < GH; ++h) alpha_prev[h] = alpha[h];
             if (last) {
                 absorb(k, alpha);
                 // ---- segment epilogue: group-wide denominators, then the shared merge
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int h = 0; h < GH; ++h) {
                     float s_ = l[h];
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) s_ += __shfl_xor_sync(FULL, s_, off);
-                    if (lane == 0) red[q4 * N + h] = s_;
+                    if (lane == 0) red[q4 * N + h0 + h] = s_;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, NT);
                 // hand the segment's state to the epilogue warps (merge: [G][D + 2])
                 alive = alive && mbar_wait(m_empty, (uint32_t)(sg & 1) ^ 1u, abort_flag, p.err);
 #pragma unroll
-                for (int h = 0; h < G; ++h) merge[h * (D + 2) + row] = o[h];
-                if (gt < G) {
+                for (int h = 0; h < GH; ++h) merge[(h0 + h) * (D + 2) + row] = o[h];
+                if (q4 == 0 && lane < GH) {
+                    // lane i of a slice's quadrant-0 warp: maximum and denominator of head h0 + i
+                    float mv = m[0];
+#pragma unroll
+                    for (int h = 1; h < GH; ++h) mv = lane == h ? m[h] : mv;
                     float s_ = 0.f;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) s_ += red[w * N + gt];
-                    merge[gt * (D + 2) + D] = m[gt];
-                    merge[gt * (D + 2) + D + 1] = s_;
+                    for (int w = 0; w < 4; ++w) s_ += red[w * N + h0 + lane];
+                    merge[(h0 + lane) * (D + 2) + D] = mv;
+                    merge[(h0 + lane) * (D + 2) + D + 1] = s_;
                 }
                 mbar_arrive(m_full);
                 ++sg;
