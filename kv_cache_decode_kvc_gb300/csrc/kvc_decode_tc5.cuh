@@ -296,17 +296,17 @@ __device__ __forceinline__ void widen_i8x16(const uint4& v, uint4& o0, uint4& o1
     o1 = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
-// Named barrier of the NT softmax threads with an OR reduction of a predicate.
-template <int NT>
-__device__ __forceinline__ bool softmax_group_any(bool pred) {
+// Named barrier BAR of NT threads with an OR reduction of a predicate.
+template <int BAR, int NT>
+__device__ __forceinline__ bool group_any(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred), "n"(NT)
+        : "r"((uint32_t)pred), "n"(BAR), "n"(NT)
         : "memory");
     return r != 0;
 }
@@ -481,6 +481,17 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     if (!work) return;
     const bool fused = p.k_new != nullptr;
     uint32_t tmem = 0;
+    // The CTA's last segment is finished (output, partial state, and the stream's merge when
+    // this CTA is the last of it) by the epilogue and the softmax warps together (named
+    // barrier 5): nothing else is left to overlap it with.  Both groups always arrive; the
+    // work is skipped by all of them if any member gave up on a wait.
+    constexpr int NJ = C::NEPI + C::NW;
+    auto final_segment = [&](bool ok, const SegIter& it, int jt) {
+        const bool skip = group_any<5, NJ * 32>(!ok || *abort_flag != 0);
+        if (!skip)
+            finish_segment<T, G, D, C::HS, 1, NJ, 5>(p, merge, it, (size_t)it.b * H_kv + it.h, W, P,
+                                                     last_flag, jt);
+    };
 
     if (warp == 0) {
         // ======================================================= producer
@@ -669,11 +680,17 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         bool ok = true;
         for (int sg = 0; it.valid; ++sg) {
             ok = ok && mbar_wait(m_full, (uint32_t)(sg & 1), abort_flag, p.err);
+            SegIter nx = it;
+            nx.next();
+            if (!nx.valid) {
+                final_segment(ok, it, et);
+                break;
+            }
             if (ok)
                 finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
                                                               W, P, last_flag, et);
             mbar_arrive(m_empty);
-            it.next();
+            it = nx;
         }
     } else {
         // ======================================================= softmax + accumulate
@@ -791,6 +808,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         float sk_next = 1.f, sv_next = 1.f;
         if constexpr (QUANT)
             if (cur.valid) load_scales(cur, sk_next, sv_next);
+        SegIter last_it = cur.it;  // the segment of the latest `last` tile
         for (int k = 0; cur.valid; ++k) {
             const int n = cur.n();
             const bool first = cur.first(), last = cur.last();
@@ -844,7 +862,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             }
 #pragma unroll
             for (int h = 0; h < GH; ++h) alpha[h] = 1.f;
-            if (softmax_group_any<NT>(need)) {
+            if (group_any<1, NT>(need)) {
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     float mx = x[h];
@@ -929,11 +947,15 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     merge[(h0 + lane) * (D + 2) + D + 1] = s_;
                 }
                 mbar_arrive(m_full);
+                last_it = cur.it;
                 ++sg;
             }
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
+        // join the epilogue warps on the last segment, once every softmax warp's state is in
+        if (sg > 0) alive = alive && mbar_wait(m_full, (uint32_t)((sg - 1) & 1), abort_flag, p.err);
+        final_segment(alive && sg > 0, last_it, C::NEPI * 32 + (tid - 64));
     }
     if (*abort_flag) {
         // broken protocol (a wait timed out): let issued copies and MMAs land, bounded
