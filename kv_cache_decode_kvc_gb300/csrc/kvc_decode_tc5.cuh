@@ -48,15 +48,21 @@ struct Tc5Cfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + QRAW_BYTES;
     static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128] operand
     static constexpr int OPB_BYTES = HALVES * OPB_BLOCK;
-    // P operand of MMA2: rows [0, N) = P_hi, rows [N, 2N) = P_lo (one MMA with N2 = 2N columns);
-    // PBLOCK = one 64-token column block of it, PBUF = one whole 128-token buffer
-    static constexpr int N2 = 2 * N;
+    // P operand of MMA2, P_hi and P_lo side by side as the N2 columns of one MMA:
+    //  K-major (G <= 8): rows [0, N) = P_hi, rows [N, 2N) = P_lo, in 64-token column blocks of
+    //    PBLOCK bytes (a thread stores its token's weights one bf16 at a time);
+    //  MN-major (G >= 16): one 128-byte row per token, P_hi at columns [0, N) and P_lo at
+    //    [32, 32 + N) (a thread stores its token's weights in 16-byte vectors).
+    // PBUF = one whole 128-token buffer.
+    static constexpr bool PMN = G >= 16;
+    static constexpr int N2 = PMN ? 64 : 2 * N;
+    static constexpr int LOOFF = PMN ? 32 : N;          // column of P_lo, and of O^T_lo
     static constexpr int PBLOCK = N2 * 128;
-    static constexpr int PBUF = (TT / 64) * PBLOCK;
+    static constexpr int PBUF = PMN ? TT * 128 : (TT / 64) * PBLOCK;
     static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
     static constexpr int MERGE_FLOATS = G * (D + 2);
     static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
-    static constexpr int RED_BYTES = 4 * N * 4;         // cross-warp reductions, [quadrant][N]
+    static constexpr int RED_BYTES = 6 * N * 4;         // reductions [quadrant][N], rescale factors [2][N]
     // 4 tensor maps: K and V with 128-row boxes (full tiles) and 32-row boxes (partial tiles)
     static constexpr int MISC_BYTES = 256;
     static constexpr int ALIGN_PAD = 1024;
@@ -66,11 +72,13 @@ struct Tc5Cfg {
     static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NST = NST_A > 4 ? 4 : NST_A;
     static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
-    // S^T buffers [0, N) and [N, 2N); O^T buffers (hi and lo halves) [2N, 4N) and [4N, 6N)
-    static constexpr int TMEM_COLS = 6 * N <= 32 ? 32 : (6 * N <= 64 ? 64 : (6 * N <= 128 ? 128 : 256));
+    // S^T buffers [0, N) and [N, 2N); O^T buffers (hi and lo columns) [2N, 2N + N2), [2N + N2, 2N + 2 N2)
+    static constexpr int TMEM_NEED = 2 * N + 2 * N2;
+    static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : 256));
     static_assert(NST >= 2, "ring too shallow");
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(HSPLIT == 1 || GH % 8 == 0, "head slices start on a swizzle row group");
+    static_assert(!PMN || N <= 32, "P_hi and P_lo share one 64-column row");
     static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
 };
 
@@ -363,7 +371,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
     int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
     float* red = reinterpret_cast<float*>(prefix + MAX_B + 1);  // [4][N]
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(red + 4 * N);
+    float* alpha_s = red + 4 * N;                                  // [2][N]: rescale factor of a tile
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(red + 6 * N);
     uint64_t* empty_bar = full_bar + NST;
     uint64_t* s_full = empty_bar + NST;   // [2]
     uint64_t* s_empty = s_full + 2;
@@ -540,13 +549,16 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         tc5_fence_after();
         tmem = *tmem_slot;
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
-        constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, 0);  // V read MN-major x [P_hi; P_lo]
+        constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
         const uint32_t qsw_s = smem_addr(qsw), pbuf_s = smem_addr(pbuf);
         using LY = Tc5Layout<C, PAGED>;
         const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);                  // + stage, block, k-step
         const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
         const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
-        const uint64_t dP0 = smem_desc_sw128(pbuf_s, 16u, 1024u);
+        // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
+        // leading offset is never stepped over)
+        const uint64_t dP0 = C::PMN ? smem_desc_sw128(pbuf_s, (uint32_t)C::PBUF, 1024u)
+                                    : smem_desc_sw128(pbuf_s, 16u, 1024u);
         TileCursor<TT> cur;
         cur.init(prefix, B, H_kv, r0, r1);
         int s = 0, s_prev = 0;
@@ -566,7 +578,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
                     for (int kk = 0; kk < TS; ++kk) {
                         const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2 * LY::GSTR);
-                        const uint32_t poff = pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
+                        const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
+                                                     : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
                         tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
                     }
                     tc5_commit(&o_full[j & 1]);
@@ -764,25 +777,34 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         const int row = q4 * 32 + lane;     // token of S^T rows / element d of O^T rows
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const float qscale = p.qscale;
-        float o[GH], m[GH], l[GH], alpha[GH], alpha_prev[GH];
+        // o: this thread's output element for the slice's heads; m: the group's running maxima
+        // (the same in every thread), mt = m + TAU; l: this thread's share of the denominators.
+        // The rescale factors of a tile whose maxima moved scale o when that tile's O^T is
+        // folded in: kept in registers (alpha, alpha_prev) for small groups, in shared memory
+        // (alpha_s[tile & 1], the same for every thread) for groups of 16+ heads, whose threads
+        // have no registers to spare.
+        constexpr bool ASH = C::PMN;
+        float o[GH], m[GH], mt[GH], l[GH], alpha[GH], alpha_prev[GH];
         TileCursor<TT> cur;
         cur.init(prefix, B, H_kv, r0, r1);
         int s = 0, sg = 0;
         uint32_t ph = 0;
         bool alive = true;
-        auto absorb = [&](int j, const float* a) {
+        auto absorb = [&](int j, bool resc, const float* areg) {
             // O^T(j) into the accumulator: o = o * alpha_j + (O^T_hi + O^T_lo)(j)[row, :]
             alive = alive && mbar_wait(&o_full[j & 1], (j >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
             const uint32_t ob = tmem + (uint32_t)(2 * N + (j & 1) * C::N2 + h0) + lane_off;
+            const float* al = ASH ? alpha_s + (j & 1) * N + h0 : areg;
             float hi[CH], lo[CH];
 #pragma unroll
             for (int c0 = 0; c0 < GH; c0 += CH) {
                 tc5_ld<CH>(ob + c0, hi);
-                tc5_ld<CH>(ob + N + c0, lo);
+                tc5_ld<CH>(ob + C::LOOFF + c0, lo);
 #pragma unroll
                 for (int i = 0; i < CH; ++i)
-                    if (c0 + i < GH) o[c0 + i] = alive ? fmaf(o[c0 + i], a[c0 + i], hi[i] + lo[i]) : o[c0 + i];
+                    if (c0 + i < GH)
+                        o[c0 + i] = fmaf(o[c0 + i], (ASH && !resc) ? 1.f : al[c0 + i], hi[i] + lo[i]);
             }
             tc5_fence_before();
             __syncwarp();
@@ -809,12 +831,15 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         if constexpr (QUANT)
             if (cur.valid) load_scales(cur, sk_next, sv_next);
         SegIter last_it = cur.it;  // the segment of the latest `last` tile
+        bool resc_prev = false;    // the previous tile moved the maxima
         for (int k = 0; cur.valid; ++k) {
             const int n = cur.n();
             const bool first = cur.first(), last = cur.last();
             if (first) {
 #pragma unroll
-                for (int h = 0; h < GH; ++h) { o[h] = 0.f; m[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f; }
+                for (int h = 0; h < GH; ++h) {
+                    o[h] = 0.f; m[h] = -INFINITY; mt[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f;
+                }
             }
             // int8 cache: this row's K and V scales, loaded one tile ahead
             const float sk = sk_next, sv = sv_next;
@@ -850,19 +875,21 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     x[h] = valid ? x[h] * qk : -INFINITY;
-                    need |= x[h] > m[h] + TAU;
+                    need |= x[h] > mt[h];
                 }
             } else {
                 const int tq1 = p.T_q - 1;
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     x[h] = (valid && ((h0 + h) & tq1) >= dmask) ? x[h] * qk : -INFINITY;
-                    need |= x[h] > m[h] + TAU;
+                    need |= x[h] > mt[h];
                 }
             }
+            if constexpr (!ASH)
 #pragma unroll
-            for (int h = 0; h < GH; ++h) alpha[h] = 1.f;
-            if (group_any<1, NT>(need)) {
+                for (int h = 0; h < GH; ++h) alpha[h] = 1.f;
+            const bool resc = group_any<1, NT>(need);
+            if (resc) {
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     float mx = x[h];
@@ -877,25 +904,57 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
                     for (int w = 1; w < 4; ++w) mx = fmaxf(mx, red[w * N + h0 + h]);
                     const float mn = fmaxf(m[h], mx);
-                    alpha[h] = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
+                    const float a = (mn == -INFINITY) ? 1.f : fast_exp2(m[h] - mn);
                     m[h] = mn;
-                    l[h] *= alpha[h];
+                    mt[h] = mn + TAU;
+                    l[h] *= a;
+                    if constexpr (ASH) {
+                        if (row == 0) alpha_s[(k & 1) * N + h0 + h] = a;
+                    } else {
+                        alpha[h] = a;
+                    }
                 }
-                named_bar_sync(1, NT);  // red is reused
+                named_bar_sync(1, NT);  // red is reused; alpha_s is written
             }
-            // ---- P(k) = P_hi + P_lo: rows h (hi) and N + h (lo) of the K-major swizzled operand,
-            // column = this thread's token (h0 is a multiple of 8: the swizzle phase is h & 7)
-            {
+            // ---- P(k) = P_hi + P_lo for this thread's token; a score of -inf (masked, or no key
+            // seen yet: -inf - -inf) gives weight 0
+            float pw[GH];
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                const float pv = fast_exp2(fmaxf(x[h] - m[h], -INFINITY));
+                l[h] += pv;
+                // int8 cache: the V row scale folds into the weight (MMA2 reads the codes)
+                pw[h] = QUANT ? pv * sv : pv;
+            }
+            if constexpr (C::PMN) {
+                // MN-major: the token's row of 64 columns, 16-byte chunks swizzled by token & 7
+                unsigned char* pr = pbuf + (k & 1) * C::PBUF + row * 128;
+                const int sw = row & 7;
+#pragma unroll
+                for (int c = 0; c < GH / 8; ++c) {
+                    uint32_t whi[4], wlo[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(pw[8 * c + 2 * i], pw[8 * c + 2 * i + 1]);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(pw[8 * c + 2 * i] - hf.x,
+                                                                        pw[8 * c + 2 * i + 1] - hf.y);
+                        whi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                        wlo[i] = *reinterpret_cast<const uint32_t*>(&l2);
+                    }
+                    const int chi = (h0 >> 3) + c, clo = (C::LOOFF >> 3) + (h0 >> 3) + c;
+                    *reinterpret_cast<uint4*>(pr + ((chi ^ sw) << 4)) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+                    *reinterpret_cast<uint4*>(pr + ((clo ^ sw) << 4)) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+                }
+            } else {
+                // K-major: rows h (hi) and N + h (lo), column = this thread's token (h0 is a
+                // multiple of 8: the swizzle phase is h & 7)
                 unsigned char* pb = pbuf + (k & 1) * C::PBUF + (row >> 6) * C::PBLOCK + h0 * 128;
                 const int chunk = (row & 63) >> 3, e = row & 7;
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    const float pv = (x[h] == -INFINITY) ? 0.f : fast_exp2(x[h] - m[h]);
-                    l[h] += pv;
-                    // int8 cache: the V row scale folds into the weight (MMA2 reads the codes)
-                    const float pw = QUANT ? pv * sv : pv;
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(pw);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(pw - __bfloat162float(hi));
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(pw[h]);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(pw[h] - __bfloat162float(hi));
                     const uint32_t off = (((chunk ^ (h & 7)) << 4) | (e << 1));  // N % 8 == 0
                     *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + off) = hi;
                     *reinterpret_cast<__nv_bfloat16*>(pb + (N + h) * 128 + off) = lo;
@@ -917,11 +976,13 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[k & 1]);
             // ---- fold in O^T of the previous tile of this segment
-            if (!first) absorb(k - 1, alpha_prev);
+            if (!first) absorb(k - 1, resc_prev, alpha_prev);
+            resc_prev = resc;
+            if constexpr (!ASH)
 #pragma unroll
-            for (int h = 0; h < GH; ++h) alpha_prev[h] = alpha[h];
+                for (int h = 0; h < GH; ++h) alpha_prev[h] = alpha[h];
             if (last) {
-                absorb(k, alpha);
+                absorb(k, resc, alpha);
                 // ---- segment epilogue: group-wide denominators, then the shared merge
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {

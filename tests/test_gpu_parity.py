@@ -136,6 +136,17 @@ def test_split_t_any_split_matches(ctas, mode, math):
     check_close(out, case.oracle_out(T_max), case.dtype, f"ctas={ctas} mode={mode} math={math}")
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("ctas", [3, 7, 152])
+@pytest.mark.parametrize("G", [16, 32])
+def test_split_t_large_groups_tcgen05(G, ctas, mode):
+    # groups of 16 and 32 heads (eight softmax warps, weights stored MN-major) cut across CTAs
+    case = Case(58 + G, 3, 2 * G, 2, 128, [1500, 3, 700], "bf16")
+    T_max = 1600
+    out, _, _ = _run(case, T_max, ctas=ctas, mode=mode, math=3)
+    check_close(out, case.oracle_out(T_max), case.dtype, f"G={G} ctas={ctas} mode={mode}")
+
+
 @pytest.mark.parametrize("ctas", [1, 5, 64])
 def test_split_t_fp32_is_tight(ctas):
     case = Case(56, 3, 32, 1, 128, [2000, 17, 900], "f32")
