@@ -386,13 +386,14 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     int* last_flag = issued + NST + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(issued + NST + 2);
     int* mma_issued = issued + NST + 3;                      // MMA2 commits issued (abort drain)
+    int* mma1_issued = issued + NST + 4;                     // MMA1 commits issued (abort drain)
     // (append_bar follows at the next 8-byte boundary)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.B, H_kv = p.H_kv;
     const size_t row_elems_q = (size_t)H_kv * G * D;
     uint64_t* append_bar = reinterpret_cast<uint64_t*>(
-        (reinterpret_cast<uintptr_t>(mma_issued + 1) + 7) & ~uintptr_t(7));
+        (reinterpret_cast<uintptr_t>(mma1_issued + 1) + 7) & ~uintptr_t(7));
     uint64_t* conv_full = append_bar + 1;  // [NST] int8 cache: the stage's tiles are bf16 now
 
     // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         *abort_flag = 0;
         *last_flag = 0;
         *mma_issued = 0;
+        *mma1_issued = 0;
         fence_mbar_init();
     }
     if (tid == 0) {
@@ -513,32 +515,88 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                                              TILE_Q, ent, lane);
                 c0.advance();
             }
-            int s = npre == NST ? 0 : npre;
-            uint32_t ph = npre == NST ? 1u : 0u;
             if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
-            while (pref.valid) {
-                // lane 0 waits; the warp follows its verdict (paged: every lane issues a block)
+            // a tile that holds a stream's new token waits for the fused append's writes (lane 0
+            // waits; the warp follows its verdict: paged, every lane issues a block)
+            auto append_ready = [&]() {
                 bool ok = true;
+                if (lane == 0 && fused && nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n()))
+                    ok = mbar_wait(append_bar, 0u, abort_flag, p.err);
+                if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                return ok;
+            };
+            auto issue_next = [&](int st) {
+                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, st, pol, &tmK, &tmV, &tmKf, &tmVf,
+                                             TILE_ALL, ent, lane);
+                if (lane == 0) issued[st] += 1;
+                pref.advance();
+                // the next tile's blocks load while lane 0 waits
+                if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
+            };
+            bool ok = true;
+            // the rest of the ring's first pass: those stages are free
+            for (int st = npre; st < NST && pref.valid; ++st) {
+                ok = append_ready();
+                if (!ok) break;
+                issue_next(st);
+            }
+            // MMA2 of each tile (this thread issues it: MMA1 is warp 1's), then the tile NST ahead
+            // into the stage that MMA2 frees.  Issued here so that MMA1 of the next tile never
+            // queues behind it in one thread (each tcgen05.mma takes ~90 cycles to issue).
+            constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
+            using LY = Tc5Layout<C, PAGED>;
+            const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
+            // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
+            // leading offset is never stepped over)
+            const uint32_t pbuf_s = smem_addr(pbuf);
+            const uint64_t dP0 = C::PMN ? smem_desc_sw128(pbuf_s, (uint32_t)C::PBUF, 1024u)
+                                        : smem_desc_sw128(pbuf_s, 16u, 1024u);
+            TileCursor<TT> mc;
+            mc.init(prefix, B, H_kv, r0, r1);
+            int s2 = 0;
+            for (int k = 0; ok && mc.valid; ++k) {
+                // ---- MMA2(k): O^T[k&1] = V(stage s2)^T . (P_hi + P_lo)^T
                 if (lane == 0) {
-                    ok = mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err);
-                    // a tile that holds a stream's new token waits for the fused append's writes
-                    if (ok && fused && nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n()))
-                        ok = mbar_wait(append_bar, 0u, abort_flag, p.err);
+                    ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
+                         mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+                    if (ok) {
+                        tc5_fence_after();
+                        // written by warp 1's allocation before the weights of tile 0 existed
+                        if (k == 0) tmem = *tmem_slot;
+                        const uint32_t tO = tmem + (uint32_t)(2 * N + (k & 1) * C::N2);
+                        const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
+#pragma unroll
+                        for (int kk = 0; kk < TS; ++kk) {
+                            const uint32_t voff = (uint32_t)(s2 * C::STAGE_BYTES + kk * 2 * LY::GSTR);
+                            const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
+                                                         : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
+                            tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
+                        }
+                        tc5_commit(&o_full[k & 1]);
+                        tc5_commit(&empty_bar[s2]);  // K/V of the stage are consumed
+                        *mma_issued += 1;
+                    }
                 }
                 if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, s, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                             TILE_ALL, ent, lane);
-                if (lane == 0) issued[s] += 1;
-                pref.advance();
-                // the next tile's blocks load while lane 0 waits for a free stage
-                if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
-                if (++s == NST) { s = 0; ph ^= 1u; }
+                if (ok && pref.valid) {
+                    // tile k + NST goes into stage s2 once MMA2(k) has read it
+                    if (lane == 0) ok = mbar_wait(&empty_bar[s2], (uint32_t)((k / NST) & 1), abort_flag, p.err);
+                    if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                    if (ok) ok = append_ready();
+                    if (ok) issue_next(s2);
+                }
+                mc.advance();
+                if (++s2 == NST) s2 = 0;
             }
         }
     } else if (warp == 1) {
-        // ======================================================= MMA issue
-        // tensor memory: S^T buffers at columns [0, N) and [N, 2N); O^T at [2N, 3N) and [3N, 4N)
+        // ======================================================= MMA1 issue
+        // Allocates tensor memory: S^T buffers at columns [0, N) and [N, 2N); O^T at
+        // [2N, 2N + N2) and [2N + N2, 2N + 2 N2).  MMA1 of each tile is issued as soon as its K
+        // tile and an S^T buffer are free; MMA2 is issued by the producer thread.  Each commits
+        // its own MMAs (a commit tracks the issuing thread's operations); MMA1 of a tile has
+        // completed before its MMA2 is issued (S^T -> softmax -> P), so MMA2's commit of the
+        // stage's empty barrier covers both reads of the stage.
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
                      "r"(C::TMEM_COLS)
@@ -549,47 +607,16 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         tc5_fence_after();
         tmem = *tmem_slot;
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
-        constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
-        const uint32_t qsw_s = smem_addr(qsw), pbuf_s = smem_addr(pbuf);
+        const uint32_t qsw_s = smem_addr(qsw);
         using LY = Tc5Layout<C, PAGED>;
-        const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);                  // + stage, block, k-step
-        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
-        const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
-        // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
-        // leading offset is never stepped over)
-        const uint64_t dP0 = C::PMN ? smem_desc_sw128(pbuf_s, (uint32_t)C::PBUF, 1024u)
-                                    : smem_desc_sw128(pbuf_s, 16u, 1024u);
         TileCursor<TT> cur;
         cur.init(prefix, B, H_kv, r0, r1);
-        int s = 0, s_prev = 0;
+        int s = 0;
         uint32_t ph = 0;
         bool alive = true;
-        for (int k = 0;; ++k) {
-            // MMA2 of the previous tile first: it frees a ring stage as soon as P is ready
-            if (k > 0 && alive) {
-                // ---- MMA2(k-1): O^T[(k-1)&1] = V(stage s_prev)^T . (P_hi + P_lo)^T
-                const int j = k - 1;
-                alive = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err) &&
-                        mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
-                if (alive && lane == 0) {
-                    tc5_fence_after();
-                    const uint32_t tO = tmem + (uint32_t)(2 * N + (j & 1) * C::N2);
-                    const uint32_t pb = (uint32_t)((j & 1) * C::PBUF);
-#pragma unroll
-                    for (int kk = 0; kk < TS; ++kk) {
-                        const uint32_t voff = (uint32_t)(s_prev * C::STAGE_BYTES + kk * 2 * LY::GSTR);
-                        const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
-                                                     : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
-                        tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
-                    }
-                    tc5_commit(&o_full[j & 1]);
-                    tc5_commit(&empty_bar[s_prev]);  // K/V of the stage are consumed
-                    *mma_issued += 1;
-                }
-                __syncwarp();
-            }
-            const bool have = cur.valid && alive;
-            if (!have) break;
+        const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);  // + stage, block, k-step
+        const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
+        for (int k = 0; cur.valid && alive; ++k) {
             // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
             // int8 cache: wait until the converter warps have widened the stage to bf16
             alive = mbar_wait(QUANT ? &conv_full[s] : &full_bar[s], ph, abort_flag, p.err);
@@ -617,9 +644,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
                 }
                 tc5_commit(&s_full[k & 1]);
+                *mma1_issued += 1;
             }
             __syncwarp();
-            s_prev = s;
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
@@ -1018,6 +1045,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         if (sg > 0) alive = alive && mbar_wait(m_full, (uint32_t)((sg - 1) & 1), abort_flag, p.err);
         final_segment(alive && sg > 0, last_it, C::NEPI * 32 + (tid - 64));
     }
+    __syncthreads();  // every role is out of its loop (all waits are bounded)
     if (*abort_flag) {
         // broken protocol (a wait timed out): let issued copies and MMAs land, bounded
         if (tid == 0) {
@@ -1033,6 +1061,12 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             const int j = *mma_issued - 1;
             const uint64_t t0 = global_ns();
             while (!mbar_try_wait(&o_full[j & 1], (j >> 1) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+            }
+        }
+        if (tid == 33 && *mma1_issued > 0) {
+            const int j = *mma1_issued - 1;
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(&s_full[j & 1], (j >> 1) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
             }
         }
     }
