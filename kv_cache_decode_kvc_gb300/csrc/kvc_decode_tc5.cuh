@@ -186,6 +186,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         "l"(policy)
         : "memory");
 }
+// 3-D tensor copy of a whole contiguous tile: the map views the cache as (64 columns, rows, 2
+// column blocks) with byte strides (256, 128), so the box lands as [column block][row][128 B].
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int row, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+        "cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
 // Shared-memory layout of a K / V tile: contiguous caches [column block][128 rows][128 B]
 // (2-D copies); paged pools [8-row group][column block][8 rows][128 B] (4-D copies above).
 template <class C, bool PAGED>
@@ -263,15 +273,19 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
         }
     } else if (part != TILE_Q) {
         const int row0 = (int)(unit * p.T_max + c.t);
-        const CUtensorMap* mk = full ? tmKf : tmK;
-        const CUtensorMap* mv = full ? tmVf : tmV;
+        if (full) {
+            // a whole tile: both column blocks in one 3-D copy per tensor
+            tma_load_3d(ks, tmKf, row0, &full_bar[stage], pol);
+            tma_load_3d(vs, tmVf, row0, &full_bar[stage], pol);
+        } else {
 #pragma unroll
-        for (int hf = 0; hf < C::HALVES; ++hf)
-            for (int bx = 0; bx < nbox; ++bx) {
-                const uint32_t off = hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128;
-                tma_load_2d(ks + off, mk, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
-                tma_load_2d(vs + off, mv, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
-            }
+            for (int hf = 0; hf < C::HALVES; ++hf)
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const uint32_t off = hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128;
+                    tma_load_2d(ks + off, tmK, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+                    tma_load_2d(vs + off, tmV, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+                }
+        }
     }
     if (with_q && part != TILE_KV && lane == 0) {
         asm volatile(

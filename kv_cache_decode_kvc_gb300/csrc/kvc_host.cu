@@ -27,7 +27,8 @@ struct kvc_cache {
     int math;                        // 0 automatic, 1 CUDA cores, 2 warp MMA, 3 tcgen05
     int overlap;                     // 1: early history reads before the preceding grid ends
     bool tc_ok;                      // tensor maps built (bf16 cache, rows < 2^31)
-    std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes);
+    std::vector<CUtensorMap> tmaps;  // per layer: K, V (32-row boxes), K, V (128-row boxes; 3-D
+                                     // maps of whole tiles for a contiguous D = 128 cache);
                                      // paged: K, V, K, V with min(bs, 128)-row boxes
     bool paged;                      // K / V of a layer are pools [num_blocks, H_kv, bs, D]
     bool rolling;                    // T_max = window slots, position p in slot p mod T_max
@@ -78,6 +79,22 @@ bool make_kv_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int D, int 
     const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over a contiguous cache with D = 128 (rows of 256 bytes): dimensions (64 columns, rows,
+// 2 column blocks) with byte strides (256, 128) for dimensions 1..2, so one box of box_rows rows
+// lands in shared memory as [column block][row][128 B] (128-byte swizzle): a whole tile of K or
+// V in one copy.
+bool make_kv3_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+    const cuuint64_t strides[2] = {256, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -408,6 +425,11 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
                      make_paged_tensor_map(&m4[1], vb, rows, box_small) &&
                      make_paged_tensor_map(&m4[2], kb, rows, box_full) &&
                      make_paged_tensor_map(&m4[3], vb, rows, box_full);
+            else if (D == 128)  // whole tiles (tcgen05 kernel only) in one 3-D copy per tensor
+                ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
+                     make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
+                     make_kv3_tensor_map(&m4[2], kb, rows, box_full) &&
+                     make_kv3_tensor_map(&m4[3], vb, rows, box_full);
             else
                 ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
                      make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
