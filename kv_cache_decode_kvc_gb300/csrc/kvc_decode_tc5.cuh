@@ -44,8 +44,7 @@ struct Tc5Cfg {
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
     static constexpr int HALF_BYTES = TT * 128;         // one column block of a K or V tile
     static constexpr int TILE_BYTES = TT * ROWB;
-    static constexpr int QRAW_BYTES = (G * ROWB + 1023) / 1024 * 1024;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + QRAW_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K and V of one tile
     static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128] operand
     static constexpr int OPB_BYTES = HALVES * OPB_BLOCK;
     // P operand of MMA2, P_hi and P_lo side by side as the N2 columns of one MMA:
@@ -169,13 +168,9 @@ __device__ __forceinline__ void tc5_ld(uint32_t taddr, float (&v)[NC]) {
     else tc5_ld16(taddr, v);
 }
 
-// Issues one tile: a full tile is one 128-row box per column block of K and of V (maps tmKf /
-// tmVf); a partial tile uses 32-row boxes (tmK / tmV), rows past the stream's end being loaded
-// and masked; the first tile of a segment also brings q.  `part` splits the issue in two for
-// tiles loaded before the preceding grid has finished: TILE_KV registers the K/V bytes on the
-// stage's barrier without arriving and starts the K/V copies; TILE_Q then adds q (first tile
-// of a segment) and arrives, so the stage cannot complete before q is in.
-enum { TILE_ALL = 0, TILE_KV = 1, TILE_Q = 2 };
+// Issues one tile: a whole tile of a contiguous cache is one 3-D copy per tensor (maps tmKf /
+// tmVf), a paged block one 4-D copy, a partial contiguous tile 32-row boxes per column block
+// (tmK / tmV), rows past the stream's end being loaded and masked.
 // 4-D tensor copy for a paged pool: the map views the pool's rows as (64 columns, 8 rows, 2
 // column blocks, row groups of 8) with strides (2, 256, 128, 2048) bytes, so one box of `groups`
 // row groups arrives as [group][column block][8 rows x 128 B]: 8-row swizzle atoms of the two
@@ -222,34 +217,21 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                                                uint32_t ring, uint64_t* full_bar, int stage,
                                                uint64_t pol, const CUtensorMap* tmK,
                                                const CUtensorMap* tmV, const CUtensorMap* tmKf,
-                                               const CUtensorMap* tmVf, int part, int ent,
-                                               int lane) {
+                                               const CUtensorMap* tmVf, int ent, int lane) {
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
     const uint32_t vs = ks + C::TILE_BYTES;
-    const uint32_t qs = vs + C::TILE_BYTES;
     constexpr bool PAGED = MODE == 1, QUANT = MODE == 3;
     constexpr bool paged = PAGED;
     const bool full = n == TT && !paged;
     const int rows = paged ? p.box_rows : (full ? TT : C::BOX_ROWS);
     const int nbox = full ? 1 : (n + rows - 1) / rows;
-    const bool with_q = c.first();
     // bf16 tiles: 2 x 128-byte column blocks per row; int8 tiles: one row of D bytes
     const uint32_t kv_bytes = (uint32_t)(2 * nbox * rows * (QUANT ? C::D : C::HALVES * 128));
-    const uint32_t q_bytes = with_q ? (uint32_t)(C::G * C::ROWB) : 0u;
-    if (lane == 0) {
-        if (part == TILE_Q) {
-            if (with_q) mbar_arrive_expect_tx(&full_bar[stage], q_bytes);
-            else mbar_arrive(&full_bar[stage]);
-        } else if (part == TILE_KV) {
-            mbar_expect_tx(&full_bar[stage], kv_bytes);
-        } else {
-            mbar_arrive_expect_tx(&full_bar[stage], kv_bytes + q_bytes);
-        }
-    }
+    if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kv_bytes);
     if constexpr (PAGED) {
-        if (part != TILE_Q) {
+        {
             __syncwarp();  // the stage's expected bytes are registered before any copy lands
             // lane bx: box bx = block bx (or the 128-row piece of a larger block)
             if (lane < nbox) {
@@ -266,7 +248,7 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                 tma_load_4d(vs + off, tmV, row >> 3, rows >> 3, &full_bar[stage], pol);
             }
         }
-    } else if (QUANT && part != TILE_Q) {
+    } else if (QUANT) {
         // int8 rows (128 bytes) into the back column block of the tile area, widened in place later
         const int row0 = (int)(unit * p.T_max + c.t);
         const CUtensorMap* mk = full ? tmKf : tmK;
@@ -276,7 +258,7 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
             tma_load_2d(ks + off, mk, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
             tma_load_2d(vs + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
         }
-    } else if (part != TILE_Q) {
+    } else {
         const int row0 = (int)(unit * p.T_max + c.t);
         if (full) {
             // a whole tile: both column blocks in one 3-D copy per tensor
@@ -291,14 +273,6 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                     tma_load_2d(vs + off, tmV, hf * 64, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
                 }
         }
-    }
-    if (with_q && part != TILE_KV && lane == 0) {
-        asm volatile(
-            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
-            "[%1], %2, [%3], %4;" ::"r"(qs),
-            "l"(static_cast<const char*>(p.q) + unit * C::G * C::ROWB), "r"(C::G * C::ROWB),
-            "r"(smem_addr(&full_bar[stage])), "l"(pol)
-            : "memory");
     }
 }
 
@@ -492,9 +466,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         if (early)
             while (pref.valid && npre < NST && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
                 if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
-                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                             TILE_KV, ent, lane);
                 if (lane == 0) issued[npre] += 1;
+                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf, ent,
+                                             lane);
                 pref.advance();
                 ++npre;
             }
@@ -526,14 +500,6 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     if (warp == 0) {
         // ======================================================= producer
         if (PAGED || lane == 0) {
-            // finish the tiles started early: q (segment's first tile) and the arrival
-            TileCursor<TT> c0;
-            c0.init(prefix, B, H_kv, r0, r1);
-            for (int i = 0; i < npre; ++i) {
-                issue_tile_tc5<C, TT, MODE>(p, c0, ring_s, full_bar, i, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                             TILE_Q, ent, lane);
-                c0.advance();
-            }
             if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
             // a tile that holds a stream's new token waits for the fused append's writes (lane 0
             // waits; the warp follows its verdict: paged, every lane issues a block)
@@ -545,9 +511,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 return ok;
             };
             auto issue_next = [&](int st) {
-                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, st, pol, &tmK, &tmV, &tmKf, &tmVf,
-                                             TILE_ALL, ent, lane);
                 if (lane == 0) issued[st] += 1;
+                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, st, pol, &tmK, &tmV, &tmKf, &tmVf, ent,
+                                             lane);
                 pref.advance();
                 // the next tile's blocks load while lane 0 waits
                 if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
@@ -621,6 +587,31 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                      "r"(C::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        // Each segment's q rows (G rows of D bf16 at row unit * G of q) go into the swizzled
+        // operand from registers, loaded one segment ahead and stored once the previous
+        // segment's last MMA1 has read the operand.
+        TileCursor<TT> cur;
+        cur.init(prefix, B, H_kv, r0, r1);
+        constexpr int QV = G * (D / 8), QPL = (QV + 31) / 32;
+        uint4 qv[QPL];
+        auto q_load = [&](const SegIter& it) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q) + ((size_t)it.b * H_kv + it.h) * QV;
+#pragma unroll
+            for (int i = 0; i < QPL; ++i)
+                if (lane + 32 * i < QV) qv[i] = __ldcg(src + lane + 32 * i);
+        };
+        auto q_store = [&]() {
+#pragma unroll
+            for (int i = 0; i < QPL; ++i) {
+                const int c = lane + 32 * i;
+                if (c < QV) {
+                    const int h = c / (D / 8), cc = c % (D / 8);
+                    *reinterpret_cast<uint4*>(qsw + (cc >> 3) * C::OPB_BLOCK + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) =
+                        qv[i];
+                }
+            }
+        };
+        if (cur.valid) q_load(cur.it);
         tc5_fence_before();
         named_bar_sync(2, 32 + C::NW * 32);
         tc5_fence_after();
@@ -628,8 +619,6 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
         const uint32_t qsw_s = smem_addr(qsw);
         using LY = Tc5Layout<C, PAGED>;
-        TileCursor<TT> cur;
-        cur.init(prefix, B, H_kv, r0, r1);
         int s = 0;
         uint32_t ph = 0;
         bool alive = true;
@@ -642,15 +631,12 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             if (alive && cur.first()) {
                 // the previous MMA1 read q_sw: let it finish before q is replaced
                 if (k > 0) alive = mbar_wait(&s_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err);
-                const unsigned char* qraw = ring + s * C::STAGE_BYTES + 2 * C::TILE_BYTES;
-                for (int c = lane; c < G * (D / 8); c += 32) {
-                    const int h = c / (D / 8), cc = c % (D / 8);
-                    const uint4 v = *reinterpret_cast<const uint4*>(qraw + h * C::ROWB + cc * 16);
-                    *reinterpret_cast<uint4*>(qsw + (cc >> 3) * C::OPB_BLOCK + h * 128 +
-                                              (((cc & 7) ^ (h & 7)) << 4)) = v;
-                }
+                q_store();
                 fence_async_smem();
                 __syncwarp();
+                SegIter nx = cur.it;
+                nx.next();
+                if (nx.valid) q_load(nx);
             }
             if (alive) alive = mbar_wait(&s_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
             if (alive && lane == 0) {
