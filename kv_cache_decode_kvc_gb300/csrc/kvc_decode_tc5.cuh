@@ -66,13 +66,8 @@ struct Tc5Cfg {
     static constexpr int MISC_BYTES = 256;
     static constexpr int ALIGN_PAD = 1024;
     static constexpr int BUDGET = 232448;               // opt-in maximum per CTA (227 KB)
-    static constexpr int FIXED2 = OPB_BYTES + 2 * PBUF + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
-                                  MISC_BYTES + ALIGN_PAD;
-    // One P buffer instead of two where that buys a ring stage (the softmax then folds in O^T of
-    // the previous tile, i.e. waits for its MMA2, before it overwrites the weights)
-    static constexpr bool P1 = (BUDGET - FIXED2 + PBUF) / STAGE_BYTES > (BUDGET - FIXED2) / STAGE_BYTES;
-    static constexpr int NPB = P1 ? 1 : 2;
-    static constexpr int FIXED = FIXED2 - (2 - NPB) * PBUF;
+    static constexpr int FIXED = OPB_BYTES + 2 * PBUF + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
+                                 MISC_BYTES + ALIGN_PAD;
     static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NST = NST_A > 4 ? 4 : NST_A;
     static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     unsigned char* ring = smem;
     unsigned char* qsw = ring + NST * C::STAGE_BYTES;        // q, [N][D] K-major swizzled
     unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][2 blocks][2N rows][128 B]
-    float* merge = reinterpret_cast<float*>(pbuf + C::NPB * C::PBUF);
+    float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
     int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
     float* red = reinterpret_cast<float*>(prefix + MAX_B + 1);  // [4][N]
     float* alpha_s = red + 4 * N;                                  // [2][N]: rescale factor of a tile
@@ -549,7 +544,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                         // written by warp 1's allocation before the weights of tile 0 existed
                         if (k == 0) tmem = *tmem_slot;
                         const uint32_t tO = tmem + (uint32_t)(2 * N + (k & 1) * C::N2);
-                        const uint32_t pb = (uint32_t)((C::P1 ? 0 : (k & 1)) * C::PBUF);
+                        const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
 #pragma unroll
                         for (int kk = 0; kk < TS; ++kk) {
                             const uint32_t voff = (uint32_t)(s2 * C::STAGE_BYTES + kk * 2 * LY::GSTR);
@@ -741,7 +736,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // ======================================================= softmax + accumulate
         // zero the padded q rows and the P rows of padded heads (they stay zero), and write the
         // fused append's new rows; then meet the MMA warp (named barrier 2) for the TMEM base
-        for (int i = tid - 64; i < (C::OPB_BYTES + C::NPB * C::PBUF) / 16; i += C::NW * 32)
+        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += C::NW * 32)
             reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
         if (warp == 2 && fused) {
             SegIter it;
@@ -948,9 +943,6 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 }
                 named_bar_sync(1, NT);  // red is reused; alpha_s is written
             }
-            // one P buffer: O^T of the previous tile first (its MMA2 has then read the weights)
-            if constexpr (C::P1)
-                if (!first) absorb(k - 1, resc_prev, alpha_prev);
             // ---- P(k) = P_hi + P_lo for this thread's token; a score of -inf (masked, or no key
             // seen yet: -inf - -inf) gives weight 0
             float pw[GH];
@@ -963,7 +955,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             }
             if constexpr (C::PMN) {
                 // MN-major: the token's row of 64 columns, 16-byte chunks swizzled by token & 7
-                unsigned char* pr = pbuf + (C::P1 ? 0 : (k & 1)) * C::PBUF + row * 128;
+                unsigned char* pr = pbuf + (k & 1) * C::PBUF + row * 128;
                 const int sw = row & 7;
 #pragma unroll
                 for (int c = 0; c < GH / 8; ++c) {
@@ -984,7 +976,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             } else {
                 // K-major: rows h (hi) and N + h (lo), column = this thread's token (h0 is a
                 // multiple of 8: the swizzle phase is h & 7)
-                unsigned char* pb = pbuf + (C::P1 ? 0 : (k & 1)) * C::PBUF + (row >> 6) * C::PBLOCK + h0 * 128;
+                unsigned char* pb = pbuf + (k & 1) * C::PBUF + (row >> 6) * C::PBLOCK + h0 * 128;
                 const int chunk = (row & 63) >> 3, e = row & 7;
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
@@ -1011,7 +1003,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[k & 1]);
             // ---- fold in O^T of the previous tile of this segment
-            if (!C::P1 && !first) absorb(k - 1, resc_prev, alpha_prev);
+            if (!first) absorb(k - 1, resc_prev, alpha_prev);
             resc_prev = resc;
             if constexpr (!ASH)
 #pragma unroll
