@@ -372,6 +372,25 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
             }
         }
     }
+    if constexpr (NWT == 1) {
+        // one state per head (merge row hg: D outputs, max, denominator): copied or normalised
+        // two elements at a time
+        static_assert(D % 2 == 0, "float2 rows");
+        for (int i2 = tid; i2 < G * D / 2; i2 += NW * 32) {
+            const int hg = (2 * i2) / D, d = 2 * i2 - hg * D;
+            const float* bw = merge + hg * (D + 2);
+            const float2 v = *reinterpret_cast<const float2*>(bw + d);
+            if (whole) {
+                const float den = bw[D + 1];
+                Elem<T>::store(p.out, unit * G * D + 2 * i2, v.x / den);
+                Elem<T>::store(p.out, unit * G * D + 2 * i2 + 1, v.y / den);
+            } else {
+                *reinterpret_cast<float2*>(p.part_o + (size_t)slot * G * D + 2 * i2) = v;
+                if (d == 0)
+                    *reinterpret_cast<float2*>(p.part_ml + ((size_t)slot * G + hg) * 2) = make_float2(bw[D], bw[D + 1]);
+            }
+        }
+    } else
     for (int idx = tid; idx < G * D; idx += NW * 32) {
         const int hg = idx / D, d = idx - hg * D;
         const int s_ = hg / HS, hh = hg - s_ * HS;
