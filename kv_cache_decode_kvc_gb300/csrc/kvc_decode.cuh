@@ -345,10 +345,15 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, size_t uni
     }
 }
 
-template <typename T, int G, int D, int HS, int NWT, int NW, int BAR = 0>
+// `released` is called by every thread once, right after its last read of `merge` (a caller
+// that overlaps the next segment may hand the buffer back there).
+struct NoRelease {
+    __device__ void operator()() const {}
+};
+template <typename T, int G, int D, int HS, int NWT, int NW, int BAR = 0, class Rel = NoRelease>
 __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* merge,
                                                const SegIter& it, size_t unit, int64_t W, int64_t P,
-                                               int* last_flag, int tid) {
+                                               int* last_flag, int tid, Rel released = Rel()) {
     const bool whole = (it.t0 == 0) && (it.t1 == it.L);
     const int64_t us = it.ustart;
     const int64_t cfirst = cta_first_of_stream(us, it.L, W, P, p.bs), clast = cta_of(us + it.L - 1, W, P);
@@ -366,6 +371,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
             group_sync<BAR, NW * 32>();
             if (*last_flag) {
                 merge_partials<T, G, D, NW * 32>(p, unit, cfirst, clast, tid, merge, (int64_t)blockIdx.x);
+                released();
                 if (tid == 0) p.counters[unit] = 0;  // every other arrival is in: ready for next call
                 group_sync<BAR, NW * 32>();
                 return;
@@ -416,6 +422,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
             }
         }
     }
+    released();
     if (!whole && p.combine_mode == 0) {
         __threadfence();
         group_sync<BAR, NW * 32>();  // also: every thread is done reading merge

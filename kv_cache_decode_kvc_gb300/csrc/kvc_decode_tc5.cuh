@@ -726,10 +726,14 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 final_segment(ok, it, et);
                 break;
             }
+            // the merge buffer goes back to the softmax warps as soon as it has been read; the
+            // partial state's fence, arrival count and any merge of the stream follow
             if (ok)
                 finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
-                                                              W, P, last_flag, et);
-            mbar_arrive(m_empty);
+                                                              W, P, last_flag, et,
+                                                              [&]() { mbar_arrive(m_empty); });
+            else
+                mbar_arrive(m_empty);
             it = nx;
         }
     } else {
