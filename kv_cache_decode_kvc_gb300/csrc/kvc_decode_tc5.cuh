@@ -492,6 +492,33 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                                                      last_flag, jt);
     };
 
+    // MMA2(k): O^T[k&1] = V(stage st)^T . (P_hi + P_lo)^T, then its commits (run by one thread:
+    // the producer's, or for a paged pool with m2p = 0 the MMA warp's: a producer warp that
+    // issues one copy per block can be the slower of the two)
+    const bool m2p = !PAGED || p.m2p != 0;
+    constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
+    using LY = Tc5Layout<C, PAGED>;
+    auto issue_mma2 = [&](int k, int st, uint32_t tm) {
+        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
+        // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
+        // leading offset is never stepped over)
+        const uint32_t pbuf_s = smem_addr(pbuf);
+        const uint64_t dP0 = C::PMN ? smem_desc_sw128(pbuf_s, (uint32_t)C::PBUF, 1024u)
+                                    : smem_desc_sw128(pbuf_s, 16u, 1024u);
+        const uint32_t tO = tm + (uint32_t)(2 * N + (k & 1) * C::N2);
+        const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
+#pragma unroll
+        for (int kk = 0; kk < TS; ++kk) {
+            const uint32_t voff = (uint32_t)(st * C::STAGE_BYTES + kk * 2 * LY::GSTR);
+            const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
+                                         : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
+            tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
+        }
+        tc5_commit(&o_full[k & 1]);
+        tc5_commit(&empty_bar[st]);  // K/V of the stage are consumed
+        *mma_issued += 1;
+    };
+
     if (warp == 0) {
         // ======================================================= producer
         if (PAGED || lane == 0) {
@@ -520,53 +547,46 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 if (!ok) break;
                 issue_next(st);
             }
-            // MMA2 of each tile (this thread issues it: MMA1 is warp 1's), then the tile NST ahead
-            // into the stage that MMA2 frees.  Issued here so that MMA1 of the next tile never
-            // queues behind it in one thread (each tcgen05.mma takes ~90 cycles to issue).
-            constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
-            using LY = Tc5Layout<C, PAGED>;
-            const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
-            // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
-            // leading offset is never stepped over)
-            const uint32_t pbuf_s = smem_addr(pbuf);
-            const uint64_t dP0 = C::PMN ? smem_desc_sw128(pbuf_s, (uint32_t)C::PBUF, 1024u)
-                                        : smem_desc_sw128(pbuf_s, 16u, 1024u);
-            TileCursor<TT> mc;
-            mc.init(prefix, B, H_kv, r0, r1);
-            int s2 = 0;
-            for (int k = 0; ok && mc.valid; ++k) {
-                // ---- MMA2(k): O^T[k&1] = V(stage s2)^T . (P_hi + P_lo)^T
-                if (lane == 0) {
-                    ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
-                         mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
-                    if (ok) {
-                        tc5_fence_after();
-                        // written by warp 1's allocation before the weights of tile 0 existed
-                        if (k == 0) tmem = *tmem_slot;
-                        const uint32_t tO = tmem + (uint32_t)(2 * N + (k & 1) * C::N2);
-                        const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
-#pragma unroll
-                        for (int kk = 0; kk < TS; ++kk) {
-                            const uint32_t voff = (uint32_t)(s2 * C::STAGE_BYTES + kk * 2 * LY::GSTR);
-                            const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
-                                                         : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
-                            tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
+            if (m2p) {
+                // MMA2 of each tile (this thread issues it: MMA1 is warp 1's), then the tile NST
+                // ahead into the stage that MMA2 frees.  Issued here so that MMA1 of the next tile
+                // never queues behind it in one thread (each tcgen05.mma takes ~90 cycles to issue).
+                TileCursor<TT> mc;
+                mc.init(prefix, B, H_kv, r0, r1);
+                int s2 = 0;
+                for (int k = 0; ok && mc.valid; ++k) {
+                    if (lane == 0) {
+                        ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
+                             mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+                        if (ok) {
+                            tc5_fence_after();
+                            // written by warp 1's allocation before the weights of tile 0 existed
+                            if (k == 0) tmem = *tmem_slot;
+                            issue_mma2(k, s2, tmem);
                         }
-                        tc5_commit(&o_full[k & 1]);
-                        tc5_commit(&empty_bar[s2]);  // K/V of the stage are consumed
-                        *mma_issued += 1;
                     }
-                }
-                if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                if (ok && pref.valid) {
-                    // tile k + NST goes into stage s2 once MMA2(k) has read it
-                    if (lane == 0) ok = mbar_wait(&empty_bar[s2], (uint32_t)((k / NST) & 1), abort_flag, p.err);
                     if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                    if (ok) ok = append_ready();
-                    if (ok) issue_next(s2);
+                    if (ok && pref.valid) {
+                        // tile k + NST goes into stage s2 once MMA2(k) has read it
+                        if (lane == 0) ok = mbar_wait(&empty_bar[s2], (uint32_t)((k / NST) & 1), abort_flag, p.err);
+                        if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                        if (ok) ok = append_ready();
+                        if (ok) issue_next(s2);
+                    }
+                    mc.advance();
+                    if (++s2 == NST) s2 = 0;
                 }
-                mc.advance();
-                if (++s2 == NST) s2 = 0;
+            } else {
+                // each further tile into the next stage once the MMA warp's MMA2 has read it
+                int s = 0;
+                uint32_t ph = 1u;
+                while (ok && pref.valid) {
+                    if (lane == 0) ok = mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err);
+                    ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                    if (ok) ok = append_ready();
+                    if (ok) issue_next(s);
+                    if (++s == NST) { s = 0; ph ^= 1u; }
+                }
             }
         }
     } else if (warp == 1) {
@@ -619,7 +639,23 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         bool alive = true;
         const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);  // + stage, block, k-step
         const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
-        for (int k = 0; cur.valid && alive; ++k) {
+        int s_prev = 0;
+        for (int k = 0;; ++k) {
+            if (!m2p) {
+                // MMA2 of the previous tile here, first (it frees a ring stage as soon as the
+                // weights are written)
+                if (k > 0 && alive) {
+                    const int j = k - 1;
+                    alive = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err) &&
+                            mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
+                    if (alive && lane == 0) {
+                        tc5_fence_after();
+                        issue_mma2(j, s_prev, tmem);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!cur.valid || !alive) break;
             // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
             // int8 cache: wait until the converter warps have widened the stage to bf16
             alive = mbar_wait(QUANT ? &conv_full[s] : &full_bar[s], ph, abort_flag, p.err);
@@ -647,6 +683,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 *mma1_issued += 1;
             }
             __syncwarp();
+            s_prev = s;
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }

@@ -224,6 +224,10 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
     p.num_blocks = h->num_blocks;
     p.box_rows = h->paged ? (h->bs < kvc::TC_FULL_ROWS ? h->bs : kvc::TC_FULL_ROWS) : 0;
     p.rolling = h->rolling ? 1 : 0;
+    // tcgen05 kernel on a paged pool: which warp issues MMA2.  Measured (8B GQA, per layer): the
+    // producer warp for 32- and 64-token blocks (2-4 copies per tile), the MMA warp for 16-token
+    // blocks (8 copies per tile keep the producer busy) and for blocks of 128 tokens or more.
+    p.m2p = (h->paged && h->bs >= 32 && h->bs < 128) ? 1 : 0;
     p.T_q = T_q;
     if (h->quant) {
         p.Ksc = h->scales + (size_t)(2 * layer) * h->scale_stride;

@@ -90,6 +90,7 @@ struct DecodeParams {
     int num_blocks;       // K / V are pools [num_blocks, H_kv, bs, D]; T_max = max_blocks * bs
     int box_rows;         // tcgen05 path: rows per tensor-copy box of a paged tile (min(bs, 128))
     int rolling;          // 1: rolling cache, T_max = window slots, position p in slot p mod T_max
+    int m2p;              // tcgen05, paged pool: MMA2 issued by the producer warp (else the MMA warp)
     int T_q;              // new tokens per sequence (>= 1); the group's G query rows are
                           // [head][token], token i seeing positions up to lens[b] - T_q + i
     const float* Ksc;     // int8 cache: K / V are codes [B, H_kv, T_max, D] and these the row

@@ -91,7 +91,7 @@ def test_paged_decode_matches_oracle(dtype, D, math, bs, G):
 @pytest.mark.parametrize("math", [3, 1])
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("ctas", [1, 3, 7, 152, 600])
-@pytest.mark.parametrize("bs", [16, 128])
+@pytest.mark.parametrize("bs", [16, 64, 128])
 def test_paged_split_t_any_split_matches(bs, ctas, mode, math):
     case = Case(60, 2, 8, 2, 128, [1500, 0], "bf16")
     max_blocks = -(-1501 // bs)
