@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -184,11 +185,16 @@ def traffic_from_profiles(kernel_src_hash: str, paged: int = 0):
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources with comments and whitespace removed: an edit to a comment does
+    not invalidate a profile, any change to the code does."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_decode_kvc_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments (no '//' in strings)
+        h.update(f.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,8 +5,8 @@
 // Same computation, split-T partition and merging as decode_kernel (kvc_decode.cuh): for every
 // query head j of sequence b, o = softmax_t(q . K_t / sqrt(D)) V over t < lens[b]
 // ("11.7 KV Cache：形状、显存与带宽" §2.2; head map of "第 1 周 · Day 4：KV Cache 与 MQA /
-// GQA" §3.4).  A CTA (producer warp, MMA warp, 4 softmax warps, 2 epilogue warps) consumes
-// 128-token tiles:
+// GQA" §3.4).  A CTA (producer warp, MMA warp, 4 or 8 softmax warps, 2 epilogue warps)
+// consumes 128-token tiles:
 //   MMA1  S^T[128 tok x N]  = K[128 x D] . Q^T[D x N]   A = K tile (K-major), B = q (K-major)
 //   softmax: a thread owns one token (one tensor-memory lane) and all N head columns
 //   MMA2  O^T[D x N]        = V^T[D x 128] . P^T[128 x N]  A = V tile read MN-major, B = P
@@ -15,9 +15,10 @@
 //   tile k+1 overlaps the softmax of tile k.
 // N = the query-head group padded to at least 16 (tcgen05 needs N % 16 == 0 at M = 128); the
 // padded q rows are zero.  P is stored as P_hi + P_lo (two bf16 terms, stacked as 2N operand
-// columns of one MMA2) so the weights keep fp32-level accuracy while V is read once.  Everything the tensor cores read is in the
-// 128-byte-swizzled K-major or MN-major canonical layout: K/V tiles arrive that way from TMA
-// tensor copies (boxes of 64 columns x 32 rows), q and P are written that way by the threads.
+// columns of one MMA2) so the weights keep fp32-level accuracy while V is read once.
+// Everything the tensor cores read is in the 128-byte-swizzled K-major or MN-major canonical
+// layout: K/V tiles arrive that way from TMA tensor copies, q and P are written that way by the
+// threads.
 // HBM traffic is unchanged: every K/V byte once per step, shared by the whole group.
 #pragma once
 
@@ -307,10 +308,12 @@ __device__ __forceinline__ bool group_any(bool pred) {
     return r != 0;
 }
 
-// Warp roles: warp 0 issues the tensor copies (producer), warp 1 issues the MMAs, warps 2-5 run
-// the softmax, write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane),
-// warps 6-7 finish segments (output or partial state, and the merge of a stream whose last
-// segment this CTA completes) while the next segment streams.
+// Warp roles: warp 0 issues the tensor copies (producer) and MMA2 (for a paged pool with
+// m2p = 0, warp 1 does), warp 1 issues MMA1 and loads q, warps 2 .. 2+NW-1 run the softmax,
+// write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane), the next two
+// warps finish segments (output or partial state, and the merge of a stream whose last segment
+// this CTA completes) while the next segment streams; the CTA's last segment is finished by the
+// epilogue and softmax warps together.
 // Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
 // the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
 // Slot of a stream's new row in the fused step (the row a preceding append may just have
