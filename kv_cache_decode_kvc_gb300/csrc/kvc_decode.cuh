@@ -826,12 +826,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
 // Merges the partial states of streams cut across CTAs (combine_mode 1): one block per
 // (stream, query head of its group).  Recomputes the same partition as the decode kernels.
 // The block's threads form SP segment lanes x D/4 column groups: lane j of a column group
-// sums segments j, j + SP, j + 2 SP, ... of four columns (float4 loads, four segments in
+// sums segments j, j + SP, j + 2 SP, ... of four columns (float4 loads, eight segments in
 // flight), and the SP partial sums meet in shared memory.  Launched as a programmatic
 // dependent of the decode kernel: lens is read before the grid dependency wait (the decode
 // kernel does not write it) when launch overlap is on, the partials after it.
 constexpr int COMBINE_MAX_SEG = 1024;
-constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_THREADS = 512;
 template <typename T>
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodeParams p, int D, int G) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -900,12 +900,12 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (j < SP) {
         int c = j;
-        for (; c + 3 * SP < nseg; c += 4 * SP) {
-            float4 v[4];
+        for (; c + 7 * SP < nseg; c += 8 * SP) {
+            float4 v[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = __ldcg(po + (size_t)(c + i * SP) * st4);
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(po + (size_t)(c + i * SP) * st4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const float w = sw[c + i * SP];
                 acc.x = fmaf(w, v[i].x, acc.x);
                 acc.y = fmaf(w, v[i].y, acc.y);
