@@ -339,10 +339,14 @@ def run_ours(args, w):
                         + 2 * B * Hkv * T_q * (D + 4 if args.int8 else D * s) + 4 * B)  # written, lens
     if args.paged:  # each block-table entry a sequence uses, read once
         alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
-    # average launch duration over the timed region (graph replay, gaps included)
-    region_launch_ms = ms_local / launches_per_step
+    # average decode-launch duration over the timed region (graph replay, gaps included; a layer
+    # whose split streams are merged by a separate combine launch counts both launches)
+    region_launch_ms = ms_local / L
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
-    traffic = None if (args.window or args.tq > 1 or args.int8) else traffic_from_profiles(kernel_source_hash(), args.paged)
+    # the committed summaries are captures of the 8B-GQA workload (plain, or paged): another
+    # workload, layer count or mode has no measured traffic
+    profiled = (w.name == "gqa8b_b24_ragged3000_6000" and not (args.window or args.tq > 1 or args.int8))
+    traffic = traffic_from_profiles(kernel_source_hash(), args.paged) if profiled else None
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
