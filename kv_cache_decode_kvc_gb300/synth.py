@@ -5,11 +5,14 @@ CUDA path), slice by slice, so the generator is counter-based: every element is 
 pure function of (seed, layer, tensor, b, head, t, d).  It is written with torch
 integer ops that give identical results on any device:
 
-* a 32-bit hash of the element's 64-bit counter (the murmur3 finaliser, with every
-  product split into 16-bit halves so no int64 ever overflows);
-* the value is (sum of the hash's four bytes - 510) / 128: an Irwin-Hall(4) draw,
-  symmetric, bell-shaped, mean 0, standard deviation 1.155, support [-3.98, 3.98];
-  every value is a multiple of 1/128 and exact in fp32 (bf16 rounds it to nearest even).
+* a 32-bit hash of the element's 64-bit counter and a second 32-bit value hashed from the
+  first (the murmur3 finaliser, with every product split into 16-bit halves so no int64 ever
+  overflows);
+* their four 16-bit halves u_1..u_4 are summed: an Irwin-Hall(4) draw on a grid of 2^-16,
+  centred and scaled by one IEEE fp32 multiplication to mean 0 and standard deviation 1
+  (support [-3.46, 3.46]), then rounded to the requested dtype (bf16: nearest even).  The
+  bell-shaped unit-variance draw stands in for N(0, 1); the fine grid makes the bf16 values
+  use their whole significand, so products and sums round as they do on real activations.
 
 Lengths and the small worked example use torch's CPU generator (seeded), which is
 device-independent because they are drawn on the host.
@@ -38,14 +41,36 @@ def _fmix32(h: torch.Tensor) -> torch.Tensor:
     return h ^ (h >> 16)
 
 
+_SALT_A = 0x9E3779B9
+_SALT_B = 0x7F4A7C15
+# 1 / sqrt(var(u_1 + u_2 + u_3 + u_4)) for u_i uniform on {0 .. 65535}: var = (65536^2 - 1) / 3
+_UNIT = float(torch.tensor(1.0 / ((65536.0 ** 2 - 1.0) / 3.0) ** 0.5, dtype=torch.float32))
+
+
+def _fmix32_int(h: int) -> int:
+    """_fmix32 of one Python integer (the seed's part of the hash, computed once)."""
+    h ^= h >> 16
+    h = (h * 0x85EBCA6B) & _M32
+    h ^= h >> 13
+    h = (h * 0xC2B2AE35) & _M32
+    return h ^ (h >> 16)
+
+
+def _hash(lo: torch.Tensor, hi: torch.Tensor, seed: int, salt: int) -> torch.Tensor:
+    s = _fmix32_int((seed ^ salt) & _M32)
+    return _fmix32(lo ^ _fmix32(hi ^ s))
+
+
 def hash_values(counter: torch.Tensor, seed: int) -> torch.Tensor:
     """float32 values (see module doc) for int64 counters >= 0."""
     lo = counter & _M32
     hi = counter >> 32
-    s = seed & _M32
-    h = _fmix32(lo ^ _fmix32(hi ^ _fmix32(torch.full_like(counter, s) ^ 0x9E3779B9)))
-    total = (h & 255) + ((h >> 8) & 255) + ((h >> 16) & 255) + ((h >> 24) & 255)
-    return (total - 510).to(torch.float32) / 128.0
+    a = _hash(lo, hi, seed, _SALT_A)
+    b = _fmix32(a ^ _SALT_B)  # a second 32-bit draw from the first
+    total = (a & 0xFFFF) + (a >> 16) + (b & 0xFFFF) + (b >> 16)
+    # |total - 131070| < 2^24: exact in fp32; one rounded multiplication on any device
+    unit = torch.tensor(_UNIT, dtype=torch.float32, device=counter.device)
+    return (total - 131070).to(torch.float32) * unit
 
 
 def rows(seed: int, layer: int, tensor: str, b: int, head: int, t0: int, t1: int, D: int,

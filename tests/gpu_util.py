@@ -23,6 +23,77 @@ def new_rows(seed, layer, tensor, lens_pre, H, D, B, dtype):
     return torch.stack(rows).contiguous()
 
 
+LOG2E = 1.4426950408889634
+
+# Score patterns of ScoreCase, in log2 units (the kernels' domain) along one direction u of
+# each KV head: tau(t) for token t.
+PATTERNS = {
+    "rising": lambda t: 0.05 * t,                       # the maximum moves up every ~160 tokens
+    "falling": lambda t: 60.0 - 0.05 * t,               # the maximum first, later scores >= 30 below
+    "sawtooth": lambda t: 12.0 * ((t // 97) % 5),       # jumps of 12 > the lazy threshold, mid-tile
+}
+
+
+class ScoreCase:
+    """One layer of inputs drawn with torch's CPU generator (fp32 randn, rounded to the cache
+    dtype: bf16 round-to-nearest-even), shaped so the online softmax meets what it must handle:
+      - "randn": q, K, V ~ N(0, 1);
+      - "peaked": q ~ 16 N(0, 1), K, V ~ N(0, 1) (scores of standard deviation ~23 in log2 units);
+      - a PATTERNS key: k_t = tau(t) ln2 sqrt(D) u + N(0, 1) and q_j = alpha_j u + 0.3 N(0, 1)
+        for a unit vector u per KV head, so query head j sees scores ~ alpha_j tau(t) + noise;
+        alpha_j runs from -1.5 to 1.5 over the group (rising and falling histories at once;
+        1 for a group of one).
+    Same attributes as Case (history of lens_pre[b] tokens, the new token at t = lens_pre[b]),
+    with T_q new tokens per sequence when T_q > 1 (q [B, H_q, T_q, D], k_new [B, H_kv, T_q, D])."""
+
+    def __init__(self, kind, seed, B, H_q, H_kv, D, lens_pre, dtype="bf16", T_q=1):
+        self.B, self.H_q, self.H_kv, self.D, self.T_q, self.layer = B, H_q, H_kv, D, T_q, 0
+        self.dtype = DT[dtype]
+        self.lens_pre = torch.as_tensor(lens_pre, dtype=torch.int32)
+        self.lens = self.lens_pre + T_q
+        G = H_q // H_kv
+        T_all = int(self.lens.max())
+        g = torch.Generator().manual_seed(seed)
+        nk = torch.randn(B, H_kv, T_all, D, generator=g)
+        V = torch.randn(B, H_kv, T_all, D, generator=g)
+        nq = torch.randn(B, H_q, T_q, D, generator=g)
+        if kind == "randn":
+            K, q = nk, nq
+        elif kind == "peaked":
+            K, q = nk, 16.0 * nq
+        else:
+            u = torch.randn(B, H_kv, 1, D, generator=g)
+            u = u / u.norm(dim=-1, keepdim=True)
+            t = torch.arange(T_all, dtype=torch.float64).view(1, 1, -1, 1)
+            tau = PATTERNS[kind](t).to(torch.float32)
+            K = tau * (np.log(2.0) * np.sqrt(D)) * u + nk
+            alpha = torch.linspace(-1.5, 1.5, G) if G > 1 else torch.ones(1)
+            qd = (alpha.view(1, 1, G, 1, 1) * u.view(B, H_kv, 1, 1, D)).reshape(B, H_q, 1, D)
+            q = qd + 0.3 * nq
+        K, V, q = K.to(self.dtype), V.to(self.dtype), q.to(self.dtype)
+        T_in = max(1, int(self.lens_pre.max()))
+        self.K = K[:, :, :T_in].contiguous()
+        self.V = V[:, :, :T_in].contiguous()
+        lp = [int(x) for x in self.lens_pre]
+        kn = torch.stack([K[b, :, lp[b]: lp[b] + T_q] for b in range(B)])
+        vn = torch.stack([V[b, :, lp[b]: lp[b] + T_q] for b in range(B)])
+        self.k_new = (kn[:, :, 0] if T_q == 1 else kn).contiguous()
+        self.v_new = (vn[:, :, 0] if T_q == 1 else vn).contiguous()
+        self.q = (q[:, :, 0] if T_q == 1 else q).contiguous()
+
+    oracle_cache = None  # set below (same as Case)
+
+    def to_device(self, dev="cuda"):
+        return {k: getattr(self, k).to(dev) for k in ("K", "V", "q", "k_new", "v_new", "lens_pre", "lens")}
+
+
+class Ref(np.ndarray):
+    """An oracle output with `abs_att`, the same attention applied to |V| (None once sliced)."""
+
+    def __array_finalize__(self, obj):
+        self.abs_att = None
+
+
 class Case:
     """One layer's worth of seeded inputs: history of lens_pre[b] tokens, the new token, q."""
 
@@ -47,8 +118,13 @@ class Case:
         return Kc, Vc
 
     def oracle_out(self, T_max):
+        """The oracle's output, carrying (for check_close) the same attention applied to |V|."""
         Kc, Vc = self.oracle_cache(T_max)
-        return oracle.decode_attn(host_bits(self.q), Kc, Vc, self.lens.numpy())
+        ref = oracle.decode_attn(host_bits(self.q), Kc, Vc, self.lens.numpy()).view(Ref)
+        if self.dtype == torch.bfloat16:
+            ref.abs_att = oracle.decode_attn(host_bits(self.q), Kc, np.ascontiguousarray(abs_bits(Vc)),
+                                             self.lens.numpy())
+        return ref
 
     def to_device(self, dev="cuda"):
         return {k: getattr(self, k).to(dev) for k in ("K", "V", "q", "k_new", "v_new", "lens_pre", "lens")}
@@ -66,6 +142,9 @@ def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what="", tight=True, 
     tensor-core path rounds each softmax weight to two bf16 terms (16 significant bits, relative
     error <= 2^-16); `abs_att` (the same attention applied to |V|, i.e. sum_t p_t |v_t| / sum_t p_t)
     adds that bound, 2^-16 abs_att, to the one-ulp bar where outputs cancel."""
+    if abs_att is None:
+        abs_att = getattr(ref, "abs_att", None)
+    ref = np.asarray(ref)
     g = got.float().cpu().numpy().astype(np.float64)
     err = np.abs(g - ref)
     mx = float(err.max()) if err.size else 0.0
@@ -84,3 +163,13 @@ def check_close(got: torch.Tensor, ref: np.ndarray, dtype, what="", tight=True, 
     bad = np.argwhere(err > tight)
     assert bad.size == 0, f"{what}: {len(bad)} outputs beyond one bf16 ulp, first {bad[:3].tolist()}"
     return mx, rel
+
+
+ScoreCase.oracle_cache = Case.oracle_cache
+ScoreCase.oracle_out = Case.oracle_out
+
+
+def abs_att_of(case, Kc, Vc):
+    """The oracle's attention applied to |V| (sum_t p_t |v_t| / sum_t p_t): bounds the error the
+    kernels' weight rounding can add to an output that cancels (see check_close)."""
+    return oracle.decode_attn(host_bits(case.q), Kc, np.ascontiguousarray(abs_bits(Vc)), case.lens.numpy())
