@@ -26,13 +26,12 @@ using ElemT = float;
 template <int G>
 static int launch_g(const DecodeParams& p, cudaStream_t s, int* smem_out) {
     using C = DecodeCfg<ElemT, KVC_INST_D, G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<ElemT, KVC_INST_D, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return (int)e;
-        attr_set = true;
-    }
+    static PerDeviceOnce smem_attr;
+    const int ea = smem_attr.run([] {
+        return (int)cudaFuncSetAttribute(decode_kernel<ElemT, KVC_INST_D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != 0) return ea;
     if (smem_out) *smem_out = C::SMEM;
     decode_kernel<ElemT, KVC_INST_D, G><<<p.P, C::NTHREADS, C::SMEM, s>>>(p);
     return (int)cudaGetLastError();

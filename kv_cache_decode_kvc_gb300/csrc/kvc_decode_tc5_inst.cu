@@ -24,13 +24,12 @@ template <int G>
 static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                         int* smem_out) {
     using C = Tc5Cfg<G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc5_kernel<G, KVC_TC5_MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return (int)e;
-        attr_set = true;
-    }
+    static PerDeviceOnce smem_attr;
+    const int ea = smem_attr.run([] {
+        return (int)cudaFuncSetAttribute(decode_tc5_kernel<G, KVC_TC5_MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != 0) return ea;
     if (smem_out) *smem_out = C::SMEM;
     // programmatic stream serialisation: this grid may be scheduled while the previous kernel on
     // the stream finishes; the kernel's griddepcontrol.wait holds every read of stream data

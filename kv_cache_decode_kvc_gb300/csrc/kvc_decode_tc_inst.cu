@@ -15,13 +15,12 @@ template <int G>
 static int launch_tc_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        cudaStream_t s, int* smem_out) {
     using C = TcCfg<KVC_INST_D, G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<KVC_INST_D, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return (int)e;
-        attr_set = true;
-    }
+    static PerDeviceOnce smem_attr;
+    const int ea = smem_attr.run([] {
+        return (int)cudaFuncSetAttribute(decode_tc_kernel<KVC_INST_D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != 0) return ea;
     if (smem_out) *smem_out = C::SMEM;
     decode_tc_kernel<KVC_INST_D, G><<<p.P, C::NTHREADS, C::SMEM, s>>>(p, tmK, tmV);
     return (int)cudaGetLastError();

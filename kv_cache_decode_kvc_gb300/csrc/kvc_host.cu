@@ -53,21 +53,24 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The driver's tensor-map encoder, fetched through the runtime (no link-time libcuda).
+// The driver's tensor-map encoder, fetched through the runtime (no link-time libcuda); looked up
+// once per process (thread-safe static initialisation).
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
+            return reinterpret_cast<EncodeTiledFn>(f);
+        return nullptr;
+    }();
     return fn;
 }
+
+}  // namespace
+
+namespace kvc {
 
 // 2-D map over one layer's K or V cache: columns D (contiguous), rows B*H_kv*T_max; boxes of 64
 // columns (128 bytes) x box_rows rows, 128-byte swizzle, zero fill past the last row.
@@ -98,6 +101,10 @@ bool make_kv3_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_ro
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace kvc
+
+namespace {
 
 // 4-D map over a paged pool with D = 128 (rows of 256 bytes): dimensions (64 columns, 8 rows,
 // 2 column blocks, rows / 8 groups) with byte strides (256, 128, 2048) for dimensions 1..3, so
@@ -430,15 +437,15 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
                      make_paged_tensor_map(&m4[2], kb, rows, box_full) &&
                      make_paged_tensor_map(&m4[3], vb, rows, box_full);
             else if (D == 128)  // whole tiles (tcgen05 kernel only) in one 3-D copy per tensor
-                ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
-                     make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
-                     make_kv3_tensor_map(&m4[2], kb, rows, box_full) &&
-                     make_kv3_tensor_map(&m4[3], vb, rows, box_full);
+                ok = kvc::make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
+                     kvc::make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
+                     kvc::make_kv3_tensor_map(&m4[2], kb, rows, box_full) &&
+                     kvc::make_kv3_tensor_map(&m4[3], vb, rows, box_full);
             else
-                ok = make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
-                     make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
-                     make_kv_tensor_map(&m4[2], kb, rows, D, box_full) &&
-                     make_kv_tensor_map(&m4[3], vb, rows, D, box_full);
+                ok = kvc::make_kv_tensor_map(&m4[0], kb, rows, D, box_small) &&
+                     kvc::make_kv_tensor_map(&m4[1], vb, rows, D, box_small) &&
+                     kvc::make_kv_tensor_map(&m4[2], kb, rows, D, box_full) &&
+                     kvc::make_kv_tensor_map(&m4[3], vb, rows, D, box_full);
         }
         h->tc_ok = ok;
         if (!ok) h->tmaps.clear();

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kvc {
 
 constexpr uint32_t DEV_BAD_LENS = 1u;      // mirrors KVC_DEV_BAD_LENS
@@ -148,7 +150,31 @@ int launch_decode_tc5q_d128(int G, const DecodeParams& p, const CUtensorMap* map
                             int* smem_out);
 constexpr int TC_BOX_ROWS = 32;
 constexpr int TC_FULL_ROWS = 128;
+// Tensor maps of a bf16 cache (host; encoded by the driver, no allocation).  2-D: columns D,
+// rows B*H_kv*T_max, boxes of 64 columns x box_rows, 128-byte swizzle.  3-D (D = 128): a whole
+// box_rows-row tile of both 64-column blocks in one copy.  False if the encoder is unavailable
+// or base is not 16-byte aligned.
+bool make_kv_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int D, int box_rows);
+bool make_kv3_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows);
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s);
+
+// cudaFuncSetAttribute applies to the current device only: a launcher sets a kernel's
+// attributes once per device (devices 0..63; beyond that, on every launch).  Setting them twice
+// from racing threads is harmless.
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};
+    template <class F>
+    int run(F&& set) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+        if (dev < 0 || dev >= 64) return set();
+        const uint64_t bit = 1ull << dev;
+        if (done.load(std::memory_order_acquire) & bit) return 0;
+        const int e = set();
+        if (e == 0) done.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+};
 int launch_append(const CopyParams& p, cudaStream_t s);
 int launch_prefill(const CopyParams& p, cudaStream_t s);
 
@@ -232,17 +258,18 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete, for at most WAIT_LIMIT_NS.  On
-// timeout (or once another thread of the CTA has timed out) it returns false, having set the
-// CTA's abort flag and the device error word; callers then skip work but keep the protocol.
+// Wait for the phase with the given parity to complete, for at most limit_ns (the kernels use
+// WAIT_LIMIT_NS).  On timeout (or once another thread of the CTA has timed out) it returns
+// false, having set the CTA's abort flag and the device error word; callers then skip work but
+// keep the protocol.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err) {
+                                          uint32_t* err, uint64_t limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
         if (*abort_flag) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(err, DEV_WAIT_TIMEOUT);
             return false;

@@ -9,6 +9,12 @@
 // states of split sequences, their arrival counters and an error word) lives in a file-scope
 // __device__ array of fixed size in this translation unit.
 //
+// The kernel is the one kvc_decode_attn picks by default for the same cache: the tcgen05 kernel
+// for a bf16 cache with D = 128 (its tensor maps are host structures, encoded per call and
+// passed by value), the CUDA-core kernel otherwise; same partition (one CTA per SM) and the same
+// merge rule, so the results agree with kvc_decode_attn's within rounding (the order in which a
+// split stream's partial states are folded can differ between runs).
+//
 // The array is SCRATCH_BYTES per device that loads the library, held until the process
 // exits.  Its device address is looked up once per device (cudaGetSymbolAddress) on the first
 // call made with that device current; that first call should therefore come before any stream
@@ -58,6 +64,11 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
                                        int D, int T_max, int dtype, const void* q, void* out,
                                        const int32_t* lens, uint32_t* err, void* stream) {
     if (!K || !V || !q || !out || !lens) return KVC_EINVAL;
+    // 16-byte vectors and bulk copies read K, V, q and write out; lens and err are 32-bit words
+    auto misaligned = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+    if (misaligned(K, 16) || misaligned(V, 16) || misaligned(q, 16) || misaligned(out, 16) ||
+        misaligned(lens, 4) || (err && misaligned(err, 4)))
+        return KVC_EINVAL;
     if (B < 1 || H_q < 1 || H_kv < 1 || T_max < 1 || H_q % H_kv != 0) return KVC_EINVAL;
     if (dtype != KVC_BF16 && dtype != KVC_F32) return KVC_EINVAL;
     if (B > kvc::MAX_B) return KVC_ERANGE;
@@ -83,6 +94,17 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     const size_t off_o = round_up(off_ml + slots * G * 2 * 4, 256);
     const size_t need = off_o + slots * G * (size_t)D * 4;
     if (need > SCRATCH_BYTES) return KVC_ERANGE;
+
+    // the tcgen05 kernel when kvc_decode_attn would take it: bf16, D = 128, rows addressable by
+    // the tensor maps' 32-bit coordinates
+    const uint64_t rows = (uint64_t)B * H_kv * (uint64_t)T_max;
+    CUtensorMap maps[4];
+    bool tc5 = dtype == KVC_BF16 && D == 128 && rows < (1ull << 31);
+    if (tc5)
+        tc5 = kvc::make_kv_tensor_map(&maps[0], const_cast<void*>(K), rows, D, kvc::TC_BOX_ROWS) &&
+              kvc::make_kv_tensor_map(&maps[1], const_cast<void*>(V), rows, D, kvc::TC_BOX_ROWS) &&
+              kvc::make_kv3_tensor_map(&maps[2], const_cast<void*>(K), rows, kvc::TC_FULL_ROWS) &&
+              kvc::make_kv3_tensor_map(&maps[3], const_cast<void*>(V), rows, kvc::TC_FULL_ROWS);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the counters must start at zero; the error word too when the kernel writes it here
@@ -112,7 +134,9 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
 
     int smem = 0, e;
-    if (dtype == KVC_BF16) {
+    if (tc5) {
+        e = kvc::launch_decode_tc5_d128(G, p, maps, s, &smem);
+    } else if (dtype == KVC_BF16) {
         switch (D) {
             case 64: e = kvc::launch_decode_bf16_d64(G, p, s, &smem); break;
             case 128: e = kvc::launch_decode_bf16_d128(G, p, s, &smem); break;
