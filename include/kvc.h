@@ -263,14 +263,20 @@ int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, i
                          int min_tokens, int b, int h, int* first, int* last);
 
 /* Decode attention for callers that cannot allocate device memory.  The pages have no
- * counterpart: this is an interface variant of kvc_decode_attn, same kernel, same results.
+ * counterpart: this is an interface variant of kvc_decode_attn.  It runs the kernel that
+ * kvc_decode_attn picks by default for the same cache (tcgen05 for a bf16 cache with D = 128,
+ * the CUDA-core kernel otherwise), with the same split over one CTA per SM and the same merge
+ * rule, so its results agree with kvc_decode_attn's within rounding (not bit for bit: the order
+ * in which a split sequence's partial states are folded may differ from run to run).
  * Who needs it: code that must not call cudaMalloc (a plugin whose host engine owns all device
  * memory, a latency-critical loop where the allocator's device synchronisation is forbidden, a
  * runtime with a fixed memory plan) and that keeps its K/V cache in memory it owns.
  * Arguments: K, V are one layer's cache [B, H_kv, T_max, D] (device, dtype KVC_BF16 or
  * KVC_F32, the same layout and limits as kvc_create); q, out [B, H_q, D] and lens [B] as in
  * kvc_decode_attn; err is an optional device uint32 that receives the KVC_DEV_* bits (NULL:
- * not reported); stream as elsewhere.
+ * not reported); stream as elsewhere.  K, V, q and out must be 16-byte aligned, lens and err
+ * 4-byte aligned, else KVC_EINVAL before any launch.  err accumulates: bits are ORed in and
+ * never cleared by the library, so zero it before the calls you want to check.
  * Scratch: a fixed 8 MiB __device__ array inside the library (held by every device that loads
  * it, until exit).  Shapes whose split-T scratch would exceed it return KVC_ERANGE before any
  * launch.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
@@ -280,6 +286,18 @@ int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, i
 int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int H_q, int H_kv, int D,
                             int T_max, int dtype, const void* q, void* out, const int32_t* lens,
                             uint32_t* err, void* stream);
+
+/* Self-test of the bounded in-kernel wait.  The pages have no counterpart: every attention
+ * kernel waits on shared-memory barriers, and each wait gives up after a time limit (2 s),
+ * sets KVC_DEV_WAIT_TIMEOUT in the device error word and lets the kernel finish instead of
+ * hanging the GPU.  A correct launch never reaches that limit, so this call makes a wait reach
+ * it on purpose, with no fault: one CTA of 64 threads waits on a barrier phase that nothing
+ * completes, for limit_ns nanoseconds (limit_ns <= 0: the kernels' own 2 s limit; more than
+ * that: KVC_ERANGE).  It ORs KVC_DEV_WAIT_TIMEOUT into *err (device uint32, 4-byte aligned)
+ * and writes info[0] = threads whose wait reported completion (0 when the wait works),
+ * info[1] = nanoseconds thread 0 waited (device int64[2], 8-byte aligned).  Asynchronous on
+ * stream; the context stays usable afterwards. */
+int kvc_selftest_wait_timeout(uint32_t* err, long long* info, long long limit_ns, void* stream);
 
 /* Human-readable name of a status code. */
 const char* kvc_status_str(int status);

@@ -25,7 +25,7 @@ DECODE_INST = [("bf16", 64), ("bf16", 128), ("bf16", 256),
 
 def _units():
     units = [("kvc_host", "kvc_host.cu", []), ("kvc_copy", "kvc_copy.cu", []),
-             ("kvc_noalloc", "kvc_noalloc.cu", [])]
+             ("kvc_noalloc", "kvc_noalloc.cu", []), ("kvc_selftest", "kvc_selftest.cu", [])]
     for d in (64, 128, 256):
         units.append((f"kvc_decode_tc_d{d}", "kvc_decode_tc_inst.cu", [f"-DKVC_INST_D={d}"]))
     units.append(("kvc_decode_tc5_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=0"]))

@@ -67,6 +67,7 @@ def load() -> ctypes.CDLL:
         "kvc_plan_stream_ctas": (I, [P, I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
         "kvc_decode_attn_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P]),
+        "kvc_selftest_wait_timeout": (I, [P, P, ctypes.c_longlong, P]),
         "kvc_create_paged": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I, I, I]),
         "kvc_create_rolling": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
         "kvc_create_quantized": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
@@ -292,6 +293,13 @@ def kvc_decode_attn_noalloc(K, V, B, H_q, H_kv, D, T_max, dtype, q, out, lens, e
     _check(load().kvc_decode_attn_noalloc(_ptr(K), _ptr(V), B, H_q, H_kv, D, T_max, dtype, _ptr(q),
                                           _ptr(out), _ptr(lens), _ptr(err), _stream(stream)),
            "kvc_decode_attn_noalloc")
+
+
+def kvc_selftest_wait_timeout(err, info, limit_ns=0, stream=None) -> None:
+    """One CTA whose in-kernel wait runs out on purpose (see include/kvc.h): err (int32 [1]) gets
+    KVC_DEV_WAIT_TIMEOUT, info (int64 [2]) the completed-wait count and thread 0's wait in ns."""
+    _check(load().kvc_selftest_wait_timeout(_ptr(err), _ptr(info), int(limit_ns), _stream(stream)),
+           "kvc_selftest_wait_timeout")
 
 
 def kvc_plan_cta_of(x, W, P) -> int:

@@ -122,3 +122,20 @@ def test_null_handle_setters_are_rejected(lib):
     assert lib.kvc_set_math(None, 0) == kvc.KVC_EINVAL
     assert lib.kvc_get_math(None) == -1
     assert lib.kvc_set_combine_mode(None, 0) == kvc.KVC_EINVAL
+
+
+@pytest.mark.parametrize("bad", ["K", "V", "q", "out", "lens", "err"])
+def test_noalloc_refuses_misaligned_pointers_before_any_launch(lib, bad):
+    # fake device addresses: every check runs on the host, before the device is touched, so a
+    # misaligned pointer is refused on a machine without a GPU as well
+    ptrs = {"K": 0x10000, "V": 0x20000, "q": 0x30000, "out": 0x40000, "lens": 0x50000, "err": 0x60000}
+    ptrs[bad] += 8 if bad in ("K", "V", "q", "out") else 2
+    st = lib.kvc_decode_attn_noalloc(ptrs["K"], ptrs["V"], 2, 8, 2, 128, 64, kvc.KVC_BF16, ptrs["q"],
+                                     ptrs["out"], ptrs["lens"], ptrs["err"], None)
+    assert st == kvc.KVC_EINVAL
+
+
+def test_wait_selftest_rejects_bad_arguments_on_the_host(lib):
+    assert lib.kvc_selftest_wait_timeout(None, 0x1000, 1000, None) == kvc.KVC_EINVAL
+    assert lib.kvc_selftest_wait_timeout(0x1000, 0x2004, 1000, None) == kvc.KVC_EINVAL  # info misaligned
+    assert lib.kvc_selftest_wait_timeout(0x1000, 0x2000, 3_000_000_000, None) == kvc.KVC_ERANGE
