@@ -117,6 +117,8 @@ def oracle_sample(w, budget_s: float, threads: int, max_layers: int | None = Non
     from kv_cache_decode_kvc_gb300 import synth
 
     used = oracle.set_threads(threads)
+    # the generator gives identical values on any device; the GPU makes them faster
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     lens = w.lens()
     lens_np = lens.numpy()
     done, secs, nbytes = 0, 0.0, 0
@@ -124,9 +126,11 @@ def oracle_sample(w, budget_s: float, threads: int, max_layers: int | None = Non
     for layer in range(layers):
         # the post-append cache of this layer is the generator's rows [0, L_b) of each stream
         T_max = int(lens.max())
-        K = synth.bf16_bits(synth.block(w.seed, layer, "K", 0, w.B, w.H_kv, 0, T_max, w.D, w.B))
-        V = synth.bf16_bits(synth.block(w.seed, layer, "V", 0, w.B, w.H_kv, 0, T_max, w.D, w.B))
-        q = synth.bf16_bits(synth.queries(w.seed, layer, w.B, w.H_q, w.D))
+        K = synth.bf16_bits(synth.block(w.seed, layer, "K", 0, w.B, w.H_kv, 0, T_max, w.D, w.B,
+                                        device=gen_dev).cpu())
+        V = synth.bf16_bits(synth.block(w.seed, layer, "V", 0, w.B, w.H_kv, 0, T_max, w.D, w.B,
+                                        device=gen_dev).cpu())
+        q = synth.bf16_bits(synth.queries(w.seed, layer, w.B, w.H_q, w.D, device=gen_dev).cpu())
         t0 = time.perf_counter()
         oracle.decode_attn(q, K, V, lens_np)
         secs += time.perf_counter() - t0
@@ -289,6 +293,18 @@ def run_ours(args, w):
 
     run = graph.replay if graph is not None else step
 
+    # ---- the same steps launched eagerly (no graph), for the eager step time beside the graph's
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ee0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ee1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = ee0.elapsed_time(ee1) / args.steps
+
     # ---- timed region: K steps, barrier + synchronize on both sides, CUDA events on `stream`
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     clocks = ClockSampler(vis.split(",")[local] if vis else str(local))
@@ -352,27 +368,31 @@ def run_ours(args, w):
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
                    3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'int8' if args.int8 else 'rolling' if args.window else 'contiguous'}> (tcgen05)"}[path]
 
-    # ---- end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
-    h_q = [i[0].cpu().pin_memory() for i in ins]
-    h_kn = [i[1].cpu().pin_memory() for i in ins]
-    h_vn = [i[2].cpu().pin_memory() for i in ins]
-    h_lens = lens_d.cpu().pin_memory()
-    h_out = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for o in outs]
-    d_q = [torch.empty_like(i[0]) for i in ins]
-    d_kn = [torch.empty_like(i[1]) for i in ins]
-    d_vn = [torch.empty_like(i[2]) for i in ins]
-    d_lens = torch.empty_like(lens_d)
-    h2d = sum(t.numel() * t.element_size() for t in h_q + h_kn + h_vn) + h_lens.numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # ---- end to end through the C ABI with host buffers: each step copies its inputs (lens and
+    # every layer's q, k_new, v_new, packed in one pinned buffer) host -> device in one copy,
+    # runs the layers, and copies every layer's output device -> host in one copy
+    parts = [lens_d] + [t for i in ins for t in i]
+    nbytes = [t.numel() * t.element_size() for t in parts]
+    offs, o = [], 0
+    for nb in nbytes:
+        offs.append(o)
+        o += -(-nb // 256) * 256  # 256-byte aligned pieces
+    h_in = torch.empty(o, dtype=torch.uint8).pin_memory()
+    for t, off, nb in zip(parts, offs, nbytes):
+        h_in[off: off + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    d_in = torch.empty(o, dtype=torch.uint8, device=dev)
+    views = [d_in[off: off + nb].view(t.dtype).view(t.shape) for t, off, nb in zip(parts, offs, nbytes)]
+    d_lens, d_ins = views[0], [views[1 + 3 * l: 4 + 3 * l] for l in range(L)]
+    d_out = torch.empty((L,) + tuple(outs[0].shape), dtype=torch.bfloat16, device=dev)
+    h_out = torch.empty(d_out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d, d2h = o, h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        d_lens.copy_(h_lens, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         for layer in range(L):
-            d_q[layer].copy_(h_q[layer], non_blocking=True)
-            d_kn[layer].copy_(h_kn[layer], non_blocking=True)
-            d_vn[layer].copy_(h_vn[layer], non_blocking=True)
-            decode(layer, d_q[layer], d_kn[layer], d_vn[layer], outs[layer], d_lens)
-            h_out[layer].copy_(outs[layer], non_blocking=True)
+            q, kn, vn = d_ins[layer]
+            decode(layer, q, kn, vn, d_out[layer], d_lens)
+        h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -431,9 +451,12 @@ def run_ours(args, w):
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                          "kernel": kernel_name, "launch_us": round(region_launch_ms * 1e3, 2),
                          "launch_us_eager_events": round(launch_ms * 1e3, 2),
+                         "eager_ms_per_step": round(eager_ms, 4),
                          "alg_bytes_per_launch": alg_bytes_launch},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                    "copies_per_step": {"h2d": 1, "d2h": 1}, "launch": "eager"},
+            "eager_ms_per_step": round(eager_ms, 4),
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clock_info,
             "cpu_baseline": cpu,
