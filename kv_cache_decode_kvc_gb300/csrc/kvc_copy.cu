@@ -136,10 +136,15 @@ int launch_prefill(const CopyParams& p, cudaStream_t s) {
     return (int)cudaGetLastError();
 }
 
-// A programmatic dependent launch of the combine kernel behind the decode kernel.
+// A programmatic dependent launch of the combine kernel behind the decode kernel.  Column
+// slices per (stream, head): doubled while the grid is smaller than the decode grid (p.P, one
+// CTA per SM by default), up to 8 and while each slice keeps at least one float4 column.
 int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t s) {
+    const long long ug = (long long)p.B * p.H_kv * G;
+    int DS = 1;
+    while (DS < 8 && 2 * DS <= D / 4 && ug * DS < p.P) DS *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.B * p.H_kv * G));
+    cfg.gridDim = dim3((unsigned)(ug * DS));
     cfg.blockDim = dim3(COMBINE_THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -148,8 +153,8 @@ int launch_combine(int dtype, int D, int G, const DecodeParams& p, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p, D, G)
-                                     : cudaLaunchKernelEx(&cfg, combine_kernel<float>, p, D, G);
+    const cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, p, D, G, DS)
+                                     : cudaLaunchKernelEx(&cfg, combine_kernel<float>, p, D, G, DS);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

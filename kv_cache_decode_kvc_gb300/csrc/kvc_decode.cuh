@@ -823,21 +823,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
     }
 }
 
-// Merges the partial states of streams cut across CTAs (combine_mode 1): one block per
-// (stream, query head of its group).  Recomputes the same partition as the decode kernels.
-// The block's threads form SP segment lanes x D/4 column groups: lane j of a column group
-// sums segments j, j + SP, j + 2 SP, ... of four columns (float4 loads, eight segments in
-// flight), and the SP partial sums meet in shared memory.  Launched as a programmatic
-// dependent of the decode kernel: lens is read before the grid dependency wait (the decode
-// kernel does not write it) when launch overlap is on, the partials after it.
+// Merges the partial states of streams cut across CTAs (combine_mode 1).  Block (u, hg, ds) of
+// the U * G * DS grid merges columns [ds D / DS, (ds + 1) D / DS) of query head hg of stream u:
+// DS > 1 spreads a few long streams (e.g. one sequence of 131k tokens, 153 segments) over many
+// SMs.  The block recomputes the decode kernels' partition.  Its threads form SL segment lanes
+// x C4 float4 column groups; lane j sums segments j, j + SL, j + 2 SL, ... with up to eight
+// loads in flight, the first eight issued before the weights are known (the weights need the
+// segments' maxima first), and the SL partial sums meet in shared memory.  Launched as a
+// programmatic dependent of the decode kernel: lens is read before the grid dependency wait
+// (the decode kernel does not write it) when launch overlap is on, the partials after it.
 constexpr int COMBINE_MAX_SEG = 1024;
-constexpr int COMBINE_THREADS = 512;
+constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_CHUNK = 8;  // segment loads in flight per thread
 template <typename T>
-__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodeParams p, int D, int G) {
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodeParams p, int D, int G, int DS) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int NWARP = COMBINE_THREADS / 32;
-    const int u = blockIdx.x / G, hg = blockIdx.x % G;
+    const int ds = blockIdx.x % DS, ug = blockIdx.x / DS;
+    const int u = ug / G, hg = ug % G;
     const int b = u / p.H_kv, h = u % p.H_kv;
     __shared__ int64_t sh_sum[2];
     __shared__ float sw[COMBINE_MAX_SEG];
@@ -867,7 +871,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs
     const size_t base = (size_t)(cfirst + u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // weights w_c = 2^(m_c - M) / sum_c 2^(m_c - M) l_c, formed once in shared memory
+    // this block's columns: C4 float4 groups (D / 4 divisible by DS, C4 divides the block)
+    const int D4 = D >> 2, C4 = D4 / DS, SL = COMBINE_THREADS / C4;
+    const int c4 = threadIdx.x % C4, j = threadIdx.x / C4;
+    const size_t st4 = (size_t)G * D4;  // float4s between consecutive segments
+    const float4* po = reinterpret_cast<const float4*>(p.part_o) + base * st4 + (size_t)hg * D4 + ds * C4 + c4;
+    float4 v[COMBINE_CHUNK];
+#pragma unroll
+    for (int i = 0; i < COMBINE_CHUNK; ++i) {
+        const int c = j + i * SL;
+        v[i] = c < nseg ? __ldcg(po + (size_t)c * st4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // weights w_c = 2^(m_c - M), M = max_c m_c, and the denominator sum_c w_c l_c
     float mx = -INFINITY;
     for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
         const float mc = p.part_ml[((base + c) * G + hg) * 2];
@@ -888,51 +903,40 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     }
     for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
     if (lane == 0) sred[warp] = den;
-    __syncthreads();
+    __syncthreads();  // also: every weight in sw is written
     float dsum = 0.f;
     for (int w = 0; w < NWARP; ++w) dsum += sred[w];
     const float inv = 1.f / dsum;
-    // D % 4 == 0 and D <= 4 * COMBINE_THREADS for every instantiated head dimension
-    const int D4 = D >> 2, SP = COMBINE_THREADS / D4;
-    const int d4 = threadIdx.x % D4, j = threadIdx.x / D4;
-    const size_t st4 = (size_t)G * D4;  // float4s between consecutive segments
-    const float4* po = reinterpret_cast<const float4*>(p.part_o) + base * st4 + (size_t)hg * D4 + d4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < SP) {
-        int c = j;
-        for (; c + 7 * SP < nseg; c += 8 * SP) {
-            float4 v[8];
+    for (int c0 = 0;; c0 += COMBINE_CHUNK * SL) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(po + (size_t)(c + i * SP) * st4);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float w = sw[c + i * SP];
-                acc.x = fmaf(w, v[i].x, acc.x);
-                acc.y = fmaf(w, v[i].y, acc.y);
-                acc.z = fmaf(w, v[i].z, acc.z);
-                acc.w = fmaf(w, v[i].w, acc.w);
-            }
+        for (int i = 0; i < COMBINE_CHUNK; ++i) {
+            const int c = c0 + j + i * SL;
+            const float w = c < nseg ? sw[c] : 0.f;
+            acc.x = fmaf(w, v[i].x, acc.x);
+            acc.y = fmaf(w, v[i].y, acc.y);
+            acc.z = fmaf(w, v[i].z, acc.z);
+            acc.w = fmaf(w, v[i].w, acc.w);
         }
-        for (; c < nseg; c += SP) {
-            const float4 v = __ldcg(po + (size_t)c * st4);
-            const float w = sw[c];
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+        const int n0 = c0 + COMBINE_CHUNK * SL;
+        if (n0 >= nseg) break;
+#pragma unroll
+        for (int i = 0; i < COMBINE_CHUNK; ++i) {
+            const int c = n0 + j + i * SL;
+            v[i] = c < nseg ? __ldcg(po + (size_t)c * st4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     spart[threadIdx.x] = acc;
     __syncthreads();
     if (j == 0) {
-        for (int jj = 1; jj < SP; ++jj) {
-            const float4 v = spart[jj * D4 + d4];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        for (int jj = 1; jj < SL; ++jj) {
+            const float4 w4 = spart[jj * C4 + c4];
+            acc.x += w4.x;
+            acc.y += w4.y;
+            acc.z += w4.z;
+            acc.w += w4.w;
         }
-        const size_t o = ((size_t)u * G + hg) * D + (size_t)d4 * 4;
+        const size_t o = ((size_t)u * G + hg) * D + (size_t)(ds * C4 + c4) * 4;
         Elem<T>::store(p.out, o, acc.x * inv);
         Elem<T>::store(p.out, o + 1, acc.y * inv);
         Elem<T>::store(p.out, o + 2, acc.z * inv);
