@@ -82,6 +82,18 @@ def lib() -> ctypes.CDLL:
         L.oracle_quant_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
         L.oracle_quant_decode_attn.restype = I
         L.oracle_quant_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+        L.oracle_e4m3_value.restype = ctypes.c_double
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_fp8_quantize_rows.restype = None
+        L.oracle_fp8_quantize_rows.argtypes = [P, I, I, I, P, P]
+        L.oracle_fp8_append.restype = I
+        L.oracle_fp8_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+        L.oracle_fp8_prefill_write.restype = I
+        L.oracle_fp8_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
+        L.oracle_fp8_decode_attn.restype = I
+        L.oracle_fp8_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
         L.oracle_set_fault.restype = None
         L.oracle_set_fault.argtypes = [I]
         L.oracle_get_fault.restype = I
@@ -227,6 +239,60 @@ class QuantCache:
         return (out, bad) if return_bad else out
 
 
+def e4m3_value(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (uint8 array)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib().oracle_e4m3_value(int(x)) for x in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at +-448."""
+    a = np.asarray(x, dtype=np.float32)
+    return np.array([lib().oracle_e4m3_encode(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
+
+
+def fp8_quantize_rows(x):
+    """E4M3 codes (uint8) and fp32 scales of the rows of x [..., D] (bf16 bits or float32)."""
+    x = np.ascontiguousarray(x)
+    D = x.shape[-1]
+    n = x.size // D
+    codes = np.zeros(x.shape, np.uint8)
+    scales = np.zeros(x.shape[:-1], np.float32)
+    lib().oracle_fp8_quantize_rows(_ptr(x), n, D, _dtype_code(x), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+class Fp8Cache(QuantCache):
+    """One layer of an fp8 cache: E4M3 codes [B,H_kv,T_max,D] (uint8) and fp32 row scales
+    [B,H_kv,T_max] for K and for V."""
+
+    def __init__(self, B, H_kv, T_max, D):
+        super().__init__(B, H_kv, T_max, D)
+        self.Kq = np.zeros((B, H_kv, T_max, D), np.uint8)
+        self.Vq = np.zeros_like(self.Kq)
+
+    def append(self, k_new, v_new, lens) -> int:
+        B, H_kv, T_max, D = self.Kq.shape
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        return lib().oracle_fp8_append(*self._args(), _ptr(k_new), _ptr(v_new), _ptr(lens), B, H_kv,
+                                       T_max, D, _dtype_code(k_new))
+
+    def prefill_write(self, K, V, lens) -> int:
+        B, H_kv, T_max, D = self.Kq.shape
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        return lib().oracle_fp8_prefill_write(*self._args(), _ptr(K), _ptr(V), K.shape[2], _ptr(lens), B,
+                                              H_kv, T_max, D, _dtype_code(K))
+
+    def decode_attn(self, q, lens, return_bad: bool = False):
+        B, H_kv, T_max, D = self.Kq.shape
+        H_q = q.shape[1]
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        out = np.zeros((B, H_q, D), dtype=np.float64)
+        bad = lib().oracle_fp8_decode_attn(_ptr(q), *self._args(), _ptr(lens), B, H_q, H_kv, T_max, D,
+                                           _dtype_code(q), _ptr(out))
+        return (out, bad) if return_bad else out
+
+
 def append_multi(Kc, Vc, k_new, v_new, lens) -> int:
     """In place: the T_q rows of k_new/v_new [B,H_kv,T_q,D] into slots [lens[b]-T_q, lens[b])."""
     B, H_kv, T_max, D = Kc.shape
@@ -313,7 +379,8 @@ class planted_fault:
     4 = the new token left out of the attention, 5 = paged block stored token-major,
     6 = sliding window one position too wide,
     7 = several-query causal mask aligned to the upper left,
-    8 = quantization scale max/128 instead of max/127."""
+    8 = quantization scale max/128 instead of max/127,
+    9 = E4M3 rounding ties away from zero, 10 = fp8 scale max/240 instead of max/448."""
 
     def __init__(self, which: int):
         self.which = which

@@ -471,6 +471,156 @@ int oracle_quant_decode_attn(const void* q, const int8_t* Kq, const float* Ks, c
 }
 
 /* ---------------------------------------------------------------------------------------
+ * fp8 cache.  The pages name fp8 beside int8 as a cache format read with higher-precision
+ * softmax accumulation ([M11] §3.1 and §8; [KVG] "MHA、GQA、MLA 与量化如何改变容量").  Reading
+ * taken: E4M3 codes as the OCP 8-bit floating-point format defines them -- 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9;
+ * there is no infinity and S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 * 2^8 = 448 -- with one fp32 scale per (sequence, KV head, token) row:
+ *   scale = max_d |x_d| / 448                      (fp32)
+ *   code_d = e4m3(x_d / scale)                     (fp32 division, then round to the nearest
+ *                                                   code, ties to the even code; magnitudes
+ *                                                   beyond 448 saturate to 448)
+ *   x_d ~ value(code_d) * scale                    (the attention reads these values)
+ * A row of zeros has scale 0 and codes 0.  Layout as for int8: codes [B, H_kv, T_max, D] (one
+ * byte each), scales [B, H_kv, T_max] fp32, for K and for V.
+ * ------------------------------------------------------------------------------------- */
+
+/* The value a code stands for (NaN for the two NaN codes). */
+double oracle_e4m3_value(uint8_t c) {
+    int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest code to x (ties to the even code), saturating at +-448; the sign bit follows x's
+ * (so -0 gives 0x80).  x is finite.  The non-negative finite codes 0x00 .. 0x7E are ordered by
+ * value, so the code below x is found by bisection over them. */
+uint8_t oracle_e4m3_encode(float x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    double v = fabs((double)x);
+    if (v >= 448.0) return sign | 0x7E;
+    int lo = 0, hi = 0x7E; /* value(lo) <= v < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (oracle_e4m3_value((uint8_t)mid) <= v) lo = mid; else hi = mid;
+    }
+    double a = oracle_e4m3_value((uint8_t)lo), b = oracle_e4m3_value((uint8_t)hi);
+    int c;
+    if (v - a < b - v) c = lo;
+    else if (v - a > b - v) c = hi;
+    else c = (lo & 1) ? hi : lo; /* a tie: the even code */
+    if (g_fault == 9 && v - a == b - v) c = hi; /* planted: ties away from zero */
+    return sign | (uint8_t)c;
+}
+
+static void fp8_row(const void* x, int dtype, size_t off, int D, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(load_f32(x, dtype, off + d));
+        if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    if (g_fault == 10) s = amax / 240.0f; /* planted: the range of the other E4M3 variant */
+    *scale = s;
+    for (int d = 0; d < D; ++d) codes[d] = s > 0.0f ? oracle_e4m3_encode(load_f32(x, dtype, off + d) / s) : 0;
+}
+
+/* Quantizes rows of a [n_rows, D] array (dtype) into E4M3 codes [n_rows, D] and scales [n_rows]. */
+void oracle_fp8_quantize_rows(const void* x, int n_rows, int D, int dtype, uint8_t* codes, float* scales) {
+    for (int r = 0; r < n_rows; ++r) fp8_row(x, dtype, (size_t)r * D, D, codes + (size_t)r * D, scales + r);
+}
+
+/* Appends k_new/v_new [B, H_kv, D] (dtype), as fp8 rows, at slot lens[b]-1.  Returns the number
+ * of invalid rows (lens out of [1, T_max]; skipped). */
+int oracle_fp8_append(uint8_t* Kq, float* Ks, uint8_t* Vq, float* Vs, const void* k_new,
+                      const void* v_new, const int32_t* lens, int B, int H_kv, int T_max, int D,
+                      int dtype) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 1 || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h) {
+            size_t row = ((size_t)b * H_kv + h) * T_max + (size_t)(L - 1);
+            size_t src = ((size_t)b * H_kv + h) * D;
+            fp8_row(k_new, dtype, src, D, Kq + row * D, Ks + row);
+            fp8_row(v_new, dtype, src, D, Vq + row * D, Vs + row);
+        }
+    }
+    return bad;
+}
+
+/* Writes K/V [B, H_kv, T_in, D] (dtype) rows [0, lens[b]) as fp8 rows.  Returns the number of
+ * invalid rows (lens out of [0, min(T_in, T_max)]). */
+int oracle_fp8_prefill_write(uint8_t* Kq, float* Ks, uint8_t* Vq, float* Vs, const void* K,
+                             const void* V, int T_in, const int32_t* lens, int B, int H_kv,
+                             int T_max, int D, int dtype) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        int L = lens[b];
+        if (L < 0 || L > T_in || L > T_max) {
+            ++bad;
+            continue;
+        }
+        for (int h = 0; h < H_kv; ++h)
+            for (int t = 0; t < L; ++t) {
+                size_t row = ((size_t)b * H_kv + h) * T_max + (size_t)t;
+                size_t src = (((size_t)b * H_kv + h) * T_in + t) * D;
+                fp8_row(K, dtype, src, D, Kq + row * D, Ks + row);
+                fp8_row(V, dtype, src, D, Vq + row * D, Vs + row);
+            }
+    }
+    return bad;
+}
+
+/* Decode attention over an fp8 cache: the same arithmetic as oracle_decode_attn on the values
+ * value(code) * scale (formed in double).  out [B, H_q, D] double. */
+int oracle_fp8_decode_attn(const void* q, const uint8_t* Kq, const float* Ks, const uint8_t* Vq,
+                           const float* Vs, const int32_t* lens, int B, int H_q, int H_kv,
+                           int T_max, int D, int dtype, double* out) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b)
+        if (lens[b] < 1 || lens[b] > T_max) ++bad;
+    const int rows = B * H_q;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) if (g_threads > 1)
+#endif
+    for (int r = 0; r < rows; ++r) {
+        int b = r / H_q, j = r % H_q;
+        int L = lens[b];
+        double* o = out + (size_t)r * D;
+        if (L < 1 || L > T_max) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        int h = kv_head_of(j, H_q, H_kv);
+        double* qd = (double*)malloc(sizeof(double) * D);
+        double* Kd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* Vd = (double*)malloc(sizeof(double) * (size_t)L * D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)L);
+        for (int d = 0; d < D; ++d) qd[d] = load_elem(q, dtype, (size_t)r * D + d);
+        size_t row0 = ((size_t)b * H_kv + h) * (size_t)T_max;
+        for (int t = 0; t < L; ++t) {
+            double sk = (double)Ks[row0 + t], sv = (double)Vs[row0 + t];
+            for (int d = 0; d < D; ++d) {
+                Kd[(size_t)t * D + d] = oracle_e4m3_value(Kq[(row0 + t) * D + d]) * sk;
+                Vd[(size_t)t * D + d] = oracle_e4m3_value(Vq[(row0 + t) * D + d]) * sv;
+            }
+        }
+        decode_row_f64(qd, Kd, Vd, L, D, (size_t)D, o, sc);
+        free(qd);
+        free(Kd);
+        free(Vd);
+        free(sc);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Several new tokens per step (chunked prefill, speculative decoding).  With a cache holding
  * S keys after appending T new tokens, new query i (absolute position S - T + i) sees keys
  * 0 .. S - T + i: the causal mask aligned to the lower right of the T x S score matrix
