@@ -229,9 +229,10 @@ def run_ours(args, w):
         table, num_blocks, max_blocks = paged_table(w, args.paged, spare=w.B)
         cache = kvc.PagedKVCache(L, num_blocks, args.paged, w.B, max_blocks, w.H_q, w.H_kv, w.D, w.dtype)
         table_d = table.to(dev)
-    elif args.int8:
-        # int8 cache with one fp32 scale per (sequence, head, token) row; q / out / new rows bf16
-        cache = kvc.QuantKVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max())
+    elif args.int8 or args.fp8:
+        # int8 or fp8 (E4M3) cache with one fp32 scale per (sequence, head, token) row; q / out /
+        # new rows bf16
+        cache = kvc.QuantKVCache(L, w.B, w.H_q, w.H_kv, w.D, w.T_max(), fp8=args.fp8)
     elif args.window:
         # sliding-window attention: a rolling cache of `window` slots per sequence
         cache = kvc.RollingKVCache(L, w.B, w.H_q, w.H_kv, w.D, args.window, w.dtype)
@@ -329,7 +330,8 @@ def run_ours(args, w):
     if st != kvc.KVC_OK:
         raise RuntimeError(f"device error in the timed region: status {st} detail {detail:#x}")
 
-    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window, args.tq, args.int8)
+    quant = args.int8 or args.fp8  # 8-bit codes + a 4-byte scale per row
+    kv_bytes_step = L * w.kv_read_bytes_per_layer(args.window, args.tq, quant)
     gbs = whole_job_rate(world, kv_bytes_step, ms)
     peak, peak_kind = measured_peaks()
 
@@ -350,9 +352,9 @@ def run_ours(args, w):
     launch_ms = statistics.mean(per_launch)
     B, Hq, Hkv, D, s = w.B, w.H_q, w.H_kv, w.D, w.elem_bytes
     T_q = args.tq
-    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window, T_q, args.int8) + 2 * B * Hq * T_q * D * s
+    alg_bytes_launch = (w.kv_read_bytes_per_layer(args.window, T_q, quant) + 2 * B * Hq * T_q * D * s
                         + 2 * B * Hkv * T_q * D * s  # k/v new read
-                        + 2 * B * Hkv * T_q * (D + 4 if args.int8 else D * s) + 4 * B)  # written, lens
+                        + 2 * B * Hkv * T_q * (D + 4 if quant else D * s) + 4 * B)  # written, lens
     if args.paged:  # each block-table entry a sequence uses, read once
         alg_bytes_launch += 4 * sum(-(-int(x) // args.paged) for x in w.lens().tolist())
     # average decode-launch duration over the timed region (graph replay, gaps included; a layer
@@ -361,12 +363,12 @@ def run_ours(args, w):
     achieved = alg_bytes_launch / (region_launch_ms * 1e-3) / 1e9
     # the committed summaries are captures of the 8B-GQA workload (plain, or paged): another
     # workload, layer count or mode has no measured traffic
-    profiled = (w.name == "gqa8b_b24_ragged3000_6000" and not (args.window or args.tq > 1 or args.int8))
+    profiled = (w.name == "gqa8b_b24_ragged3000_6000" and not (args.window or args.tq > 1 or quant))
     traffic = traffic_from_profiles(kernel_source_hash(), args.paged) if profiled else None
     path = kvc.kvc_get_math(cache.h)
     kernel_name = {1: f"decode_kernel<{w.dtype},{w.D},{w.G}> (CUDA cores)",
                    2: f"decode_tc_kernel<{w.D},{w.G}> (mma.sync)",
-                   3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'int8' if args.int8 else 'rolling' if args.window else 'contiguous'}> (tcgen05)"}[path]
+                   3: f"decode_tc5_kernel<{w.G}, {'paged' if args.paged else 'int8' if args.int8 else 'fp8' if args.fp8 else 'rolling' if args.window else 'contiguous'}> (tcgen05)"}[path]
 
     # ---- end to end through the C ABI with host buffers: each step copies its inputs (lens and
     # every layer's q, k_new, v_new, packed in one pinned buffer) host -> device in one copy,
@@ -415,7 +417,7 @@ def run_ours(args, w):
 
     # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
     cpu = None
-    plain = not (args.paged or args.window or args.tq > 1 or args.int8)  # the oracle arm's workload
+    plain = not (args.paged or args.window or args.tq > 1 or quant)  # the oracle arm's workload
     if rank == 0 and world == 1 and not args.no_cpu_baseline and plain:
         threads = os.cpu_count() or 1
         cgbs, layers_done, secs, used = oracle_sample(w, budget_s=args.cpu_budget, threads=threads)
@@ -438,7 +440,8 @@ def run_ours(args, w):
             "config": {"workload": w.name + (f", paged cache, {args.paged}-token blocks" if args.paged else "")
                                    + (f", rolling cache, window {args.window}" if args.window else "")
                                    + (f", {args.tq} new tokens per step" if args.tq > 1 else "")
-                                   + (", int8 cache with per-row fp32 scales" if args.int8 else ""),
+                                   + (", int8 cache with per-row fp32 scales" if args.int8 else "")
+                                   + (", fp8 (E4M3) cache with per-row fp32 scales" if args.fp8 else ""),
                        "layers": L, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
                        "D": w.D, "lens": (f"U{{{w.T_lo}..{w.T_hi}}}+1 seed {w.seed}" if w.T is None else f"{w.T}+1"),
                        "kv_bytes_per_step": kv_bytes_step,
@@ -481,6 +484,8 @@ def main():
                     help="run the workload from a paged cache with this block size (0: contiguous)")
     ap.add_argument("--int8", action="store_true",
                     help="int8 cache with per-row fp32 scales (quantized on write)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="fp8 (E4M3) cache with per-row fp32 scales (quantized on write)")
     ap.add_argument("--tq", type=int, default=1, choices=[1, 2, 4, 8],
                     help="new tokens per sequence and step (speculative decoding; 1: plain decode)")
     ap.add_argument("--window", type=int, default=0,
@@ -498,8 +503,10 @@ def main():
         ap.error("--paged and --window are separate cache kinds")
     if args.tq > 1 and (args.paged or args.window):
         ap.error("--tq runs on the contiguous cache")
-    if args.int8 and (args.paged or args.window or args.tq > 1):
-        ap.error("--int8 runs on the contiguous cache with one new token")
+    if (args.int8 or args.fp8) and (args.paged or args.window or args.tq > 1):
+        ap.error("--int8 / --fp8 run on the contiguous cache with one new token")
+    if args.int8 and args.fp8:
+        ap.error("--int8 and --fp8 are separate cache kinds")
     from kv_cache_decode_kvc_gb300.workloads import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
     if args.layers:

@@ -168,6 +168,26 @@ int kvc_create_quantized(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
                          int dtype);
 int kvc_layer_scales(kvc_t h, int layer, float** Ks, float** Vs);
 
+/* fp8 cache: as kvc_create_quantized, with E4M3 codes (the OCP 8-bit float: 1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits, subnormals m * 2^-9, no infinity, largest finite 448) and
+ * one fp32 scale per (sequence, KV head, token) row for K and for V:
+ *     scale = max_d |x_d| / 448,   code_d = E4M3(x_d / scale)
+ * (IEEE fp32 division; round to the nearest code, ties to even, saturating at +-448; a zero row
+ * has scale 0), and the attention reads value(code) * scale.  The same names as for int8 ("KV 缓存",
+ * "MHA、GQA、MLA 与量化如何改变容量"; "11.7 KV Cache" §3.1 and §8 list int8 and fp8 caches).
+ * The tcgen05 kernel multiplies the K codes by q directly (q split exactly into three E4M3 terms),
+ * so only V is widened (to f16) on chip.  Per layer: codes [B, H_kv, T_max, D] (one byte each,
+ * kvc_layer_ptrs) and scales (kvc_layer_scales).  Supported: dtype KVC_BF16, D = 128,
+ * H_q / H_kv <= 8, one new token per step, math 0 or 3; else KVC_EUNSUPPORTED. */
+int kvc_create_fp8(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype);
+
+/* The handle's cache format: KVC_CACHE_PLAIN (bf16 / fp32 values), KVC_CACHE_INT8, KVC_CACHE_FP8;
+ * -1 for NULL. */
+#define KVC_CACHE_PLAIN 0
+#define KVC_CACHE_INT8 1
+#define KVC_CACHE_FP8 2
+int kvc_get_cache_format(kvc_t h);
+
 /* ---------------------------------------------------------------------------------------
  * Several new tokens per step (chunked prefill, speculative decoding).  After T_q new tokens
  * are appended to a sequence of S = lens[b] positions, new query i sits at position S - T_q + i

@@ -32,6 +32,7 @@ def _units():
     units.append(("kvc_decode_tc5p_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=1"]))
     units.append(("kvc_decode_tc5r_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=2"]))
     units.append(("kvc_decode_tc5q_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=3"]))
+    units.append(("kvc_decode_tc5f_d128", "kvc_decode_tc5_inst.cu", ["-DKVC_TC5_MODE=4"]))
     for dt, d in DECODE_INST:
         units.append((f"kvc_decode_{dt}_d{d}", "kvc_decode_inst.cu",
                       [f"-DKVC_INST_BF16={1 if dt == 'bf16' else 0}", f"-DKVC_INST_D={d}"]))

@@ -74,8 +74,8 @@ __global__ void prefill_kernel(const CopyParams p) {
     }
 }
 
-// int8 cache (p.Ksc set; bf16 source rows, D = 128): one warp per (b, h, row) quantizes the
-// source row into codes and a row scale (q8_store_row).  Append: rows [L - T_in, L) from the
+// int8 or fp8 cache (p.Ksc set; bf16 source rows, D = 128): one warp per (b, h, row) quantizes
+// the source row into codes and a row scale (q8_store_row, or f8_store_row for E4M3 codes).  Append: rows [L - T_in, L) from the
 // [B, H_kv, T_in, D] source; prefill: rows [0, L) from [B, H_kv, T_in, D].
 __global__ void quant_write_kernel(const CopyParams p, int prefill) {
     const size_t gw = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
@@ -104,8 +104,13 @@ __global__ void quant_write_kernel(const CopyParams p, int prefill) {
     const size_t crow = bh * p.T_max + t;
     const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(p.K) + gw * 128;
     const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.V) + gw * 128;
-    q8_store_row(ks, static_cast<int8_t*>(p.Kc) + crow * 128, p.Ksc + crow, lane);
-    q8_store_row(vs, static_cast<int8_t*>(p.Vc) + crow * 128, p.Vsc + crow, lane);
+    if (p.fp8) {
+        f8_store_row(ks, static_cast<uint8_t*>(p.Kc) + crow * 128, p.Ksc + crow, lane);
+        f8_store_row(vs, static_cast<uint8_t*>(p.Vc) + crow * 128, p.Vsc + crow, lane);
+    } else {
+        q8_store_row(ks, static_cast<int8_t*>(p.Kc) + crow * 128, p.Ksc + crow, lane);
+        q8_store_row(vs, static_cast<int8_t*>(p.Vc) + crow * 128, p.Vsc + crow, lane);
+    }
 }
 
 static int launch_quant_write(const CopyParams& p, int prefill, cudaStream_t s) {

@@ -26,13 +26,17 @@
 
 namespace kvc {
 
-template <int G_>
+template <int G_, int MODE_ = 0>
 struct Tc5Cfg {
     static constexpr int D = 128;
     static constexpr int G = G_;
-    static constexpr int N = G < 16 ? 16 : G;           // MMA N (heads, padded)
+    // fp8 cache (MODE 4): MMA1 reads the E4M3 K tile as it lands and q as three E4M3 terms per
+    // head (rows [t G, (t + 1) G) hold term t); only V is widened (to f16) for MMA2
+    static constexpr bool FP8 = MODE_ == 4;
+    static constexpr int NP = G < 16 ? 16 : G;          // heads, padded (P rows and O^T columns)
+    static constexpr int N = FP8 ? (3 * G + 15) / 16 * 16 : NP;  // MMA1 N (q rows, padded)
     static constexpr int ROWB = D * 2;
-    static constexpr int HALVES = D / 64;               // 128-byte column blocks
+    static constexpr int HALVES = D / 64;               // 128-byte column blocks of a 16-bit row
     // softmax warps (+ producer + MMA warp): HSPLIT per tensor-memory lane quadrant, each with
     // GH = G / HSPLIT of the group's head columns (large groups: more warps, fewer registers each)
     static constexpr int HSPLIT = G >= 16 ? 2 : 1;
@@ -40,23 +44,28 @@ struct Tc5Cfg {
     static constexpr int NW = 4 * HSPLIT;
     static constexpr int NEPI = 2;                      // segment-epilogue warps
     static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
-    static constexpr int NCONV = 4;                     // int8 -> bf16 converter warps (int8 cache)
+    static constexpr int NCONV = 4;                     // converter warps (int8 and fp8 caches)
     static constexpr int TT = 128;                      // tokens per tile = MMA M
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
-    static constexpr int HALF_BYTES = TT * 128;         // one column block of a K or V tile
-    static constexpr int TILE_BYTES = TT * ROWB;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K and V of one tile
-    static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128] operand
-    static constexpr int OPB_BYTES = HALVES * OPB_BLOCK;
+    static constexpr int HALF_BYTES = TT * 128;         // one column block of a 16-bit K or V tile
+    static constexpr int TILE_BYTES = TT * ROWB;        // a 16-bit tile
+    // a ring stage holds one tile of K and one of V as they land: 16-bit tiles, or for an fp8
+    // cache 8-bit ones (TT rows of D bytes, 128-byte swizzled), whose V is widened into one of
+    // two f16 working tiles (VW)
+    static constexpr int LAND_BYTES = FP8 ? TT * D : TILE_BYTES;
+    static constexpr int STAGE_BYTES = 2 * LAND_BYTES;
+    static constexpr int VW_BYTES = FP8 ? 2 * TILE_BYTES : 0;
+    static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128 B] operand
+    static constexpr int OPB_BYTES = (FP8 ? 1 : HALVES) * OPB_BLOCK;
     // P operand of MMA2, P_hi and P_lo side by side as the N2 columns of one MMA:
-    //  K-major (G <= 8): rows [0, N) = P_hi, rows [N, 2N) = P_lo, in 64-token column blocks of
-    //    PBLOCK bytes (a thread stores its token's weights one bf16 at a time);
-    //  MN-major (G >= 16): one 128-byte row per token, P_hi at columns [0, N) and P_lo at
-    //    [32, 32 + N) (a thread stores its token's weights in 16-byte vectors).
-    // PBUF = one whole 128-token buffer.
+    //  K-major (G <= 8): rows [0, NP) = P_hi, rows [NP, 2NP) = P_lo, in 64-token column blocks of
+    //    PBLOCK bytes (a thread stores its token's weights one 16-bit value at a time);
+    //  MN-major (G >= 16): one 128-byte row per token, P_hi at columns [0, NP) and P_lo at
+    //    [32, 32 + NP) (a thread stores its token's weights in 16-byte vectors).
+    // PBUF = one whole 128-token buffer.  (fp8 cache: P and the widened V are f16, else bf16.)
     static constexpr bool PMN = G >= 16;
-    static constexpr int N2 = PMN ? 64 : 2 * N;
-    static constexpr int LOOFF = PMN ? 32 : N;          // column of P_lo, and of O^T_lo
+    static constexpr int N2 = PMN ? 64 : 2 * NP;
+    static constexpr int LOOFF = PMN ? 32 : NP;         // column of P_lo, and of O^T_lo
     static constexpr int PBLOCK = N2 * 128;
     static constexpr int PBUF = PMN ? TT * 128 : (TT / 64) * PBLOCK;
     static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
@@ -64,11 +73,11 @@ struct Tc5Cfg {
     static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
     static constexpr int RED_BYTES = 6 * N * 4;         // reductions [quadrant][N], rescale factors [2][N]
     // 4 tensor maps: K and V with 128-row boxes (full tiles) and 32-row boxes (partial tiles)
-    static constexpr int MISC_BYTES = 256;
+    static constexpr int MISC_BYTES = 512;              // mbarriers and flags
     static constexpr int ALIGN_PAD = 1024;
     static constexpr int BUDGET = 232448;               // opt-in maximum per CTA (227 KB)
-    static constexpr int FIXED = OPB_BYTES + 2 * PBUF + MERGE_FLOATS * 4 + PREFIX_BYTES + RED_BYTES +
-                                 MISC_BYTES + ALIGN_PAD;
+    static constexpr int FIXED = OPB_BYTES + 2 * PBUF + VW_BYTES + MERGE_FLOATS * 4 + PREFIX_BYTES +
+                                 RED_BYTES + MISC_BYTES + ALIGN_PAD;
     static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NST = NST_A > 4 ? 4 : NST_A;
     static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
@@ -78,7 +87,8 @@ struct Tc5Cfg {
     static_assert(NST >= 2, "ring too shallow");
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(HSPLIT == 1 || GH % 8 == 0, "head slices start on a swizzle row group");
-    static_assert(!PMN || N <= 32, "P_hi and P_lo share one 64-column row");
+    static_assert(!PMN || NP <= 32, "P_hi and P_lo share one 64-column row");
+    static_assert(!FP8 || G <= 8, "fp8 cache: up to 8 query heads per KV head");
     static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
 };
 
@@ -97,7 +107,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Threads of the kernel instantiation: a quantized cache adds the converter warps.
 template <int G, int MODE>
 __host__ __device__ constexpr int tc5_threads() {
-    return Tc5Cfg<G>::NTHREADS + (MODE == 3 ? Tc5Cfg<G>::NCONV * 32 : 0);
+    return Tc5Cfg<G, MODE>::NTHREADS + ((MODE == 3 || MODE == 4) ? Tc5Cfg<G, MODE>::NCONV * 32 : 0);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness (0 = K-major,
@@ -105,6 +115,25 @@ __host__ __device__ constexpr int tc5_threads() {
 __host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor with f16 A and B (format code 0; fp32 accumulator), and for kind::f8f6f4
+// with E4M3 A and B (format code 0 there too; both K-major).
+__host__ __device__ constexpr uint32_t instr_desc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t instr_desc_e4m3(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc5_mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc5_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -217,14 +246,14 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
-    const uint32_t vs = ks + C::TILE_BYTES;
-    constexpr bool PAGED = MODE == 1, QUANT = MODE == 3;
+    const uint32_t vs = ks + C::LAND_BYTES;
+    constexpr bool PAGED = MODE == 1, QUANT = MODE == 3, FP8 = MODE == 4;
     constexpr bool paged = PAGED;
     const bool full = n == TT && !paged;
     const int rows = paged ? p.box_rows : (full ? TT : C::BOX_ROWS);
     const int nbox = full ? 1 : (n + rows - 1) / rows;
-    // bf16 tiles: 2 x 128-byte column blocks per row; int8 tiles: one row of D bytes
-    const uint32_t kv_bytes = (uint32_t)(2 * nbox * rows * (QUANT ? C::D : C::HALVES * 128));
+    // bf16 tiles: 2 x 128-byte column blocks per row; int8 and fp8 tiles: one row of D bytes
+    const uint32_t kv_bytes = (uint32_t)(2 * nbox * rows * ((QUANT || FP8) ? C::D : C::HALVES * 128));
     if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], kv_bytes);
     if constexpr (PAGED) {
         {
@@ -243,6 +272,17 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
                 tma_load_4d(ks + off, tmK, row >> 3, rows >> 3, &full_bar[stage], pol);
                 tma_load_4d(vs + off, tmV, row >> 3, rows >> 3, &full_bar[stage], pol);
             }
+        }
+    } else if (FP8) {
+        // E4M3 rows (128 bytes, 128-byte swizzled) as they are: K is MMA1's operand, V is widened
+        // by the converter warps
+        const int row0 = (int)(unit * p.T_max + c.t);
+        const CUtensorMap* mk = full ? tmKf : tmK;
+        const CUtensorMap* mv = full ? tmVf : tmV;
+        for (int bx = 0; bx < nbox; ++bx) {
+            const uint32_t off = bx * C::BOX_ROWS * C::D;
+            tma_load_2d(ks + off, mk, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+            tma_load_2d(vs + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
         }
     } else if (QUANT) {
         // int8 rows (128 bytes) into the back column block of the tile area, widened in place later
@@ -348,16 +388,19 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                       const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKf,
                       const __grid_constant__ CUtensorMap tmVf) {
-    using C = Tc5Cfg<G>;
+    using C = Tc5Cfg<G, MODE>;
     using T = __nv_bfloat16;
-    constexpr bool PAGED = MODE == 1, ROLL = MODE == 2, QUANT = MODE == 3;
-    constexpr int D = C::D, N = C::N, TT = C::TT, NST = C::NST, KS = D / 16, TS = TT / 16;
+    constexpr bool PAGED = MODE == 1, ROLL = MODE == 2, QUANT = MODE == 3, FP8 = MODE == 4;
+    constexpr bool SCALED = QUANT || FP8;  // rows carry fp32 scales (K: scores, V: weights)
+    constexpr int D = C::D, N = C::N, NP = C::NP, TT = C::TT, NST = C::NST, TS = TT / 16;
+    constexpr int KS = FP8 ? D / 32 : D / 16;  // MMA1 k-steps of 32 bytes
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = smem;
-    unsigned char* qsw = ring + NST * C::STAGE_BYTES;        // q, [N][D] K-major swizzled
+    unsigned char* vw = ring + NST * C::STAGE_BYTES;          // fp8 cache: f16 V working tiles [2]
+    unsigned char* qsw = vw + C::VW_BYTES;                    // q, [N][D] K-major swizzled
     unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][2 blocks][2N rows][128 B]
     float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
     int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
@@ -386,6 +429,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     uint64_t* append_bar = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(mma1_issued + 1) + 7) & ~uintptr_t(7));
     uint64_t* conv_full = append_bar + 1;  // [NST] int8 cache: the stage's tiles are bf16 now
+    uint64_t* vw_full = conv_full + NST;   // [2] fp8 cache: V working tile written (converters)
+    uint64_t* vw_empty = vw_full + 2;      // [2] fp8 cache: V working tile read (MMA2 commit)
 
     // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
     // CTAs take SMs as ours exit) but waits in griddepcontrol.wait until this grid is complete.
@@ -393,7 +438,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     if (tid == 32) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            // a stage is free once MMA2 has read it; fp8: once MMA1 has read K and the converters V
+            mbar_init(&empty_bar[s], FP8 ? 2 : 1);
             issued[s] = 0;
         }
         for (int i = 0; i < 2; ++i) {
@@ -408,6 +454,11 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         mbar_init(append_bar, 1);
         if constexpr (QUANT)
             for (int s = 0; s < NST; ++s) mbar_init(&conv_full[s], C::NCONV * 32);
+        if constexpr (FP8)
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&vw_full[i], C::NCONV * 32);
+                mbar_init(&vw_empty[i], 1);
+            }
         *abort_flag = 0;
         *last_flag = 0;
         *mma_issued = 0;
@@ -498,11 +549,18 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     // MMA2(k): O^T[k&1] = V(stage st)^T . (P_hi + P_lo)^T, then its commits (run by one thread:
     // the producer's, or for a paged pool with m2p = 0 the MMA warp's: a producer warp that
     // issues one copy per block can be the slower of the two)
-    const bool m2p = !PAGED || p.m2p != 0;
-    constexpr uint32_t IDESC2 = instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);  // V read MN-major x P
+    // (fp8: the MMA warp issues MMA2 as well, one tile behind MMA1; a stage is free once MMA1
+    // has read K and the converters V, and the producer thread only refills the ring: a tensor
+    // copy can hold its issuing thread for hundreds of cycles, so no MMA waits behind one)
+    const bool m2p = !FP8 && (!PAGED || p.m2p != 0);
+    // V read MN-major x P; an fp8 cache's widened V and its weights are f16
+    constexpr uint32_t IDESC2 = FP8 ? instr_desc_f16(128, C::N2, 1, C::PMN ? 1 : 0)
+                                    : instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);
     using LY = Tc5Layout<C, PAGED>;
+    const uint32_t vw_s = smem_addr(vw);
     auto issue_mma2 = [&](int k, int st, uint32_t tm) {
-        const uint64_t dV0 = smem_desc_sw128(ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
+        // V: the stage's tile, or (fp8) the f16 working tile k & 1
+        const uint64_t dV0 = smem_desc_sw128(FP8 ? vw_s : ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
         // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
         // leading offset is never stepped over)
         const uint32_t pbuf_s = smem_addr(pbuf);
@@ -512,13 +570,17 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
 #pragma unroll
         for (int kk = 0; kk < TS; ++kk) {
-            const uint32_t voff = (uint32_t)(st * C::STAGE_BYTES + kk * 2 * LY::GSTR);
+            const uint32_t voff = (uint32_t)((FP8 ? (k & 1) * C::TILE_BYTES : st * C::STAGE_BYTES) +
+                                             kk * 2 * LY::GSTR);
             const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
                                          : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
             tc5_mma(tO, dV0 + (voff >> 4), dP0 + (poff >> 4), IDESC2, kk > 0 ? 1u : 0u);
         }
         tc5_commit(&o_full[k & 1]);
-        tc5_commit(&empty_bar[st]);  // K/V of the stage are consumed
+        if constexpr (FP8)
+            tc5_commit(&vw_empty[k & 1]);  // the working tile is free (the stage was freed earlier)
+        else
+            tc5_commit(&empty_bar[st]);  // K/V of the stage are consumed
         *mma_issued += 1;
     };
 
@@ -561,6 +623,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     if (lane == 0) {
                         ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
                              mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+                        if (FP8 && ok) ok = mbar_wait(&vw_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
                         if (ok) {
                             tc5_fence_after();
                             // written by warp 1's allocation before the weights of tile 0 existed
@@ -569,7 +632,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                         }
                     }
                     if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                    if (ok && pref.valid) {
+                    if (!FP8 && ok && pref.valid) {
                         // tile k + NST goes into stage s2 once MMA2(k) has read it
                         if (lane == 0) ok = mbar_wait(&empty_bar[s2], (uint32_t)((k / NST) & 1), abort_flag, p.err);
                         if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
@@ -580,12 +643,13 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     if (++s2 == NST) s2 = 0;
                 }
             } else {
-                // each further tile into the next stage once the MMA warp's MMA2 has read it
+                // each further tile into the next stage once it is free (MMA2 has read it; fp8: MMA1
+                // has read K and the converters V)
                 int s = 0;
                 uint32_t ph = 1u;
                 while (ok && pref.valid) {
                     if (lane == 0) ok = mbar_wait(&empty_bar[s], ph ^ 1u, abort_flag, p.err);
-                    ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                    if constexpr (PAGED) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;  // (else lane 0 alone)
                     if (ok) ok = append_ready();
                     if (ok) issue_next(s);
                     if (++s == NST) { s = 0; ph ^= 1u; }
@@ -622,7 +686,32 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
             for (int i = 0; i < QPL; ++i) {
                 const int c = lane + 32 * i;
-                if (c < QV) {
+                if constexpr (FP8) {
+                    // a head's 16 chunks sit on 16 consecutive lanes of one slot: its largest |q| by a
+                    // half-warp reduction, then 2^-e q as three E4M3 terms in rows t G + h (one
+                    // 128-byte row per head and term, 8 bytes per chunk)
+                    const uint4 w = c < QV ? qv[i] : make_uint4(0u, 0u, 0u, 0u);
+                    float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                  bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, off));
+                    const float sc = exp2i(-f8_head_exp(amax));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] *= sc;
+                    uint2 t[3];
+                    e4m3_split3(f, t[0], t[1], t[2]);
+                    if (c < QV) {
+                        const int h = c / (D / 8), cc = c % (D / 8);
+#pragma unroll
+                        for (int tt = 0; tt < 3; ++tt) {
+                            const int r = tt * G + h;
+                            *reinterpret_cast<uint2*>(qsw + r * 128 + (((cc >> 1) ^ (r & 7)) << 4) + (cc & 1) * 8) = t[tt];
+                        }
+                    }
+                } else if (c < QV) {
                     const int h = c / (D / 8), cc = c % (D / 8);
                     *reinterpret_cast<uint4*>(qsw + (cc >> 3) * C::OPB_BLOCK + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) =
                         qv[i];
@@ -634,7 +723,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         named_bar_sync(2, 32 + C::NW * 32);
         tc5_fence_after();
         tmem = *tmem_slot;
-        constexpr uint32_t IDESC1 = instr_desc_bf16(128, N, 0, 0);  // K (K-major) x q (K-major)
+        // K (K-major) x q (K-major): bf16, or E4M3 codes and terms (kind::f8f6f4)
+        constexpr uint32_t IDESC1 = FP8 ? instr_desc_e4m3(128, N) : instr_desc_bf16(128, N, 0, 0);
         const uint32_t qsw_s = smem_addr(qsw);
         using LY = Tc5Layout<C, PAGED>;
         int s = 0;
@@ -643,25 +733,33 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         const uint64_t dK0 = smem_desc_sw128(ring_s, 16u, LY::GSTR);  // + stage, block, k-step
         const uint64_t dQ0 = smem_desc_sw128(qsw_s, 16u, 1024u);
         int s_prev = 0;
+        // MMA2 of tile j from this warp (the m2p = 0 orders below)
+        auto mma2_here = [&](int j) {
+            alive = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err) &&
+                    mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
+            if (FP8 && alive) alive = mbar_wait(&vw_full[j & 1], (j >> 1) & 1, abort_flag, p.err);
+            if (alive && lane == 0) {
+                tc5_fence_after();
+                issue_mma2(j, s_prev, tmem);
+            }
+            __syncwarp();
+        };
         for (int k = 0;; ++k) {
-            if (!m2p) {
+            if (!m2p && !FP8) {
                 // MMA2 of the previous tile here, first (it frees a ring stage as soon as the
                 // weights are written)
-                if (k > 0 && alive) {
-                    const int j = k - 1;
-                    alive = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.err) &&
-                            mbar_wait(&o_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, p.err);
-                    if (alive && lane == 0) {
-                        tc5_fence_after();
-                        issue_mma2(j, s_prev, tmem);
-                    }
-                    __syncwarp();
-                }
+                if (k > 0 && alive) mma2_here(k - 1);
+            }
+            if (FP8 && !cur.valid) {
+                // the last tile's MMA2 (MMA1 runs one tile ahead of MMA2 here)
+                if (k > 0 && alive) mma2_here(k - 1);
+                break;
             }
             if (!cur.valid || !alive) break;
             // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
             // int8 cache: wait until the converter warps have widened the stage to bf16
             alive = mbar_wait(QUANT ? &conv_full[s] : &full_bar[s], ph, abort_flag, p.err);
+            // (fp8: the K codes are read as they landed)
             if (alive && cur.first()) {
                 // the previous MMA1 read q_sw: let it finish before q is replaced
                 if (k > 0) alive = mbar_wait(&s_full[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, p.err);
@@ -678,16 +776,90 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 const uint32_t tS = tmem + (uint32_t)((k & 1) * N);
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
-                    const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * LY::HSTR + (kk & 3) * 32);
-                    const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
-                    tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
+                    if constexpr (FP8) {
+                        // one 128-byte column block: k-steps of 32 codes
+                        const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + kk * 32);
+                        tc5_mma_f8(tS, dK0 + (off >> 4), dQ0 + ((uint32_t)(kk * 32) >> 4), IDESC1, kk > 0 ? 1u : 0u);
+                    } else {
+                        const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * LY::HSTR + (kk & 3) * 32);
+                        const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
+                        tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
+                    }
                 }
                 tc5_commit(&s_full[k & 1]);
+                if constexpr (FP8) tc5_commit(&empty_bar[s]);  // K read (the converters arrive for V)
                 *mma1_issued += 1;
             }
             __syncwarp();
+            // fp8: MMA2 of the previous tile after MMA1 of this one, so the scores run a tile ahead
+            // of the weights (MMA1 of a tile is four instructions; the stage does not wait for MMA2)
+            if (FP8 && k > 0 && alive) mma2_here(k - 1);
             s_prev = s;
             cur.advance();
+            if (++s == NST) { s = 0; ph ^= 1u; }
+        }
+    } else if (FP8 && warp >= 2 + C::NW + C::NEPI) {
+        // ======================================================= E4M3 V -> f16 converters
+        // Per tile, in order: wait for the copies and for working tile k & 1 to be free (MMA2 of
+        // tile k - 2 has read it); widen the V codes (128-byte swizzled rows) into it, in the
+        // 128-byte-swizzled MN-major layout MMA2 reads ([column block][row][128 B]); rows past
+        // the loaded boxes become zeros (they meet weight 0, and stale bytes could be NaN codes).
+        // Then publish the working tile to the tensor cores and hand the stage's V back (MMA1's
+        // commit hands back K).
+        const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
+        TileCursor<TT> cc;
+        cc.init(prefix, B, H_kv, r0, r1);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int k = 0; cc.valid; ++k) {
+            const int w = k & 1;
+            ok = ok && mbar_wait(&full_bar[s], ph, abort_flag, p.err);
+            ok = ok && mbar_wait(&vw_empty[w], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+            if (ok) {
+                const int n = cc.n();
+                const int loaded = n == TT ? TT : ((n + C::BOX_ROWS - 1) / C::BOX_ROWS) * C::BOX_ROWS;
+                const unsigned char* vl = ring + s * C::STAGE_BYTES + C::LAND_BYTES;
+                unsigned char* vt = vw + w * C::TILE_BYTES;
+                // unit = (row r, 16-code column group c) -> 32 bytes of f16 (two 16-byte chunks).
+                // The 8 lanes of a quarter warp take one c and 8 consecutive rows, so their loads
+                // and stores hit 8 different swizzled chunks (no bank conflicts); each thread loads
+                // all of its units before converting any.
+                constexpr int PER = TT * 8 / (C::NCONV * 32);  // units per thread (8)
+                uint4 v[PER];
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int u = ct + i * C::NCONV * 32;
+                    const int r = ((u >> 6) << 3) | (u & 7), c = (u >> 3) & 7;
+                    v[i] = r < loaded ? *reinterpret_cast<const uint4*>(vl + r * 128 + ((c ^ (r & 7)) << 4))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int u = ct + i * C::NCONV * 32;
+                    const int r = ((u >> 6) << 3) | (u & 7), c = (u >> 3) & 7;
+                    // two codes per conversion (E4M3 -> f16 is exact; a zero code gives +0)
+                    const uint32_t x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+                            "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+                            : "=r"(h[2 * j]), "=r"(h[2 * j + 1])
+                            : "r"(x[j]));
+                    }
+                    // f16 columns [16c, 16c + 16): column block c / 4, chunks 2 (c % 4) and + 1
+                    unsigned char* row = vt + (c >> 2) * C::HALF_BYTES + r * 128;
+                    const int cb = 2 * (c & 3);
+                    *reinterpret_cast<uint4*>(row + ((cb ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4*>(row + (((cb + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+                }
+            }
+            fence_async_smem();  // generic-proxy writes before the tensor cores read them
+            mbar_arrive(&vw_full[w]);
+            named_bar_sync(4, C::NCONV * 32);  // every converter is done with the landed V
+            if (ct == 0) mbar_arrive(&empty_bar[s]);
+            cc.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
     } else if (QUANT && warp >= 2 + C::NW + C::NEPI) {
@@ -811,6 +983,18 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     }
                     r1 = r0;  // nothing left for the plain copy below
                 }
+                if constexpr (FP8) {
+                    for (int r = r0; r < r1; ++r) {
+                        const size_t crow = unit * p.T_max + r;
+                        f8_store_row(static_cast<const __nv_bfloat16*>(p.k_new) + unit * D,
+                                     static_cast<uint8_t*>(const_cast<void*>(p.K)) + crow * D,
+                                     const_cast<float*>(p.Ksc) + crow, lane);
+                        f8_store_row(static_cast<const __nv_bfloat16*>(p.v_new) + unit * D,
+                                     static_cast<uint8_t*>(const_cast<void*>(p.V)) + crow * D,
+                                     const_cast<float*>(p.Vsc) + crow, lane);
+                    }
+                    r1 = r0;
+                }
                 for (int r = r0; r < r1; ++r) {
                     int64_t arow;
                     if constexpr (PAGED)
@@ -881,8 +1065,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_empty[j & 1]);
         };
-        // int8 cache: the K and V scales of this thread's row of a tile; the new row of a fused
-        // step takes them from k_new / v_new, as its append computes them
+        // int8 / fp8 cache: the K and V scales of this thread's row of a tile; the new row of a
+        // fused step takes them from k_new / v_new, as its append computes them
         auto load_scales = [&](const TileCursor<TT>& c, float& a, float& b) {
             a = 1.f;
             b = 1.f;
@@ -890,8 +1074,10 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 const int t = c.t + row;
                 const size_t unit = (size_t)c.it.b * H_kv + c.it.h;
                 if (fused && t == c.it.L - 1) {
-                    a = q8_row_scale(static_cast<const __nv_bfloat16*>(p.k_new) + unit * D);
-                    b = q8_row_scale(static_cast<const __nv_bfloat16*>(p.v_new) + unit * D);
+                    const __nv_bfloat16* kr = static_cast<const __nv_bfloat16*>(p.k_new) + unit * D;
+                    const __nv_bfloat16* vr = static_cast<const __nv_bfloat16*>(p.v_new) + unit * D;
+                    a = FP8 ? f8_row_scale(kr) : q8_row_scale(kr);
+                    b = FP8 ? f8_row_scale(vr) : q8_row_scale(vr);
                 } else {
                     a = __ldcg(p.Ksc + unit * p.T_max + t);
                     b = __ldcg(p.Vsc + unit * p.T_max + t);
@@ -899,8 +1085,11 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             }
         };
         float sk_next = 1.f, sv_next = 1.f;
-        if constexpr (QUANT)
+        if constexpr (SCALED)
             if (cur.valid) load_scales(cur, sk_next, sv_next);
+        // fp8 cache: 2^e of each head's q terms (the MMA warp derives the same e from the same q)
+        float qe[FP8 ? GH : 1];
+        qe[0] = 1.f;
         SegIter last_it = cur.it;  // the segment of the latest `last` tile
         bool resc_prev = false;    // the previous tile moved the maxima
         for (int k = 0; cur.valid; ++k) {
@@ -912,19 +1101,50 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     o[h] = 0.f; m[h] = -INFINITY; mt[h] = -INFINITY; l[h] = 0.f; alpha_prev[h] = 1.f;
                 }
             }
-            // int8 cache: this row's K and V scales, loaded one tile ahead
+            // int8 / fp8 cache: this row's K and V scales, loaded one tile ahead
             const float sk = sk_next, sv = sv_next;
-            if constexpr (QUANT) {
+            if constexpr (SCALED) {
                 TileCursor<TT> nxt = cur;
                 nxt.advance();
                 if (nxt.valid) load_scales(nxt, sk_next, sv_next);
             }
-            const float qk = QUANT ? qscale * sk : qscale;
+            const float qk = SCALED ? qscale * sk : qscale;
+            // fp8 cache, a segment's first tile: each head's largest |q| (lane l reads elements
+            // 4l .. 4l+3; loads issued before the score wait), then 2^e after it
+            uint2 qraw[FP8 ? GH : 1];
+            if constexpr (FP8)
+                if (first) {
+                    const uint2* qg = reinterpret_cast<const uint2*>(p.q) + ((size_t)cur.it.b * H_kv + cur.it.h) * G * (D / 4);
+#pragma unroll
+                    for (int h = 0; h < GH; ++h) qraw[h] = __ldcg(qg + (size_t)h * (D / 4) + lane);
+                }
             // ---- scores of tile k
             alive = alive && mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
             tc5_fence_after();
             float x[GH];
-            {
+            if constexpr (FP8) {
+                if (first) {
+#pragma unroll
+                    for (int h = 0; h < GH; ++h) {
+                        float a = fmaxf(fmaxf(fabsf(bf16_lo(qraw[h].x)), fabsf(bf16_hi(qraw[h].x))),
+                                        fmaxf(fabsf(bf16_lo(qraw[h].y)), fabsf(bf16_hi(qraw[h].y))));
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(FULL, a, off));
+                        qe[h] = exp2i(f8_head_exp(a));
+                    }
+                }
+                // the three terms of head h are columns h, G + h, 2G + h
+                float v[N];
+#pragma unroll
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float w[16];
+                    tc5_ld<16>(tmem + (uint32_t)((k & 1) * N + c0) + lane_off, w);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[c0 + i] = w[i];
+                }
+#pragma unroll
+                for (int h = 0; h < GH; ++h) x[h] = ((v[h] + v[G + h]) + v[2 * G + h]) * qe[h];
+            } else {
                 float v[CH];
 #pragma unroll
                 for (int c0 = 0; c0 < GH; c0 += CH) {
@@ -994,8 +1214,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             for (int h = 0; h < GH; ++h) {
                 const float pv = fast_exp2(fmaxf(x[h] - m[h], -INFINITY));
                 l[h] += pv;
-                // int8 cache: the V row scale folds into the weight (MMA2 reads the codes)
-                pw[h] = QUANT ? pv * sv : pv;
+                // int8 / fp8 cache: the V row scale folds into the weight (MMA2 reads the codes)
+                pw[h] = SCALED ? pv * sv : pv;
             }
             if constexpr (C::PMN) {
                 // MN-major: the token's row of 64 columns, 16-byte chunks swizzled by token & 7
@@ -1024,17 +1244,25 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 const int chunk = (row & 63) >> 3, e = row & 7;
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(pw[h]);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(pw[h] - __bfloat162float(hi));
-                    const uint32_t off = (((chunk ^ (h & 7)) << 4) | (e << 1));  // N % 8 == 0
-                    *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + off) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(pb + (N + h) * 128 + off) = lo;
+                    const uint32_t off = (((chunk ^ (h & 7)) << 4) | (e << 1));  // NP % 8 == 0
+                    if constexpr (FP8) {  // f16 terms (the widened V is f16)
+                        const __half hi = __float2half_rn(pw[h]);
+                        const __half lo = __float2half_rn(pw[h] - __half2float(hi));
+                        *reinterpret_cast<__half*>(pb + h * 128 + off) = hi;
+                        *reinterpret_cast<__half*>(pb + (NP + h) * 128 + off) = lo;
+                    } else {
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(pw[h]);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(pw[h] - __bfloat162float(hi));
+                        *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + off) = hi;
+                        *reinterpret_cast<__nv_bfloat16*>(pb + (NP + h) * 128 + off) = lo;
+                    }
                 }
             }
-            // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2)
+            // V rows past the loaded boxes hold stale bytes: zero them (they meet p = 0 in MMA2;
+            // fp8: the converters write zeros there)
             const int br = paged ? p.box_rows : C::BOX_ROWS;
             const int loaded = ((n + br - 1) / br) * br;
-            if (h0 == 0 && row >= loaded) {
+            if (!FP8 && h0 == 0 && row >= loaded) {
                 using LY = Tc5Layout<C, PAGED>;
                 unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + (row >> 3) * LY::GSTR + (row & 7) * 128;
 #pragma unroll

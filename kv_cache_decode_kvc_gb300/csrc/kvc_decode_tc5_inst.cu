@@ -2,7 +2,8 @@
 // query-head group G is dispatched at run time.  Compiled once per cache mode, so no kernel
 // carries another mode's code: KVC_TC5_MODE = 0 contiguous (launch_decode_tc5_d128), 1 paged
 // pool (launch_decode_tc5p_d128), 2 rolling cache (launch_decode_tc5r_d128), 3 int8 cache
-// (launch_decode_tc5q_d128; group sizes up to 8, the converter warps leave fewer registers).
+// (launch_decode_tc5q_d128; group sizes up to 8, the converter warps leave fewer registers), 4 fp8
+// cache (launch_decode_tc5f_d128; group sizes up to 8).
 #include "kvc_decode_tc5.cuh"
 
 #ifndef KVC_TC5_MODE
@@ -14,6 +15,8 @@
 #define KVC_TC5_LAUNCHER launch_decode_tc5r_d128
 #elif KVC_TC5_MODE == 3
 #define KVC_TC5_LAUNCHER launch_decode_tc5q_d128
+#elif KVC_TC5_MODE == 4
+#define KVC_TC5_LAUNCHER launch_decode_tc5f_d128
 #else
 #define KVC_TC5_LAUNCHER launch_decode_tc5_d128
 #endif
@@ -23,7 +26,7 @@ namespace kvc {
 template <int G>
 static int launch_tc5_g(const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                         int* smem_out) {
-    using C = Tc5Cfg<G>;
+    using C = Tc5Cfg<G, KVC_TC5_MODE>;
     static PerDeviceOnce smem_attr;
     const int ea = smem_attr.run([] {
         return (int)cudaFuncSetAttribute(decode_tc5_kernel<G, KVC_TC5_MODE>,
@@ -56,7 +59,7 @@ int KVC_TC5_LAUNCHER(int G, const DecodeParams& p, const CUtensorMap* maps, cuda
         case 2: return launch_tc5_g<2>(p, maps, s, smem_out);
         case 4: return launch_tc5_g<4>(p, maps, s, smem_out);
         case 8: return launch_tc5_g<8>(p, maps, s, smem_out);
-#if KVC_TC5_MODE != 3
+#if KVC_TC5_MODE != 3 && KVC_TC5_MODE != 4
         case 16: return launch_tc5_g<16>(p, maps, s, smem_out);
         case 32: return launch_tc5_g<32>(p, maps, s, smem_out);
 #endif

@@ -32,7 +32,8 @@ struct kvc_cache {
                                      // paged: K, V, K, V with min(bs, 128)-row boxes
     bool paged;                      // K / V of a layer are pools [num_blocks, H_kv, bs, D]
     bool rolling;                    // T_max = window slots, position p in slot p mod T_max
-    bool quant;                      // int8 codes + fp32 row scales (q, out, new rows in dtype)
+    bool quant;                      // 8-bit codes + fp32 row scales (q, out, new rows in dtype)
+    bool fp8;                        // the codes are E4M3 (else int8)
     float* scales;                   // int8 cache: K / V row scales of layer l at 2l, 2l + 1
     size_t scale_stride;             // floats between consecutive scale arrays (256-byte aligned)
     int bs, max_blocks, num_blocks;  // paged geometry (T_max = max_blocks * bs)
@@ -136,6 +137,20 @@ bool make_q8_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_row
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over an fp8 cache with D = 128 (rows of 128 E4M3 codes): boxes of 128 bytes x box_rows
+// rows, 128-byte swizzle (the K tile is MMA1's operand as it lands).
+bool make_f8_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // a * b with overflow detection (all operands >= 0)
 bool mul_ok(uint64_t a, uint64_t b, uint64_t* r) {
     if (a != 0 && b > UINT64_MAX / a) return false;
@@ -160,7 +175,8 @@ int launch_decode(const kvc_cache* h, int layer, const kvc::DecodeParams& p, cud
         const CUtensorMap* maps = &h->tmaps[4 * (size_t)layer];
         e = h->paged     ? kvc::launch_decode_tc5p_d128(Gq, p, maps, s, &smem)
             : h->rolling ? kvc::launch_decode_tc5r_d128(Gq, p, maps, s, &smem)
-            : h->quant   ? kvc::launch_decode_tc5q_d128(Gq, p, maps, s, &smem)
+            : h->quant   ? (h->fp8 ? kvc::launch_decode_tc5f_d128(Gq, p, maps, s, &smem)
+                                   : kvc::launch_decode_tc5q_d128(Gq, p, maps, s, &smem))
                          : kvc::launch_decode_tc5_d128(Gq, p, maps, s, &smem);
     } else if (path == 2) {
         const CUtensorMap& tk = h->tmaps[4 * (size_t)layer];
@@ -257,6 +273,7 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
 // int8 cache: the layer's row-scale arrays for the quantizing writes
 void set_quant_scales(const kvc_cache* h, int layer, kvc::CopyParams& p) {
     if (!h->quant) return;
+    p.fp8 = h->fp8 ? 1 : 0;
     p.Ksc = h->scales + (size_t)(2 * layer) * h->scale_stride;
     p.Vsc = h->scales + (size_t)(2 * layer + 1) * h->scale_stride;
 }
@@ -334,7 +351,8 @@ int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, i
 }
 
 static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max,
-                         int dtype, int bs, int max_blocks, int num_blocks, bool quant = false) {
+                         int dtype, int bs, int max_blocks, int num_blocks, bool quant = false,
+                         bool fp8 = false) {
     const bool paged = bs > 0;
     if (!out) return KVC_EINVAL;
     *out = nullptr;
@@ -379,6 +397,7 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     h->paged = paged;
     h->rolling = false;
     h->quant = quant;
+    h->fp8 = quant && fp8;
     h->scale_stride = scale_stride;
     h->bs = paged ? bs : 1;
     h->max_blocks = paged ? max_blocks : 0;
@@ -426,7 +445,12 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
             void* kb = h->slab + (size_t)(2 * l) * h->layer_bytes;
             void* vb = h->slab + (size_t)(2 * l + 1) * h->layer_bytes;
             CUtensorMap* m4 = &h->tmaps[4 * (size_t)l];
-            if (quant)  // int8 rows of 128 bytes, unswizzled (widened to bf16 in the kernel)
+            if (quant && fp8)  // E4M3 rows of 128 bytes, 128-byte swizzled
+                ok = make_f8_tensor_map(&m4[0], kb, rows, box_small) &&
+                     make_f8_tensor_map(&m4[1], vb, rows, box_small) &&
+                     make_f8_tensor_map(&m4[2], kb, rows, box_full) &&
+                     make_f8_tensor_map(&m4[3], vb, rows, box_full);
+            else if (quant)  // int8 rows of 128 bytes, unswizzled (widened to bf16 in the kernel)
                 ok = make_q8_tensor_map(&m4[0], kb, rows, box_small) &&
                      make_q8_tensor_map(&m4[1], vb, rows, box_small) &&
                      make_q8_tensor_map(&m4[2], kb, rows, box_full) &&
@@ -472,6 +496,26 @@ int kvc_create_quantized(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
         return KVC_EUNSUPPORTED;
     }
     return rc;
+}
+
+int kvc_create_fp8(kvc_t* out, int layers, int B, int H_q, int H_kv, int D, int T_max, int dtype) {
+    if (!out) return KVC_EINVAL;
+    *out = nullptr;
+    // the tcgen05 kernel reads E4M3 tiles: bf16 queries, D = 128, up to 8 query heads per KV head
+    if (dtype != KVC_BF16 || D != 128 || H_kv < 1 || H_q % H_kv != 0 || H_q / H_kv > 8)
+        return KVC_EUNSUPPORTED;
+    const int rc = create_common(out, layers, B, H_q, H_kv, D, T_max, dtype, 0, 0, 0, true, true);
+    if (rc == KVC_OK && !(*out)->tc_ok) {  // no tensor maps: nothing can read this cache
+        kvc_destroy(*out);
+        *out = nullptr;
+        return KVC_EUNSUPPORTED;
+    }
+    return rc;
+}
+
+int kvc_get_cache_format(kvc_t h) {
+    if (!h) return -1;
+    return h->quant ? (h->fp8 ? KVC_CACHE_FP8 : KVC_CACHE_INT8) : KVC_CACHE_PLAIN;
 }
 
 int kvc_layer_scales(kvc_t h, int layer, float** Ks, float** Vs) {

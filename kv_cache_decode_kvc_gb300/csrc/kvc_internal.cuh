@@ -4,6 +4,8 @@
 
 #include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -111,8 +113,9 @@ struct CopyParams {
     const int32_t* table; // paged cache: [B, max_blocks] block table, else nullptr
     int bs, max_blocks, num_blocks;
     int rolling;          // rolling cache: position p in slot p mod T_max (lens may exceed T_max)
-    float* Ksc;           // int8 cache: row scales of K / V; the rows are quantized on write
+    float* Ksc;           // int8 / fp8 cache: row scales of K / V; the rows are quantized on write
     float* Vsc;
+    int fp8;              // 1: the codes are E4M3 (fp8 cache), 0: int8
 };
 
 // One launcher per (dtype, D) translation unit; G selects the instantiation.  Each returns
@@ -147,6 +150,9 @@ int launch_decode_tc5r_d128(int G, const DecodeParams& p, const CUtensorMap* map
                             int* smem_out);
 // ... and for an int8 cache (p.Ksc / p.Vsc set; maps over the int8 rows, no swizzle)
 int launch_decode_tc5q_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
+                            int* smem_out);
+// ... and for an fp8 cache (E4M3 codes and row scales; maps over the code rows, 128-byte swizzle)
+int launch_decode_tc5f_d128(int G, const DecodeParams& p, const CUtensorMap* maps, cudaStream_t s,
                             int* smem_out);
 constexpr int TC_BOX_ROWS = 32;
 constexpr int TC_FULL_ROWS = 128;
@@ -383,6 +389,71 @@ __device__ __forceinline__ void q8_store_row(const __nv_bfloat16* x, int8_t* cod
     }
     reinterpret_cast<uint32_t*>(codes)[lane] = packed;
     if (lane == 0) *scale = s;
+}
+
+// ---- fp8 (E4M3) cache: one fp32 scale per row, scale = max |x| / 448, code = E4M3 of x / scale
+// (IEEE fp32 division; round to nearest even, saturating at +-448; a zero row gets scale 0).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {  // a in the low byte
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t c2) {    // the two codes of the low 16 bits
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c2 & 0xFFFFu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+__device__ __forceinline__ float f8_row_scale(const __nv_bfloat16* x) {
+    float amax = 0.f;
+    const uint4* v = reinterpret_cast<const uint4*>(x);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const uint4 w = __ldg(v + i);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+    }
+    return __fdiv_rn(amax, 448.f);
+}
+// Warp-cooperative: lane l encodes elements 4l .. 4l+3 of a D = 128 row; lane 0 stores the scale.
+__device__ __forceinline__ void f8_store_row(const __nv_bfloat16* x, uint8_t* codes, float* scale, int lane) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(x) + lane);
+    const float f[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+    float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float s = __fdiv_rn(amax, 448.f);
+    uint32_t packed = 0;
+    if (s > 0.f)
+        packed = e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+                 (e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+    reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+    if (lane == 0) *scale = s;
+}
+// q of one head as three E4M3 terms: q = 2^e (t0 + t1 + t2).  e puts the head's largest |q| in
+// [128, 256) (the exponent of amax minus 7, clamped so 2^-e stays a normal fp32); the scaled
+// value v = q 2^-e is exact, t0 is its nearest code and t1, t2 those of the (exact) residues, so a
+// bf16 value within the codes' normal range is represented exactly.
+__device__ __forceinline__ int f8_head_exp(float amax) {
+    const int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+    const int e = amax > 0.f ? E - 7 : 0;
+    return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+// Eight scaled values -> their three E4M3 terms, 8 bytes each (value i in byte i).
+__device__ __forceinline__ void e4m3_split3(const float (&v)[8], uint2& t0, uint2& t1, uint2& t2) {
+    uint32_t c[3][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float a = v[2 * i], b = v[2 * i + 1];
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            c[t][i] = e4m3x2(a, b);
+            const float2 r = e4m3x2_value(c[t][i]);
+            a -= r.x;
+            b -= r.y;
+        }
+    }
+    t0 = make_uint2(c[0][0] | (c[0][1] << 16), c[0][2] | (c[0][3] << 16));
+    t1 = make_uint2(c[1][0] | (c[1][1] << 16), c[1][2] | (c[1][3] << 16));
+    t2 = make_uint2(c[2][0] | (c[2][1] << 16), c[2][2] | (c[2][3] << 16));
 }
 
 #endif  // __CUDACC__

@@ -20,6 +20,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "kvc.h")
 KVC_BF16, KVC_F32 = 0, 1
 KVC_OK, KVC_EINVAL, KVC_ENOMEM, KVC_ECUDA, KVC_ERANGE, KVC_EDEVICE, KVC_EUNSUPPORTED = range(7)
 KVC_DEV_BAD_LENS, KVC_DEV_WAIT_TIMEOUT, KVC_DEV_BAD_BLOCK = 1, 2, 4
+KVC_CACHE_PLAIN, KVC_CACHE_INT8, KVC_CACHE_FP8 = 0, 1, 2
 
 _lib = None
 
@@ -72,6 +73,8 @@ def load() -> ctypes.CDLL:
         "kvc_create_rolling": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
         "kvc_create_quantized": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
         "kvc_layer_scales": (I, [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]),
+        "kvc_create_fp8": (I, [ctypes.POINTER(P), I, I, I, I, I, I, I]),
+        "kvc_get_cache_format": (I, [P]),
         "kvc_append_multi": (I, [P, I, P, P, P, I, P]),
         "kvc_decode_attn_multi": (I, [P, I, P, P, P, I, P]),
         "kvc_decode_step_multi": (I, [P, I, P, P, P, P, P, I, P]),
@@ -171,6 +174,16 @@ def kvc_create_quantized(layers, B, H_q, H_kv, D, T_max, dtype) -> int:
     _check(load().kvc_create_quantized(ctypes.byref(h), layers, B, H_q, H_kv, D, T_max, dtype),
            "kvc_create_quantized")
     return h.value
+
+
+def kvc_create_fp8(layers, B, H_q, H_kv, D, T_max, dtype) -> int:
+    h = ctypes.c_void_p()
+    _check(load().kvc_create_fp8(ctypes.byref(h), layers, B, H_q, H_kv, D, T_max, dtype), "kvc_create_fp8")
+    return h.value
+
+
+def kvc_get_cache_format(h) -> int:
+    return int(load().kvc_get_cache_format(h))
 
 
 def kvc_layer_scales(h, layer):
@@ -392,7 +405,7 @@ def _wrap_device(ptr: int, shape, dtype):
 
     class _Iface:
         def __init__(self):
-            typestr = {torch.bfloat16: "<i2", torch.float32: "<f4", torch.int8: "|i1"}[dtype]
+            typestr = {torch.bfloat16: "<i2", torch.float32: "<f4", torch.int8: "|i1", torch.uint8: "|u1"}[dtype]
             self.__cuda_array_interface__ = {
                 "shape": tuple(shape), "typestr": typestr, "data": (ptr, False), "version": 2,
                 "strides": None,
@@ -447,19 +460,23 @@ class RollingKVCache(KVCache):
 
 
 class QuantKVCache(KVCache):
-    """Owns one int8 kvc handle: per layer, codes [B, H_kv, T_max, D] (int8) and row scales
-    [B, H_kv, T_max] (fp32) for K and V; q, out and new rows stay bf16."""
+    """Owns one int8 kvc handle (fp8=True: an E4M3 handle): per layer, codes [B, H_kv, T_max, D]
+    (int8, or uint8 E4M3 bit patterns) and row scales [B, H_kv, T_max] (fp32) for K and V; q,
+    out and new rows stay bf16."""
 
-    def __init__(self, layers, B, H_q, H_kv, D, T_max, dtype="bf16"):
+    def __init__(self, layers, B, H_q, H_kv, D, T_max, dtype="bf16", fp8=False):
         self.dtype_code = {"bf16": KVC_BF16, KVC_BF16: KVC_BF16}[dtype]
         self.layers, self.B, self.H_q, self.H_kv, self.D, self.T_max = layers, B, H_q, H_kv, D, T_max
-        self.h = kvc_create_quantized(layers, B, H_q, H_kv, D, T_max, self.dtype_code)
+        self.fp8 = fp8
+        create = kvc_create_fp8 if fp8 else kvc_create_quantized
+        self.h = create(layers, B, H_q, H_kv, D, T_max, self.dtype_code)
 
     def layer_views(self, layer):
-        """torch views (no copy): K codes, V codes (int8) and K scales, V scales (fp32)."""
+        """torch views (no copy): K codes, V codes (int8 / uint8) and K scales, V scales (fp32)."""
         import torch
         kp, vp = kvc_layer_ptrs(self.h, layer)
         ks, vs = kvc_layer_scales(self.h, layer)
         shape = (self.B, self.H_kv, self.T_max, self.D)
-        return (_wrap_device(kp, shape, torch.int8), _wrap_device(vp, shape, torch.int8),
+        cdt = torch.uint8 if self.fp8 else torch.int8
+        return (_wrap_device(kp, shape, cdt), _wrap_device(vp, shape, cdt),
                 _wrap_device(ks, shape[:3], torch.float32), _wrap_device(vs, shape[:3], torch.float32))
