@@ -19,88 +19,103 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvc_oracle.c")
 _SO = os.path.join(_HERE, "libkvc_oracle.so")
+# the same source with the planted mistakes compiled in (tests of the pins only)
+_SO_PLANTED = os.path.join(_HERE, "libkvc_oracle_planted.so")
 
 BF16, F32 = 0, 1
 _lib = None
+_lib_planted = None
+_planted_on = False
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (OpenMP when the compiler has it).  Returns the .so path."""
-    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
-        return _SO
-    tmp = _SO + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+def _compile(out: str, defines) -> None:
+    tmp = out + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", *defines, "-o", tmp, _SRC, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(tmp, _SO)
+    os.replace(tmp, out)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when the compiler has it), and its planted-mistake
+    variant for the pin tests.  Returns the oracle's .so path."""
+    for out, defs in ((_SO, []), (_SO_PLANTED, ["-DORACLE_PLANTED"])):
+        if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+            _compile(out, defs)
     return _SO
 
 
 def lib() -> ctypes.CDLL:
-    global _lib
+    """The oracle library (its planted-mistake build while a planted_fault context is open)."""
+    global _lib, _lib_planted
     if _lib is None:
         build()
-        L = ctypes.CDLL(_SO)
-        P, I, U64, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64
-        L.oracle_kv_bytes.restype = U64
-        L.oracle_kv_bytes.argtypes = [I64] * 6
-        L.oracle_kv_bytes_ragged.restype = U64
-        L.oracle_kv_bytes_ragged.argtypes = [I64, I64, I64, I64, P, I]
-        L.oracle_append.restype = I
-        L.oracle_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
-        L.oracle_prefill_write.restype = I
-        L.oracle_prefill_write.argtypes = [P, P, P, P, I, P, I, I, I, I, I]
-        L.oracle_decode_attn.restype = I
-        L.oracle_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
-        L.oracle_layer_full.restype = None
-        L.oracle_layer_full.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P]
-        L.oracle_layer_incremental.restype = None
-        L.oracle_layer_incremental.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P, P, P]
-        L.oracle_paged_append.restype = I
-        L.oracle_paged_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I]
-        L.oracle_paged_prefill_write.restype = I
-        L.oracle_paged_prefill_write.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I]
-        L.oracle_paged_decode_attn.restype = I
-        L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P]
-        L.oracle_window_decode_attn.restype = I
-        L.oracle_window_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
-        L.oracle_rolling_append.restype = I
-        L.oracle_rolling_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
-        L.oracle_rolling_decode_attn.restype = I
-        L.oracle_rolling_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
-        L.oracle_append_multi.restype = I
-        L.oracle_append_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
-        L.oracle_decode_multi.restype = I
-        L.oracle_decode_multi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
-        L.oracle_quantize_rows.restype = None
-        L.oracle_quantize_rows.argtypes = [P, I, I, I, P, P]
-        L.oracle_quant_append.restype = I
-        L.oracle_quant_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
-        L.oracle_quant_prefill_write.restype = I
-        L.oracle_quant_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
-        L.oracle_quant_decode_attn.restype = I
-        L.oracle_quant_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
-        L.oracle_e4m3_value.restype = ctypes.c_double
-        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
-        L.oracle_e4m3_encode.restype = ctypes.c_uint8
-        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
-        L.oracle_fp8_quantize_rows.restype = None
-        L.oracle_fp8_quantize_rows.argtypes = [P, I, I, I, P, P]
-        L.oracle_fp8_append.restype = I
-        L.oracle_fp8_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
-        L.oracle_fp8_prefill_write.restype = I
-        L.oracle_fp8_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
-        L.oracle_fp8_decode_attn.restype = I
-        L.oracle_fp8_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
-        L.oracle_set_fault.restype = None
-        L.oracle_set_fault.argtypes = [I]
-        L.oracle_get_fault.restype = I
-        L.oracle_set_threads.restype = I
-        L.oracle_set_threads.argtypes = [I]
-        _lib = L
-    return _lib
+        _lib = _load(_SO)
+        _lib_planted = _load(_SO_PLANTED)
+        _lib_planted.oracle_set_fault.restype = None
+        _lib_planted.oracle_set_fault.argtypes = [ctypes.c_int]
+        _lib_planted.oracle_get_fault.restype = ctypes.c_int
+    return _lib_planted if _planted_on else _lib
+
+
+def _load(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    P, I, U64, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_int64
+    L.oracle_kv_bytes.restype = U64
+    L.oracle_kv_bytes.argtypes = [I64] * 6
+    L.oracle_kv_bytes_ragged.restype = U64
+    L.oracle_kv_bytes_ragged.argtypes = [I64, I64, I64, I64, P, I]
+    L.oracle_append.restype = I
+    L.oracle_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    L.oracle_prefill_write.restype = I
+    L.oracle_prefill_write.argtypes = [P, P, P, P, I, P, I, I, I, I, I]
+    L.oracle_decode_attn.restype = I
+    L.oracle_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+    L.oracle_layer_full.restype = None
+    L.oracle_layer_full.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P, P, P]
+    L.oracle_layer_incremental.restype = None
+    L.oracle_layer_incremental.argtypes = [P, I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+    L.oracle_paged_append.restype = I
+    L.oracle_paged_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I]
+    L.oracle_paged_prefill_write.restype = I
+    L.oracle_paged_prefill_write.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I]
+    L.oracle_paged_decode_attn.restype = I
+    L.oracle_paged_decode_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P]
+    L.oracle_window_decode_attn.restype = I
+    L.oracle_window_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
+    L.oracle_rolling_append.restype = I
+    L.oracle_rolling_append.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    L.oracle_rolling_decode_attn.restype = I
+    L.oracle_rolling_decode_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+    L.oracle_append_multi.restype = I
+    L.oracle_append_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
+    L.oracle_decode_multi.restype = I
+    L.oracle_decode_multi.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
+    L.oracle_quantize_rows.restype = None
+    L.oracle_quantize_rows.argtypes = [P, I, I, I, P, P]
+    L.oracle_quant_append.restype = I
+    L.oracle_quant_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+    L.oracle_quant_prefill_write.restype = I
+    L.oracle_quant_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
+    L.oracle_quant_decode_attn.restype = I
+    L.oracle_quant_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+    L.oracle_e4m3_value.restype = ctypes.c_double
+    L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_fp8_quantize_rows.restype = None
+    L.oracle_fp8_quantize_rows.argtypes = [P, I, I, I, P, P]
+    L.oracle_fp8_append.restype = I
+    L.oracle_fp8_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I]
+    L.oracle_fp8_prefill_write.restype = I
+    L.oracle_fp8_prefill_write.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I]
+    L.oracle_fp8_decode_attn.restype = I
+    L.oracle_fp8_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+    L.oracle_set_threads.restype = I
+    L.oracle_set_threads.argtypes = [I]
+    return L
 
 
 def _ptr(a: np.ndarray):
@@ -386,11 +401,16 @@ class planted_fault:
         self.which = which
 
     def __enter__(self):
-        lib().oracle_set_fault(self.which)
+        global _planted_on
+        lib()
+        _lib_planted.oracle_set_fault(self.which)
+        _planted_on = True
         return self
 
     def __exit__(self, *exc):
-        lib().oracle_set_fault(0)
+        global _planted_on
+        _lib_planted.oracle_set_fault(0)
+        _planted_on = False
         return False
 
 

@@ -37,10 +37,17 @@
 #define OR_BF16 0
 #define OR_F32 1
 
-/* Planted-mistake switch for the tests that show the pins have teeth.  0 = correct. */
+/* Planted mistakes, for the tests that show the pins have teeth.  They exist only in a second
+ * build of this file (-DORACLE_PLANTED, libkvc_oracle_planted.so) that the tests switch to while
+ * a mistake is planted; in the oracle itself PLANTED(n) is the constant 0 and no branch is left. */
+#ifdef ORACLE_PLANTED
 static int g_fault = 0;
 void oracle_set_fault(int which) { g_fault = which; }
 int oracle_get_fault(void) { return g_fault; }
+#define PLANTED(n) (g_fault == (n))
+#else
+#define PLANTED(n) 0
+#endif
 
 static int g_threads = 1;
 /* Number of host threads the decode routine may use (1 = plain single-threaded loop). */
@@ -101,7 +108,7 @@ int oracle_append(void* Kc, void* Vc, const void* k_new, const void* v_new, cons
             continue;
         }
         int slot = L - 1;
-        if (g_fault == 3) slot = L; /* planted: off-by-one slot */
+        if (PLANTED(3)) slot = L; /* planted: off-by-one slot */
         if (slot >= T_max) continue;
         for (int h = 0; h < H_kv; ++h) {
             size_t dst = (((size_t)b * H_kv + h) * T_max + slot) * row;
@@ -146,8 +153,8 @@ int oracle_prefill_write(void* Kc, void* Vc, const void* K, const void* V, int T
 static void decode_row_f64(const double* q, const double* K, const double* V, int L, int D,
                            size_t ld, double* o, double* s /* scratch, L doubles */) {
     double scale = 1.0 / sqrt((double)D);
-    if (g_fault == 2) scale = 1.0 / (double)D; /* planted: the garbled "/d_k" reading */
-    int Lr = (g_fault == 4) ? L - 1 : L;       /* planted: new token left out */
+    if (PLANTED(2)) scale = 1.0 / (double)D; /* planted: the garbled "/d_k" reading */
+    int Lr = (PLANTED(4)) ? L - 1 : L;       /* planted: new token left out */
     if (Lr < 1) Lr = 1;
     for (int t = 0; t < Lr; ++t) {
         double acc = 0.0;
@@ -172,7 +179,7 @@ static void decode_row_f64(const double* q, const double* K, const double* V, in
 /* KV head read by query head j: [W1D4] §3.4, floor(j / (H_q / H_kv)). */
 static int kv_head_of(int j, int H_q, int H_kv) {
     int g = H_q / H_kv;
-    if (g_fault == 1) return j % H_kv; /* planted: interleaved ("repeat") grouping */
+    if (PLANTED(1)) return j % H_kv; /* planted: interleaved ("repeat") grouping */
     return j / g;
 }
 
@@ -245,7 +252,7 @@ static int paged_row_ok(const int32_t* table, int b, int L, int L_min, int bs, i
 static size_t paged_row_offset(const int32_t* table, int b, int h, int t, int H_kv, int bs,
                                int max_blocks) {
     int e = table[(size_t)b * max_blocks + t / bs];
-    if (g_fault == 5) /* planted: token-major block ([bs, H_kv] instead of [H_kv, bs]) */
+    if (PLANTED(5)) /* planted: token-major block ([bs, H_kv] instead of [H_kv, bs]) */
         return ((size_t)e * bs + (size_t)(t % bs)) * H_kv + h;
     return (((size_t)e * H_kv + h) * bs + (size_t)(t % bs));
 }
@@ -365,7 +372,7 @@ static void quant_row(const void* x, int dtype, size_t off, int D, int8_t* codes
         if (a > amax) amax = a;
     }
     float s = amax / 127.0f;
-    if (g_fault == 8) s = amax / 128.0f; /* planted: scale off by one level */
+    if (PLANTED(8)) s = amax / 128.0f; /* planted: scale off by one level */
     *scale = s;
     for (int d = 0; d < D; ++d) {
         float c = 0.0f;
@@ -511,7 +518,7 @@ uint8_t oracle_e4m3_encode(float x) {
     if (v - a < b - v) c = lo;
     else if (v - a > b - v) c = hi;
     else c = (lo & 1) ? hi : lo; /* a tie: the even code */
-    if (g_fault == 9 && v - a == b - v) c = hi; /* planted: ties away from zero */
+    if (PLANTED(9) && v - a == b - v) c = hi; /* planted: ties away from zero */
     return sign | (uint8_t)c;
 }
 
@@ -522,7 +529,7 @@ static void fp8_row(const void* x, int dtype, size_t off, int D, uint8_t* codes,
         if (a > amax) amax = a;
     }
     float s = amax / 448.0f;
-    if (g_fault == 10) s = amax / 240.0f; /* planted: the range of the other E4M3 variant */
+    if (PLANTED(10)) s = amax / 240.0f; /* planted: the range of the other E4M3 variant */
     *scale = s;
     for (int d = 0; d < D; ++d) codes[d] = s > 0.0f ? oracle_e4m3_encode(load_f32(x, dtype, off + d) / s) : 0;
 }
@@ -672,7 +679,7 @@ int oracle_decode_multi(const void* q, const void* Kc, const void* Vc, const int
             continue;
         }
         int visible = L - T_q + i + 1; /* keys 0 .. L - T_q + i */
-        if (g_fault == 7) visible = i + 1; /* planted: upper-left aligned causal mask */
+        if (PLANTED(7)) visible = i + 1; /* planted: upper-left aligned causal mask */
         int h = kv_head_of(j, H_q, H_kv);
         double* qd = (double*)malloc(sizeof(double) * D);
         double* Kd = (double*)malloc(sizeof(double) * (size_t)visible * D);
@@ -703,7 +710,7 @@ int oracle_decode_multi(const void* q, const void* Kc, const void* Vc, const int
 /* First position of the window of a sequence of length L. */
 static int window_start(int L, int W) {
     int t0 = L - W;
-    if (g_fault == 6) t0 = L - W - 1; /* planted: one position too many */
+    if (PLANTED(6)) t0 = L - W - 1; /* planted: one position too many */
     return t0 > 0 ? t0 : 0;
 }
 

@@ -318,3 +318,12 @@ def test_planted_missing_new_token_is_caught():
     with oracle.planted_fault(4):
         assert _fails(test_newest_slot_is_attended)
         assert _fails(lambda: test_incremental_equals_full_mha_gqa_mqa(2))
+
+
+def test_the_oracle_itself_carries_no_planted_mistakes():
+    """The planted mistakes live only in the separate test build; the oracle the other tests
+    trust has no switch for them."""
+    import ctypes
+    oracle.lib()
+    assert not hasattr(ctypes.CDLL(oracle._SO), "oracle_set_fault")
+    assert hasattr(ctypes.CDLL(oracle._SO_PLANTED), "oracle_set_fault")
