@@ -78,13 +78,21 @@ struct Tc5Cfg {
     static constexpr int BUDGET = 232448;               // opt-in maximum per CTA (227 KB)
     static constexpr int FIXED = OPB_BYTES + 2 * PBUF + VW_BYTES + MERGE_FLOATS * 4 + PREFIX_BYTES +
                                  RED_BYTES + MISC_BYTES + ALIGN_PAD;
-    static constexpr int NST_A = (BUDGET - FIXED) / STAGE_BYTES;
-    static constexpr int NST = NST_A > 4 ? 4 : NST_A;
-    static constexpr int SMEM = NST * STAGE_BYTES + FIXED;
+    // Groups of 16+ heads on a contiguous or rolling cache keep K and V in separate rings of
+    // 16-bit tiles: a K slot is refilled as soon as MMA1 has read it, a V slot once MMA2 has, so
+    // the V loads get two tiles of lead where one joint ring (two stages fit) gives them one.
+    static constexpr bool SPLIT = PMN && (MODE_ == 0 || MODE_ == 2);
+    static constexpr int NSLOT = (BUDGET - FIXED) / TILE_BYTES;
+    static constexpr int NV = SPLIT ? 2 : 0;                         // V slots
+    static constexpr int NST_A = SPLIT ? NSLOT - NV : (BUDGET - FIXED) / STAGE_BYTES;
+    static constexpr int NST = NST_A > 4 ? 4 : NST_A;                // stages (SPLIT: K slots)
+    static constexpr int RING_BYTES = SPLIT ? (NST + NV) * TILE_BYTES : NST * STAGE_BYTES;
+    static constexpr int SMEM = RING_BYTES + FIXED;
     // S^T buffers [0, N) and [N, 2N); O^T buffers (hi and lo columns) [2N, 2N + N2), [2N + N2, 2N + 2 N2)
     static constexpr int TMEM_NEED = 2 * N + 2 * N2;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : 256));
     static_assert(NST >= 2, "ring too shallow");
+    static_assert(!SPLIT || NST >= 3, "split rings: at least 3 K slots");
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(HSPLIT == 1 || GH % 8 == 0, "head slices start on a swizzle row group");
     static_assert(!PMN || NP <= 32, "P_hi and P_lo share one 64-column row");
@@ -312,6 +320,28 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     }
 }
 
+// Split rings: one tensor's tile (K or V, 16-bit, contiguous or rolling cache) into a 32 KB slot:
+// a whole tile in one 3-D copy, a partial tile in 32-row 2-D boxes per column block.
+template <class C, int TT>
+__device__ __forceinline__ void issue_one_tc5(const DecodeParams& p, const TileCursor<TT>& c, uint32_t dst,
+                                              uint64_t* bar, uint64_t pol, const CUtensorMap* tm,
+                                              const CUtensorMap* tmf) {
+    const int n = c.n();
+    const bool full = n == TT;
+    const int nbox = full ? 1 : (n + C::BOX_ROWS - 1) / C::BOX_ROWS;
+    const int row0 = (int)(((size_t)c.it.b * p.H_kv + c.it.h) * p.T_max + c.t);
+    mbar_arrive_expect_tx(bar, (uint32_t)(full ? C::TILE_BYTES : nbox * C::BOX_ROWS * C::ROWB));
+    if (full) {
+        tma_load_3d(dst, tmf, row0, bar, pol);
+    } else {
+#pragma unroll
+        for (int hf = 0; hf < C::HALVES; ++hf)
+            for (int bx = 0; bx < nbox; ++bx)
+                tma_load_2d(dst + hf * C::HALF_BYTES + bx * C::BOX_ROWS * 128, tm, hf * 64, row0 + bx * C::BOX_ROWS,
+                            bar, pol);
+    }
+}
+
 // 16 int8 values -> 16 bf16, exactly, with full-rate integer and bf16x2 operations: for the
 // byte x = l - 128 s (l its low 7 bits, s its sign bit), the bf16 with bits 0x43:l is 128 + l and
 // the one with bits 0x43:(s << 7) is 128 + 128 s; their difference is x, exactly representable.
@@ -399,8 +429,10 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = smem;
-    unsigned char* vw = ring + NST * C::STAGE_BYTES;          // fp8 cache: f16 V working tiles [2]
-    unsigned char* qsw = vw + C::VW_BYTES;                    // q, [N][D] K-major swizzled
+    unsigned char* vw = ring + C::RING_BYTES;                 // fp8 cache: f16 V working tiles [2]
+    unsigned char* qsw = ring + C::RING_BYTES + C::VW_BYTES;  // q, [N][D] K-major swizzled
+    // split rings (groups of 16+): K slots [0, NST), then V slots [NST, NST + NV), one tile each
+    unsigned char* vring = ring + NST * C::TILE_BYTES;
     unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][2 blocks][2N rows][128 B]
     float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
     int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
@@ -431,6 +463,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     uint64_t* conv_full = append_bar + 1;  // [NST] int8 cache: the stage's tiles are bf16 now
     uint64_t* vw_full = conv_full + NST;   // [2] fp8 cache: V working tile written (converters)
     uint64_t* vw_empty = vw_full + 2;      // [2] fp8 cache: V working tile read (MMA2 commit)
+    uint64_t* sv_full = vw_empty + 2;      // [NV] split rings: V slot landed
+    uint64_t* sv_empty = sv_full + 2;      // [NV] split rings: V slot read by MMA2
+    int* vissued = reinterpret_cast<int*>(sv_empty + 2);  // [NV] V copies issued per slot (abort drain)
 
     // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
     // CTAs take SMs as ours exit) but waits in griddepcontrol.wait until this grid is complete.
@@ -458,6 +493,12 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&vw_full[i], C::NCONV * 32);
                 mbar_init(&vw_empty[i], 1);
+            }
+        if constexpr (C::SPLIT)
+            for (int i = 0; i < C::NV; ++i) {
+                mbar_init(&sv_full[i], 1);
+                mbar_init(&sv_empty[i], 1);
+                vissued[i] = 0;
             }
         *abort_flag = 0;
         *last_flag = 0;
@@ -515,9 +556,19 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         if (early)
             while (pref.valid && npre < NST && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
                 if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
-                if (lane == 0) issued[npre] += 1;
-                issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf, ent,
-                                             lane);
+                if constexpr (C::SPLIT) {
+                    issued[npre] += 1;
+                    issue_one_tc5<C, TT>(p, pref, ring_s + npre * C::TILE_BYTES, &full_bar[npre], pol, &tmK, &tmKf);
+                    if (npre < C::NV) {
+                        vissued[npre] += 1;
+                        issue_one_tc5<C, TT>(p, pref, smem_addr(vring) + npre * C::TILE_BYTES, &sv_full[npre], pol,
+                                             &tmV, &tmVf);
+                    }
+                } else {
+                    if (lane == 0) issued[npre] += 1;
+                    issue_tile_tc5<C, TT, MODE>(p, pref, ring_s, full_bar, npre, pol, &tmK, &tmV, &tmKf, &tmVf, ent,
+                                                 lane);
+                }
                 pref.advance();
                 ++npre;
             }
@@ -560,7 +611,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     const uint32_t vw_s = smem_addr(vw);
     auto issue_mma2 = [&](int k, int st, uint32_t tm) {
         // V: the stage's tile, or (fp8) the f16 working tile k & 1
-        const uint64_t dV0 = smem_desc_sw128(FP8 ? vw_s : ring_s + C::TILE_BYTES, LY::HSTR, LY::GSTR);
+        const uint64_t dV0 = smem_desc_sw128(FP8 ? vw_s : (C::SPLIT ? smem_addr(vring) : ring_s + C::TILE_BYTES),
+                                             LY::HSTR, LY::GSTR);
         // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
         // leading offset is never stepped over)
         const uint32_t pbuf_s = smem_addr(pbuf);
@@ -570,7 +622,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         const uint32_t pb = (uint32_t)((k & 1) * C::PBUF);
 #pragma unroll
         for (int kk = 0; kk < TS; ++kk) {
-            const uint32_t voff = (uint32_t)((FP8 ? (k & 1) * C::TILE_BYTES : st * C::STAGE_BYTES) +
+            const uint32_t voff = (uint32_t)((FP8 ? (k & 1) * C::TILE_BYTES
+                                                  : C::SPLIT ? (k % C::NV) * C::TILE_BYTES : st * C::STAGE_BYTES) +
                                              kk * 2 * LY::GSTR);
             const uint32_t poff = C::PMN ? pb + (uint32_t)(kk * 2048)
                                          : pb + (uint32_t)((kk >> 2) * C::PBLOCK + (kk & 3) * 32);
@@ -579,6 +632,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         tc5_commit(&o_full[k & 1]);
         if constexpr (FP8)
             tc5_commit(&vw_empty[k & 1]);  // the working tile is free (the stage was freed earlier)
+        else if constexpr (C::SPLIT)
+            tc5_commit(&sv_empty[k % C::NV]);  // the V slot is consumed (MMA1 freed the K slot)
         else
             tc5_commit(&empty_bar[st]);  // K/V of the stage are consumed
         *mma_issued += 1;
@@ -606,6 +661,64 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 if constexpr (PAGED) if (pref.valid) ent = tile_block<TT>(p, pref, lane);
             };
             bool ok = true;
+            if constexpr (C::SPLIT) {
+                // K slots: tile k in slot k % NST, refilled with tile k + NST once MMA1(k) has read
+                // it; V slots: tile k in slot k % NV, refilled with tile k + NV once MMA2(k) has.
+                // This thread issues MMA2 (its V wait included) between the two refills.
+                auto ready = [&](const TileCursor<TT>& c) {
+                    return !(fused && nrow.in_tile(p, c.it.b, c.it.L, c.t, c.n())) ||
+                           mbar_wait(append_bar, 0u, abort_flag, p.err);
+                };
+                TileCursor<TT> vp;  // V cursor
+                vp.init(prefix, B, H_kv, r0, r1);
+                const int nvpre = npre < C::NV ? npre : C::NV;
+                for (int i = 0; i < nvpre && vp.valid; ++i) vp.advance();
+                for (int st = npre; st < NST && pref.valid && ok; ++st) {
+                    ok = ready(pref);
+                    if (!ok) break;
+                    issued[st] += 1;
+                    issue_one_tc5<C, TT>(p, pref, ring_s + st * C::TILE_BYTES, &full_bar[st], pol, &tmK, &tmKf);
+                    pref.advance();
+                }
+                for (int sv = nvpre; sv < C::NV && vp.valid && ok; ++sv) {
+                    ok = ready(vp);
+                    if (!ok) break;
+                    vissued[sv] += 1;
+                    issue_one_tc5<C, TT>(p, vp, smem_addr(vring) + sv * C::TILE_BYTES, &sv_full[sv], pol, &tmV, &tmVf);
+                    vp.advance();
+                }
+                TileCursor<TT> mc;
+                mc.init(prefix, B, H_kv, r0, r1);
+                for (int k = 0; ok && mc.valid; ++k) {
+                    const int sk = k % NST, sv = k % C::NV;
+                    if (pref.valid) {
+                        ok = mbar_wait(&empty_bar[sk], (uint32_t)((k / NST) & 1), abort_flag, p.err) && ready(pref);
+                        if (ok) {
+                            issued[sk] += 1;
+                            issue_one_tc5<C, TT>(p, pref, ring_s + sk * C::TILE_BYTES, &full_bar[sk], pol, &tmK, &tmKf);
+                            pref.advance();
+                        }
+                    }
+                    ok = ok && mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
+                         mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err) &&
+                         mbar_wait(&sv_full[sv], (uint32_t)((k / C::NV) & 1), abort_flag, p.err);
+                    if (ok) {
+                        tc5_fence_after();
+                        if (k == 0) tmem = *tmem_slot;
+                        issue_mma2(k, sk, tmem);
+                    }
+                    if (ok && vp.valid) {
+                        ok = mbar_wait(&sv_empty[sv], (uint32_t)((k / C::NV) & 1), abort_flag, p.err) && ready(vp);
+                        if (ok) {
+                            vissued[sv] += 1;
+                            issue_one_tc5<C, TT>(p, vp, smem_addr(vring) + sv * C::TILE_BYTES, &sv_full[sv], pol,
+                                                 &tmV, &tmVf);
+                            vp.advance();
+                        }
+                    }
+                    mc.advance();
+                }
+            } else {
             // the rest of the ring's first pass: those stages are free
             for (int st = npre; st < NST && pref.valid; ++st) {
                 ok = append_ready();
@@ -654,6 +767,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     if (ok) issue_next(s);
                     if (++s == NST) { s = 0; ph ^= 1u; }
                 }
+            }
             }
         }
     } else if (warp == 1) {
@@ -781,13 +895,16 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                         const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + kk * 32);
                         tc5_mma_f8(tS, dK0 + (off >> 4), dQ0 + ((uint32_t)(kk * 32) >> 4), IDESC1, kk > 0 ? 1u : 0u);
                     } else {
-                        const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + (kk >> 2) * LY::HSTR + (kk & 3) * 32);
+                        // (split rings: K slots of one tile each)
+                        const uint32_t off = (uint32_t)(s * (C::SPLIT ? C::TILE_BYTES : C::STAGE_BYTES) +
+                                                        (kk >> 2) * LY::HSTR + (kk & 3) * 32);
                         const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
                         tc5_mma(tS, dK0 + (off >> 4), dQ0 + (qoff >> 4), IDESC1, kk > 0 ? 1u : 0u);
                     }
                 }
                 tc5_commit(&s_full[k & 1]);
                 if constexpr (FP8) tc5_commit(&empty_bar[s]);  // K read (the converters arrive for V)
+                if constexpr (C::SPLIT) tc5_commit(&empty_bar[s]);  // split rings: the K slot is free
                 *mma1_issued += 1;
             }
             __syncwarp();
@@ -1264,7 +1381,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             const int loaded = ((n + br - 1) / br) * br;
             if (!FP8 && h0 == 0 && row >= loaded) {
                 using LY = Tc5Layout<C, PAGED>;
-                unsigned char* vt = ring + s * C::STAGE_BYTES + C::TILE_BYTES + (row >> 3) * LY::GSTR + (row & 7) * 128;
+                unsigned char* vt = (C::SPLIT ? vring + (k % C::NV) * C::TILE_BYTES : ring + s * C::STAGE_BYTES + C::TILE_BYTES) +
+                                    (row >> 3) * LY::GSTR + (row & 7) * 128;
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf)
 #pragma unroll
@@ -1328,6 +1446,14 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 while (!mbar_try_wait(&full_bar[s], par) && global_ns() - t0 < WAIT_LIMIT_NS) {
                 }
             }
+            if constexpr (C::SPLIT)
+                for (int v = 0; v < C::NV; ++v) {
+                    if (vissued[v] == 0) continue;
+                    const uint32_t par = (uint32_t)((vissued[v] - 1) & 1);
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(&sv_full[v], par) && global_ns() - t0 < WAIT_LIMIT_NS) {
+                    }
+                }
         }
         if (tid == 32 && *mma_issued > 0) {
             const int j = *mma_issued - 1;
