@@ -112,10 +112,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)2u << 61;
     return d;
 }
+// fp8 cache with groups of up to 4 heads: one more warp, which issues MMA2 alone (the MMA warp then
+// issues only MMA1; each tcgen05.mma holds its issuing thread ~90 cycles, and the two contractions
+// plus their waits exceeded an fp8 tile's time on one thread)
+template <int G, int MODE>
+__host__ __device__ constexpr bool tc5_mma2_warp() {
+    return MODE == 4 && G <= 4;
+}
 // Threads of the kernel instantiation: a quantized cache adds the converter warps.
 template <int G, int MODE>
 __host__ __device__ constexpr int tc5_threads() {
-    return Tc5Cfg<G, MODE>::NTHREADS + ((MODE == 3 || MODE == 4) ? Tc5Cfg<G, MODE>::NCONV * 32 : 0);
+    return Tc5Cfg<G, MODE>::NTHREADS + ((MODE == 3 || MODE == 4) ? Tc5Cfg<G, MODE>::NCONV * 32 : 0) +
+           (tc5_mma2_warp<G, MODE>() ? 32 : 0);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness (0 = K-major,
@@ -422,6 +430,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     using T = __nv_bfloat16;
     constexpr bool PAGED = MODE == 1, ROLL = MODE == 2, QUANT = MODE == 3, FP8 = MODE == 4;
     constexpr bool SCALED = QUANT || FP8;  // rows carry fp32 scales (K: scores, V: weights)
+    constexpr bool DED2 = tc5_mma2_warp<G, MODE>();  // a warp of its own issues MMA2
     constexpr int D = C::D, N = C::N, NP = C::NP, TT = C::TT, NST = C::NST, TS = TT / 16;
     constexpr int KS = FP8 ? D / 32 : D / 16;  // MMA1 k-steps of 32 bytes
 
@@ -866,7 +875,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             }
             if (FP8 && !cur.valid) {
                 // the last tile's MMA2 (MMA1 runs one tile ahead of MMA2 here)
-                if (k > 0 && alive) mma2_here(k - 1);
+                if (!DED2 && k > 0 && alive) mma2_here(k - 1);
                 break;
             }
             if (!cur.valid || !alive) break;
@@ -910,10 +919,32 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
             // fp8: MMA2 of the previous tile after MMA1 of this one, so the scores run a tile ahead
             // of the weights (MMA1 of a tile is four instructions; the stage does not wait for MMA2)
-            if (FP8 && k > 0 && alive) mma2_here(k - 1);
+            if (FP8 && !DED2 && k > 0 && alive) mma2_here(k - 1);
             s_prev = s;
             cur.advance();
             if (++s == NST) { s = 0; ph ^= 1u; }
+        }
+    } else if (DED2 && warp == 2 + C::NW + C::NEPI + C::NCONV) {
+        // ======================================================= MMA2 issue (fp8, groups <= 4)
+        // MMA2 of each tile once its weights, its O^T buffer and its f16 V working tile are ready
+        // (lane 0 issues; the warp follows its verdict)
+        TileCursor<TT> mc;
+        mc.init(prefix, B, H_kv, r0, r1);
+        bool ok = true;
+        for (int k = 0; ok && mc.valid; ++k) {
+            if (lane == 0) {
+                ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
+                     mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err) &&
+                     mbar_wait(&vw_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
+                if (ok) {
+                    tc5_fence_after();
+                    // written by warp 1's allocation before the weights of tile 0 existed
+                    if (k == 0) tmem = *tmem_slot;
+                    issue_mma2(k, 0, tmem);
+                }
+            }
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            mc.advance();
         }
     } else if (FP8 && warp >= 2 + C::NW + C::NEPI) {
         // ======================================================= E4M3 V -> f16 converters
