@@ -263,23 +263,30 @@ int kvc_get_paged_shape(kvc_t h, int* num_blocks, int* block_size, int* max_bloc
 int kvc_get_shape(kvc_t h, int* layers, int* B, int* H_q, int* H_kv, int* D, int* T_max,
                   int* dtype);
 
-/* Split-T partition used by the attention kernel (host copy of the device arithmetic, for
+/* Split-T partition used by the attention kernels (host copy of the device arithmetic, for
  * tests).  The B*H_kv (sequence, KV head) streams are laid end to end, stream u = b*H_kv + h
- * holding lens[b] tokens; with W tokens in total, CTA i of P takes positions
- * [floor(i*W/P), floor((i+1)*W/P)).  Returns the CTA that owns position x (0 <= x < W). */
-int kvc_plan_cta_of(int64_t x, int64_t W, int P);
+ * holding lens[b] tokens, and each stream is cut into units of `grain` tokens (its last unit
+ * may be partial); with U units in total, CTA i of P takes units [floor(i*U/P), floor((i+1)*U/P)).
+ * So every CTA holds floor(U/P) or ceil(U/P) units and every cut falls on a unit boundary of its
+ * stream.  The kernels use grain 128 (one tcgen05 tile: no tile is shared by two CTAs), except
+ * that query groups of 16 or 32 heads whose split streams are merged inside the kernel
+ * (combine_mode 0) use the plain token split: grain 1, or a paged cache's block size.
+ * kvc_plan_grain(G, combine_mode, block_size) returns it (block_size 1 for a contiguous cache;
+ * -1 for bad arguments).  kvc_plan_cta_of returns the CTA that owns unit x (0 <= x < U), -1 for
+ * bad arguments. */
+int kvc_plan_grain(int G, int combine_mode, int block_size);
+int kvc_plan_cta_of(int64_t x, int64_t U, int P);
 
 /* The partition the attention kernels use, on the host (for tests).  lens_host [B] holds
- * post-append lengths (invalid ones count as 0); block_size 1 for a contiguous cache.  The
- * kernels use Pu = min(P, ceil(W / min_tokens)) CTAs, further capped at floor(W / block_size)
- * for a paged cache; CTA i takes stream positions [cuts[i], cuts[i+1]).  A paged cache rounds
- * each cut down to a block boundary of the stream it falls in, so every segment starts on a
- * block.  Writes cuts[0..Pu] (Pu + 1 values; cuts must hold P + 1) and returns Pu (0 when
- * W = 0, -1 for bad arguments). */
-int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+ * post-append lengths (invalid ones count as 0).  The kernels use
+ * Pu = min(P, ceil(W / min_tokens), U) CTAs for W tokens in U units; CTA i takes stream
+ * positions [cuts[i], cuts[i+1]).  Writes cuts[0..Pu] (Pu + 1 values; cuts must hold P + 1) and
+ * returns Pu (0 when W = 0, -1 for bad arguments, including B * T_max >= 2^31). */
+int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int grain, int P,
                   int min_tokens, int64_t* cuts);
-/* First and last CTA holding stream (b, h) under that partition (KVC_EINVAL if it is empty). */
-int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+/* First and last CTA holding stream (b, h) under that partition (KVC_EINVAL if it is empty,
+ * KVC_ERANGE if B * T_max >= 2^31). */
+int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int grain, int P,
                          int min_tokens, int b, int h, int* first, int* last);
 
 /* Decode attention for callers that cannot allocate device memory.  The pages have no

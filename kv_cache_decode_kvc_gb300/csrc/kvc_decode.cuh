@@ -73,7 +73,7 @@ struct DecodeCfg {
     static constexpr int Q_BYTES = (G * ROWB + 127) / 128 * 128;  // the group's q rows
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + Q_BYTES;
     static constexpr int MERGE_FLOATS = NW * HS * (D + 2);
-    static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
+    static constexpr int PREFIX_BYTES = 2 * (MAX_B + 1) * 4;  // prefix and uprefix (int32)
     static constexpr int MISC_BYTES = 256;
     static constexpr int BUDGET = 230400;
     static constexpr int NST_A =
@@ -92,7 +92,9 @@ constexpr unsigned FULL = 0xFFFFFFFFu;
 
 // Walks the (b, h) streams a CTA's range [r0, r1) touches, in order.
 struct SegIter {
-    const int64_t* prefix;  // prefix[b] = sum_{b' < b} L_b' (invalid lengths count as 0)
+    // prefix[b] = sum_{b' < b} L_b' (invalid lengths count as 0); the partition-unit prefix
+    // uprefix[b] = sum_{b' < b} ceil(L_b' / grain) follows it in shared memory at prefix + MAX_B + 1
+    const int32_t* prefix;
     int B, H_kv;
     int64_t r1;
     int b, h, L;
@@ -100,7 +102,7 @@ struct SegIter {
     int t0, t1;      // this segment: tokens [t0, t1) of the stream
     bool valid;
 
-    __device__ void init(const int64_t* pre, int B_, int H_kv_, int64_t r0, int64_t r1_) {
+    __device__ void init(const int32_t* pre, int B_, int H_kv_, int64_t r0, int64_t r1_) {
         prefix = pre; B = B_; H_kv = H_kv_; r1 = r1_;
         int lo = 0, hi = B - 1;  // largest b with H_kv * prefix[b] <= r0
         while (lo < hi) {
@@ -108,7 +110,7 @@ struct SegIter {
             if ((int64_t)H_kv * prefix[mid] <= r0) lo = mid; else hi = mid - 1;
         }
         b = lo;
-        L = (int)(prefix[b + 1] - prefix[b]);
+        L = prefix[b + 1] - prefix[b];
         h = (int)((r0 - (int64_t)H_kv * prefix[b]) / L);
         ustart = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
         t0 = (int)(r0 - ustart);
@@ -121,7 +123,7 @@ struct SegIter {
         if (++h == H_kv) {
             h = 0;
             do { ++b; } while (prefix[b + 1] == prefix[b]);  // skip empty sequences
-            L = (int)(prefix[b + 1] - prefix[b]);
+            L = prefix[b + 1] - prefix[b];
         }
         ustart = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
         t0 = 0;
@@ -129,13 +131,43 @@ struct SegIter {
     }
 };
 
+// Prefix sums of the sequences' valid lengths and of their partition units (one warp):
+// prefix[b] = sum_{b' < b} L_b', uprefix[b] = sum_{b' < b} ceil(L_b' / p.grain), B + 1 entries.
+__device__ __forceinline__ void scan_lengths(const DecodeParams& p, int rolling, int32_t* prefix,
+                                             int32_t* uprefix, int lane) {
+    int carry = 0, ucarry = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int x = b < p.B ? eff_len(p.lens[b], p.T_max, rolling, p.T_q) : 0;
+        int u = (int)units_of(x, p.grain);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, o), v = __shfl_up_sync(FULL, u, o);
+            if (lane >= o) {
+                x += y;
+                u += v;
+            }
+        }
+        if (b < p.B) {
+            prefix[b + 1] = carry + x;
+            uprefix[b + 1] = ucarry + u;
+        }
+        carry += __shfl_sync(FULL, x, 31);
+        ucarry += __shfl_sync(FULL, u, 31);
+    }
+    if (lane == 0) {
+        prefix[0] = 0;
+        uprefix[0] = 0;
+    }
+}
+
 // Position in the CTA's tile sequence: segment + first token of the tile.
 template <int TT>
 struct TileCursor {
     SegIter it;
     int t;
     bool valid;
-    __device__ void init(const int64_t* pre, int B, int H_kv, int64_t r0, int64_t r1) {
+    __device__ void init(const int32_t* pre, int B, int H_kv, int64_t r0, int64_t r1) {
         it.init(pre, B, H_kv, r0, r1);
         t = it.t0;
         valid = it.valid;
@@ -352,11 +384,15 @@ struct NoRelease {
 };
 template <typename T, int G, int D, int HS, int NWT, int NW, int BAR = 0, class Rel = NoRelease>
 __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* merge,
-                                               const SegIter& it, size_t unit, int64_t W, int64_t P,
+                                               const SegIter& it, size_t unit, int64_t U, int64_t P,
                                                int* last_flag, int tid, Rel released = Rel()) {
     const bool whole = (it.t0 == 0) && (it.t1 == it.L);
     const int64_t us = it.ustart;
-    const int64_t cfirst = cta_first_of_stream(us, it.L, W, P, p.bs), clast = cta_of(us + it.L - 1, W, P);
+    // the stream's partition units [u0, u0 + nu)
+    const int32_t* uprefix = it.prefix + MAX_B + 1;
+    const int64_t nu = uprefix[it.b + 1] - uprefix[it.b];
+    const int64_t u0 = (int64_t)it.H_kv * uprefix[it.b] + (int64_t)it.h * nu;
+    const int64_t cfirst = cta_of(u0, U, P), clast = cta_of(u0 + nu - 1, U, P);
     const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
     if constexpr (NWT == 1) {
         // `merge` holds this segment's final state.  If every other CTA of the stream has
@@ -450,8 +486,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ring = smem;
     float* merge = reinterpret_cast<float*>(smem + NST * C::STAGE_BYTES);
-    int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(prefix + MAX_B + 1);
+    int32_t* prefix = reinterpret_cast<int32_t*>(merge + C::MERGE_FLOATS);
+    int32_t* uprefix = prefix + MAX_B + 1;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(uprefix + MAX_B + 1);
     int* release_cnt = reinterpret_cast<int*>(full_bar + NST);   // [NST]
     int* issued = release_cnt + NST;                                // [NST] tiles issued per stage
     volatile int* abort_flag = issued + NST;
@@ -462,25 +499,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
     const size_t row_elems_q = (size_t)H_kv * G * D;  // one sequence of q / out
 
     // ---- lengths -> stream prefix sums (warp 0); barriers (thread 32)
-    if (warp == 0) {
-        int64_t carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            int64_t x = 0;
-            if (b < B) {
-                const int L = p.lens[b];
-                x = eff_len(L, p.T_max, p.rolling, p.T_q);
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int64_t y = __shfl_up_sync(FULL, x, o);
-                if (lane >= o) x += y;
-            }
-            if (b < B) prefix[b + 1] = carry + x;
-            carry += __shfl_sync(FULL, x, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
-    }
+    if (warp == 0) scan_lengths(p, p.rolling, prefix, uprefix, lane);
     if (tid == (NW > 1 ? 32 : 0)) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -502,12 +521,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
         }
     }
 
-    const int64_t W = (int64_t)H_kv * prefix[B];
+    const int64_t W = (int64_t)H_kv * prefix[B], U = (int64_t)H_kv * uprefix[B];
     if (W == 0) return;
-    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
+    const int64_t P = plan_ctas(W, U, p.P, p.min_tokens);
     if ((int64_t)blockIdx.x >= P) return;
-    const int64_t r0 = cta_cut(blockIdx.x, prefix, B, H_kv, W, P, p.bs);
-    const int64_t r1 = cta_cut(blockIdx.x + 1, prefix, B, H_kv, W, P, p.bs);
+    const int64_t r0 = cta_cut(blockIdx.x, prefix, uprefix, B, H_kv, U, P, p.grain);
+    const int64_t r1 = cta_cut(blockIdx.x + 1, prefix, uprefix, B, H_kv, U, P, p.grain);
     if (r0 >= r1) return;
     const bool fused = p.k_new != nullptr;
     const uint64_t pol = policy_evict_first();
@@ -803,7 +822,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, G>::NTHREADS, 1)
             }
             __syncthreads();
 
-            finish_segment<T, G, D, HS, NWT, NW>(p, merge, cur.it, unit, W, P, last_flag, tid);
+            finish_segment<T, G, D, HS, NWT, NW>(p, merge, cur.it, unit, U, P, last_flag, tid);
         }
         cur.advance();
     }
@@ -843,29 +862,36 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     const int ds = blockIdx.x % DS, ug = blockIdx.x / DS;
     const int u = ug / G, hg = ug % G;
     const int b = u / p.H_kv, h = u % p.H_kv;
-    __shared__ int64_t sh_sum[2];
+    __shared__ int64_t sh_sum[4];
     __shared__ float sw[COMBINE_MAX_SEG];
     __shared__ float sred[NWARP];
     __shared__ float4 spart[COMBINE_THREADS];
-    if (threadIdx.x < 2) sh_sum[threadIdx.x] = 0;
+    if (threadIdx.x < 4) sh_sum[threadIdx.x] = 0;
     __syncthreads();
-    int64_t before = 0, all = 0;
+    // tokens and partition units of the sequences before b, and of all
+    int64_t before = 0, all = 0, ubefore = 0, uall = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
         const int L = p.lens[i];
-        const int64_t v = eff_len(L, p.T_max, p.rolling, p.T_q);
+        const int64_t v = eff_len(L, p.T_max, p.rolling, p.T_q), nv = units_of(v, p.grain);
         all += v;
-        if (i < b) before += v;
+        uall += nv;
+        if (i < b) {
+            before += v;
+            ubefore += nv;
+        }
     }
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[0]), (unsigned long long)before);
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[1]), (unsigned long long)all);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[2]), (unsigned long long)ubefore);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sh_sum[3]), (unsigned long long)uall);
     __syncthreads();
     if (p.overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int Lb = eff_len(p.lens[b], p.T_max, p.rolling, p.T_q);
     if (Lb == 0) return;
-    const int64_t W = (int64_t)p.H_kv * sh_sum[1];
-    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
-    const int64_t us = (int64_t)p.H_kv * sh_sum[0] + (int64_t)h * Lb;
-    const int64_t cfirst = cta_first_of_stream(us, Lb, W, P, p.bs), clast = cta_of(us + Lb - 1, W, P);
+    const int64_t W = (int64_t)p.H_kv * sh_sum[1], U = (int64_t)p.H_kv * sh_sum[3];
+    const int64_t P = plan_ctas(W, U, p.P, p.min_tokens);
+    const int64_t nu = units_of(Lb, p.grain), u0 = (int64_t)p.H_kv * sh_sum[2] + (int64_t)h * nu;
+    const int64_t cfirst = cta_of(u0, U, P), clast = cta_of(u0 + nu - 1, U, P);
     if (cfirst == clast) return;  // written directly by its CTA
     const int nseg = (int)(clast - cfirst + 1);
     if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs

@@ -46,7 +46,7 @@ struct TcCfg {
     static constexpr int Q_BYTES = (G * ROWB + 1023) / 1024 * 1024;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + Q_BYTES;
     static constexpr int MERGE_FLOATS = NW * HS * (D + 2);
-    static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
+    static constexpr int PREFIX_BYTES = 2 * (MAX_B + 1) * 4;  // prefix and uprefix (int32)
     static constexpr int MISC_BYTES = 256;
     static constexpr int ALIGN_PAD = 1024;
     static constexpr int BUDGET = 230400;
@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(TcCfg<D, G>::NTHREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* ring = smem;
     float* merge = reinterpret_cast<float*>(smem + NST * C::STAGE_BYTES);
-    int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(prefix + MAX_B + 1);
+    int32_t* prefix = reinterpret_cast<int32_t*>(merge + C::MERGE_FLOATS);
+    int32_t* uprefix = prefix + MAX_B + 1;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(uprefix + MAX_B + 1);
     int* release_cnt = reinterpret_cast<int*>(full_bar + NST);
     int* issued = release_cnt + NST;
     volatile int* abort_flag = issued + NST;
@@ -166,25 +167,7 @@ __global__ void __launch_bounds__(TcCfg<D, G>::NTHREADS, 1)
     const int B = p.B, H_kv = p.H_kv;
     const size_t row_elems_q = (size_t)H_kv * G * D;
 
-    if (warp == 0) {
-        int64_t carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            int64_t x = 0;
-            if (b < B) {
-                const int L = p.lens[b];
-                x = (L >= 1 && L <= p.T_max) ? L : 0;
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int64_t y = __shfl_up_sync(FULL, x, o);
-                if (lane >= o) x += y;
-            }
-            if (b < B) prefix[b + 1] = carry + x;
-            carry += __shfl_sync(FULL, x, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
-    }
+    if (warp == 0) scan_lengths(p, 0, prefix, uprefix, lane);
     if (tid == 32) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -205,11 +188,12 @@ __global__ void __launch_bounds__(TcCfg<D, G>::NTHREADS, 1)
         }
     }
 
-    const int64_t W = (int64_t)H_kv * prefix[B];
+    const int64_t W = (int64_t)H_kv * prefix[B], U = (int64_t)H_kv * uprefix[B];
     if (W == 0) return;
-    const int64_t P = plan_ctas(W, p.P, p.min_tokens, p.bs);
+    const int64_t P = plan_ctas(W, U, p.P, p.min_tokens);
     if ((int64_t)blockIdx.x >= P) return;
-    const int64_t r0 = cta_begin(blockIdx.x, W, P), r1 = cta_begin(blockIdx.x + 1, W, P);
+    const int64_t r0 = cta_cut(blockIdx.x, prefix, uprefix, B, H_kv, U, P, p.grain);
+    const int64_t r1 = cta_cut(blockIdx.x + 1, prefix, uprefix, B, H_kv, U, P, p.grain);
     if (r0 >= r1) return;
 
     // ---- fused append: write the new rows of the streams whose last token this CTA owns,
@@ -403,7 +387,7 @@ __global__ void __launch_bounds__(TcCfg<D, G>::NTHREADS, 1)
                 if (h1 < HS) { mw[h1 * (D + 2) + D] = m[1]; mw[h1 * (D + 2) + D + 1] = lt1; }
             }
             __syncthreads();
-            finish_segment<T, G, D, HS, NWT, NW>(p, merge, cur.it, unit, W, P, last_flag, tid);
+            finish_segment<T, G, D, HS, NWT, NW>(p, merge, cur.it, unit, U, P, last_flag, tid);
         }
         cur.advance();
     }

@@ -70,7 +70,7 @@ struct Tc5Cfg {
     static constexpr int PBUF = PMN ? TT * 128 : (TT / 64) * PBLOCK;
     static constexpr int HS = G < 8 ? G : 8;            // head slices for finish_segment
     static constexpr int MERGE_FLOATS = G * (D + 2);
-    static constexpr int PREFIX_BYTES = (MAX_B + 1) * 8;
+    static constexpr int PREFIX_BYTES = 2 * (MAX_B + 1) * 4;  // prefix and uprefix (int32)
     static constexpr int RED_BYTES = 6 * N * 4;         // reductions [quadrant][N], rescale factors [2][N]
     // 4 tensor maps: K and V with 128-row boxes (full tiles) and 32-row boxes (partial tiles)
     static constexpr int MISC_BYTES = 512;              // mbarriers and flags
@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     constexpr bool DED2 = tc5_mma2_warp<G, MODE>();  // a warp of its own issues MMA2
     constexpr int D = C::D, N = C::N, NP = C::NP, TT = C::TT, NST = C::NST, TS = TT / 16;
     constexpr int KS = FP8 ? D / 32 : D / 16;  // MMA1 k-steps of 32 bytes
+    using Cur = TileCursor<TT>;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -444,8 +445,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     unsigned char* vring = ring + NST * C::TILE_BYTES;
     unsigned char* pbuf = qsw + C::OPB_BYTES;                 // [2 buffers][2 blocks][2N rows][128 B]
     float* merge = reinterpret_cast<float*>(pbuf + 2 * C::PBUF);
-    int64_t* prefix = reinterpret_cast<int64_t*>(merge + C::MERGE_FLOATS);
-    float* red = reinterpret_cast<float*>(prefix + MAX_B + 1);  // [4][N]
+    int32_t* prefix = reinterpret_cast<int32_t*>(merge + C::MERGE_FLOATS);
+    int32_t* uprefix = prefix + MAX_B + 1;
+    float* red = reinterpret_cast<float*>(uprefix + MAX_B + 1);  // [4][N]
     float* alpha_s = red + 4 * N;                                  // [2][N]: rescale factor of a tile
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(red + 6 * N);
     uint64_t* empty_bar = full_bar + NST;
@@ -527,36 +529,18 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     const bool early = p.overlap != 0;
     if (!early) asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    if (warp == 0) {
-        int64_t carry = 0;
-        for (int b0 = 0; b0 < B; b0 += 32) {
-            const int b = b0 + lane;
-            int64_t x = 0;
-            if (b < B) {
-                const int L = p.lens[b];
-                x = eff_len(L, p.T_max, ROLL ? 1 : 0, p.T_q);
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int64_t y = __shfl_up_sync(FULL, x, o);
-                if (lane >= o) x += y;
-            }
-            if (b < B) prefix[b + 1] = carry + x;
-            carry += __shfl_sync(FULL, x, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
-    }
+    if (warp == 0) scan_lengths(p, ROLL ? 1 : 0, prefix, uprefix, lane);
     __syncthreads();
 
-    const int64_t W = (int64_t)H_kv * prefix[B];
-    const int64_t P = W > 0 ? plan_ctas(W, p.P, p.min_tokens, p.bs) : 0;
-    const int64_t r0 = W > 0 ? cta_cut(blockIdx.x, prefix, B, H_kv, W, P, p.bs) : 0;
-    const int64_t r1 = W > 0 ? cta_cut(blockIdx.x + 1, prefix, B, H_kv, W, P, p.bs) : 0;
+    const int64_t W = (int64_t)H_kv * prefix[B], U = (int64_t)H_kv * uprefix[B];
+    const int64_t P = W > 0 ? plan_ctas(W, U, p.P, p.min_tokens) : 0;
+    const int64_t r0 = W > 0 ? cta_cut(blockIdx.x, prefix, uprefix, B, H_kv, U, P, p.grain) : 0;
+    const int64_t r1 = W > 0 ? cta_cut(blockIdx.x + 1, prefix, uprefix, B, H_kv, U, P, p.grain) : 0;
     const bool work = W > 0 && (int64_t)blockIdx.x < P && r0 < r1;
     const uint32_t ring_s = smem_addr(ring);
     const uint64_t pol = policy_evict_first();
     constexpr bool paged = PAGED;  // paged pool through the block table (separate instantiation)
-    TileCursor<TT> pref;  // producer's cursor (thread 0; the whole warp 0 when paged)
+    Cur pref;  // producer's cursor (thread 0; the whole warp 0 when paged)
     NewRow<ROLL> nrow;    // producer: where the stream's new row is
     int ent = 0;          // paged: this lane's block of the tile at pref
     int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
@@ -602,7 +586,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     auto final_segment = [&](bool ok, const SegIter& it, int jt) {
         const bool skip = group_any<5, NJ * 32>(!ok || *abort_flag != 0);
         if (!skip)
-            finish_segment<T, G, D, C::HS, 1, NJ, 5>(p, merge, it, (size_t)it.b * H_kv + it.h, W, P,
+            finish_segment<T, G, D, C::HS, 1, NJ, 5>(p, merge, it, (size_t)it.b * H_kv + it.h, U, P,
                                                      last_flag, jt);
     };
 
@@ -674,11 +658,11 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 // K slots: tile k in slot k % NST, refilled with tile k + NST once MMA1(k) has read
                 // it; V slots: tile k in slot k % NV, refilled with tile k + NV once MMA2(k) has.
                 // This thread issues MMA2 (its V wait included) between the two refills.
-                auto ready = [&](const TileCursor<TT>& c) {
+                auto ready = [&](const Cur& c) {
                     return !(fused && nrow.in_tile(p, c.it.b, c.it.L, c.t, c.n())) ||
                            mbar_wait(append_bar, 0u, abort_flag, p.err);
                 };
-                TileCursor<TT> vp;  // V cursor
+                Cur vp;  // V cursor
                 vp.init(prefix, B, H_kv, r0, r1);
                 const int nvpre = npre < C::NV ? npre : C::NV;
                 for (int i = 0; i < nvpre && vp.valid; ++i) vp.advance();
@@ -696,7 +680,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                     issue_one_tc5<C, TT>(p, vp, smem_addr(vring) + sv * C::TILE_BYTES, &sv_full[sv], pol, &tmV, &tmVf);
                     vp.advance();
                 }
-                TileCursor<TT> mc;
+                Cur mc;
                 mc.init(prefix, B, H_kv, r0, r1);
                 for (int k = 0; ok && mc.valid; ++k) {
                     const int sk = k % NST, sv = k % C::NV;
@@ -738,7 +722,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 // MMA2 of each tile (this thread issues it: MMA1 is warp 1's), then the tile NST
                 // ahead into the stage that MMA2 frees.  Issued here so that MMA1 of the next tile
                 // never queues behind it in one thread (each tcgen05.mma takes ~90 cycles to issue).
-                TileCursor<TT> mc;
+                Cur mc;
                 mc.init(prefix, B, H_kv, r0, r1);
                 int s2 = 0;
                 for (int k = 0; ok && mc.valid; ++k) {
@@ -795,7 +779,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // Each segment's q rows (G rows of D bf16 at row unit * G of q) go into the swizzled
         // operand from registers, loaded one segment ahead and stored once the previous
         // segment's last MMA1 has read the operand.
-        TileCursor<TT> cur;
+        Cur cur;
         cur.init(prefix, B, H_kv, r0, r1);
         constexpr int QV = G * (D / 8), QPL = (QV + 31) / 32;
         uint4 qv[QPL];
@@ -928,7 +912,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // ======================================================= MMA2 issue (fp8, groups <= 4)
         // MMA2 of each tile once its weights, its O^T buffer and its f16 V working tile are ready
         // (lane 0 issues; the warp follows its verdict)
-        TileCursor<TT> mc;
+        Cur mc;
         mc.init(prefix, B, H_kv, r0, r1);
         bool ok = true;
         for (int k = 0; ok && mc.valid; ++k) {
@@ -955,7 +939,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // Then publish the working tile to the tensor cores and hand the stage's V back (MMA1's
         // commit hands back K).
         const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
-        TileCursor<TT> cc;
+        Cur cc;
         cc.init(prefix, B, H_kv, r0, r1);
         int s = 0;
         uint32_t ph = 0;
@@ -1018,7 +1002,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // written first (it does not overlap the int8 rows); after a barrier of the converter
         // warps, each thread widens whole rows' second halves in place.
         const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
-        TileCursor<TT> cc;
+        Cur cc;
         cc.init(prefix, B, H_kv, r0, r1);
         int s = 0;
         uint32_t ph = 0;
@@ -1090,7 +1074,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // partial state's fence, arrival count and any merge of the stream follow
             if (ok)
                 finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
-                                                              W, P, last_flag, et,
+                                                              U, P, last_flag, et,
                                                               [&]() { mbar_arrive(m_empty); });
             else
                 mbar_arrive(m_empty);
@@ -1188,7 +1172,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // have no registers to spare.
         constexpr bool ASH = C::PMN;
         float o[GH], m[GH], mt[GH], l[GH], alpha[GH], alpha_prev[GH];
-        TileCursor<TT> cur;
+        Cur cur;
         cur.init(prefix, B, H_kv, r0, r1);
         int s = 0, sg = 0;
         uint32_t ph = 0;
@@ -1215,7 +1199,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         };
         // int8 / fp8 cache: the K and V scales of this thread's row of a tile; the new row of a
         // fused step takes them from k_new / v_new, as its append computes them
-        auto load_scales = [&](const TileCursor<TT>& c, float& a, float& b) {
+        auto load_scales = [&](const Cur& c, float& a, float& b) {
             a = 1.f;
             b = 1.f;
             if (row < c.n()) {
@@ -1252,7 +1236,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             // int8 / fp8 cache: this row's K and V scales, loaded one tile ahead
             const float sk = sk_next, sv = sv_next;
             if constexpr (SCALED) {
-                TileCursor<TT> nxt = cur;
+                Cur nxt = cur;
                 nxt.advance();
                 if (nxt.valid) load_scales(nxt, sk_next, sv_next);
             }

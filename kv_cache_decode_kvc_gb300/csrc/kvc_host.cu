@@ -265,6 +265,7 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
         mode = (nseg * h->G * T_q * h->D * 4 > 65536) ? 1 : 0;
     }
     p.combine_mode = mode;
+    p.grain = kvc::partition_grain(h->G, mode, p.bs);
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
     p.overlap = h->overlap;
     return launch_decode(h, layer, p, static_cast<cudaStream_t>(stream));
@@ -305,48 +306,62 @@ uint64_t kvc_bytes_formula(int64_t L, int64_t B, int64_t H_kv, int64_t D, int64_
     return r;
 }
 
-int kvc_plan_cta_of(int64_t x, int64_t W, int P) {
-    if (W <= 0 || P <= 0 || x < 0 || x >= W) return -1;
-    return (int)kvc::cta_of(x, W, P);
+int kvc_plan_grain(int G, int combine_mode, int block_size) {
+    if (G < 1 || (combine_mode != 0 && combine_mode != 1) || block_size < 1) return -1;
+    return kvc::partition_grain(G, combine_mode, block_size);
+}
+
+int kvc_plan_cta_of(int64_t x, int64_t U, int P) {
+    if (U <= 0 || P <= 0 || x < 0 || x >= U) return -1;
+    return (int)kvc::cta_of(x, U, P);
 }
 
 namespace {
-// prefix[b] = sum of the valid lengths before b (host copy of the kernels' first step)
-int64_t plan_prefix(const int32_t* lens, int B, int T_max, std::vector<int64_t>& prefix) {
+// prefix[b] / uprefix[b] = valid lengths / partition units before b (host copy of the kernels'
+// first step; B * T_max < 2^31 keeps both in 32 bits)
+bool plan_prefix(const int32_t* lens, int B, int T_max, int grain, std::vector<int32_t>& prefix,
+                 std::vector<int32_t>& uprefix) {
+    if ((int64_t)B * T_max >= (int64_t(1) << 31)) return false;
     prefix.assign((size_t)B + 1, 0);
-    for (int b = 0; b < B; ++b)
-        prefix[b + 1] = prefix[b] + ((lens[b] >= 1 && lens[b] <= T_max) ? lens[b] : 0);
-    return prefix[B];
+    uprefix.assign((size_t)B + 1, 0);
+    for (int b = 0; b < B; ++b) {
+        const int L = (lens[b] >= 1 && lens[b] <= T_max) ? lens[b] : 0;
+        prefix[b + 1] = prefix[b] + L;
+        uprefix[b + 1] = uprefix[b] + (int32_t)kvc::units_of(L, grain);
+    }
+    return true;
 }
 }  // namespace
 
-int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+int kvc_plan_cuts(const int32_t* lens_host, int B, int H_kv, int T_max, int grain, int P,
                   int min_tokens, int64_t* cuts) {
-    if (!lens_host || !cuts || B < 1 || B > kvc::MAX_B || H_kv < 1 || P < 1 || min_tokens < 1 ||
-        block_size < 1)
+    if (!lens_host || !cuts || B < 1 || B > kvc::MAX_B || H_kv < 1 || T_max < 1 || grain < 1 ||
+        P < 1 || min_tokens < 1)
         return -1;
-    std::vector<int64_t> prefix;
-    const int64_t W = (int64_t)H_kv * plan_prefix(lens_host, B, T_max, prefix);
+    std::vector<int32_t> prefix, uprefix;
+    if (!plan_prefix(lens_host, B, T_max, grain, prefix, uprefix)) return -1;
+    const int64_t W = (int64_t)H_kv * prefix[B], U = (int64_t)H_kv * uprefix[B];
     if (W == 0) return 0;
-    const int64_t Pu = kvc::plan_ctas(W, P, min_tokens, block_size);
+    const int64_t Pu = kvc::plan_ctas(W, U, P, min_tokens);
     for (int64_t i = 0; i <= Pu; ++i)
-        cuts[i] = kvc::cta_cut(i, prefix.data(), B, H_kv, W, Pu, block_size);
+        cuts[i] = kvc::cta_cut(i, prefix.data(), uprefix.data(), B, H_kv, U, Pu, grain);
     return (int)Pu;
 }
 
-int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int block_size, int P,
+int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, int grain, int P,
                          int min_tokens, int b, int h, int* first, int* last) {
-    if (!lens_host || !first || !last || B < 1 || B > kvc::MAX_B || b < 0 || b >= B || h < 0 ||
-        h >= H_kv || P < 1 || min_tokens < 1 || block_size < 1)
+    if (!lens_host || !first || !last || B < 1 || B > kvc::MAX_B || T_max < 1 || grain < 1 || b < 0 ||
+        b >= B || h < 0 || h >= H_kv || P < 1 || min_tokens < 1)
         return KVC_EINVAL;
-    std::vector<int64_t> prefix;
-    const int64_t W = (int64_t)H_kv * plan_prefix(lens_host, B, T_max, prefix);
-    const int64_t L = prefix[b + 1] - prefix[b];
-    if (W == 0 || L == 0) return KVC_EINVAL;
-    const int64_t Pu = kvc::plan_ctas(W, P, min_tokens, block_size);
-    const int64_t us = (int64_t)H_kv * prefix[b] + (int64_t)h * L;
-    *first = (int)kvc::cta_first_of_stream(us, L, W, Pu, block_size);
-    *last = (int)kvc::cta_of(us + L - 1, W, Pu);
+    std::vector<int32_t> prefix, uprefix;
+    if (!plan_prefix(lens_host, B, T_max, grain, prefix, uprefix)) return KVC_ERANGE;
+    const int64_t W = (int64_t)H_kv * prefix[B], U = (int64_t)H_kv * uprefix[B];
+    const int64_t nu = uprefix[b + 1] - uprefix[b];
+    if (W == 0 || nu == 0) return KVC_EINVAL;
+    const int64_t Pu = kvc::plan_ctas(W, U, P, min_tokens);
+    const int64_t u0 = (int64_t)H_kv * uprefix[b] + (int64_t)h * nu;
+    *first = (int)kvc::cta_of(u0, U, Pu);
+    *last = (int)kvc::cta_of(u0 + nu - 1, U, Pu);
     return KVC_OK;
 }
 
@@ -363,8 +378,8 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
     const int G = H_q / H_kv;
     if (!g_supported(G) || !d_supported(dtype, D)) return KVC_EUNSUPPORTED;
     const int es = dtype == KVC_BF16 ? 2 : 4;
-    // partition positions: B * H_kv * T_max < 2^50
-    if ((double)B * H_kv * (double)T_max >= 1125899906842624.0) return KVC_ERANGE;
+    // the kernels keep prefix sums of the sequence lengths in 32 bits: B * T_max < 2^31
+    if ((int64_t)B * T_max >= (int64_t(1) << 31)) return KVC_ERANGE;
     // rows of one layer's K (or V): streams x T_max, or the pool's blocks x heads x bs
     uint64_t rows = 0;
     if (!mul_ok(paged ? (uint64_t)num_blocks : (uint64_t)B, (uint64_t)H_kv, &rows) ||

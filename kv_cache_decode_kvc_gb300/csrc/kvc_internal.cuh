@@ -23,49 +23,57 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 // ------------------------------------------------------------------ split-T partition
 // The B*H_kv (sequence b, KV head h) streams are laid end to end, stream u = b*H_kv + h
-// holding L_b tokens; W = H_kv * sum_b L_b.  CTA i of P owns positions
-// [cta_begin(i), cta_begin(i+1)).  W < 2^50 and P <= 2^12 keep every product below 2^63.
-__host__ __device__ inline int64_t cta_begin(int64_t i, int64_t W, int64_t P) {
-    return (i * W) / P;
+// holding L_b tokens; W = H_kv * sum_b L_b.  Each stream is cut into units of g tokens (the
+// stream's last unit may be partial): n_b = ceil(L_b / g) units, U = H_kv * sum_b n_b in all.
+// CTA i of P owns units [cta_begin(i), cta_begin(i+1)), so every CTA holds floor(U / P) or
+// ceil(U / P) units and every cut falls on a unit boundary of its stream.  With g = GRAIN = 128
+// (one tcgen05 tile) a tile never straddles two CTAs and the split adds no partial tiles (a
+// CTA's tile count is its unit count); paged blocks of 16..128 tokens divide a unit, a 256-token
+// block may be cut at its 128-token boundary.  g = 1 is the plain token split (every CTA holds
+// W / P tokens; a paged cache takes g = its block size), used where groups of 16+ query heads
+// merge their split streams inside the kernel: measured faster there (MQA, B = 64 streams of
+// 4097 tokens: 38.2 against 42.3 us per layer), the merges of their large partial states falling
+// better behind the streaming of other CTAs; with the separate combine kernel (one long stream)
+// the tile-aligned split is the faster one (29.1 against 31.0 us).
+// prefix[b] = sum_{b' < b} L_b' and uprefix[b] = sum_{b' < b} n_b' (B + 1 entries each,
+// 32-bit: creation keeps B * T_max below 2^31).  U and P <= 2^12 keep products below 2^63.
+constexpr int GRAIN = 128;
+__host__ __device__ inline int64_t units_of(int64_t L, int g) {
+    return (L + g - 1) / g;
 }
-// CTA owning position x: the largest i with cta_begin(i) <= x.
-__host__ __device__ inline int64_t cta_of(int64_t x, int64_t W, int64_t P) {
-    return ((x + 1) * P - 1) / W;
+// Partition unit for a query group of G heads, the merge mode (0: in the kernel, 1: combine
+// kernel) and the block size of a paged cache (1: contiguous).
+__host__ __device__ inline int partition_grain(int G, int combine_mode, int bs) {
+    if (G >= 16 && combine_mode == 0) return bs > 1 ? bs : 1;
+    return GRAIN;
 }
-
-// Paged caches (block size bs > 1) round every cut down to a block boundary of the stream it
-// falls in, so each segment starts on a block and a 128-token tile covers whole blocks.
-// prefix[b] = sum_{b' < b} L_b' (B + 1 entries).  With W / P >= bs the rounded cuts stay
-// strictly increasing, so no CTA range is empty.  bs <= 1: the plain cut.
-__host__ __device__ inline int64_t cta_cut(int64_t i, const int64_t* prefix, int B, int H_kv,
-                                           int64_t W, int64_t P, int bs) {
-    const int64_t x = cta_begin(i, W, P);
-    if (bs <= 1 || x >= W) return x;
-    int lo = 0, hi = B - 1;  // largest b with H_kv * prefix[b] <= x
+__host__ __device__ inline int64_t cta_begin(int64_t i, int64_t U, int64_t P) {
+    return (i * U) / P;
+}
+// CTA owning unit x: the largest i with cta_begin(i) <= x.
+__host__ __device__ inline int64_t cta_of(int64_t x, int64_t U, int64_t P) {
+    return ((x + 1) * P - 1) / U;
+}
+// Token position of CTA i's first unit (i = P: the end, W).
+__host__ __device__ inline int64_t cta_cut(int64_t i, const int32_t* prefix, const int32_t* uprefix,
+                                           int B, int H_kv, int64_t U, int64_t P, int g) {
+    if (i >= P) return (int64_t)H_kv * prefix[B];
+    const int64_t x = cta_begin(i, U, P);
+    int lo = 0, hi = B - 1;  // largest b with H_kv * uprefix[b] <= x (a sequence with units)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)H_kv * prefix[mid] <= x) lo = mid; else hi = mid - 1;
+        if ((int64_t)H_kv * uprefix[mid] <= x) lo = mid; else hi = mid - 1;
     }
-    const int64_t L = prefix[lo + 1] - prefix[lo];
-    const int64_t base = (int64_t)H_kv * prefix[lo];
-    const int64_t ustart = base + ((x - base) / L) * L;
-    return ustart + ((x - ustart) / bs) * bs;
+    const int64_t nb = uprefix[lo + 1] - uprefix[lo];
+    const int64_t r = x - (int64_t)H_kv * uprefix[lo];
+    const int64_t h = r / nb;
+    return (int64_t)H_kv * prefix[lo] + h * (int64_t)(prefix[lo + 1] - prefix[lo]) + (r - h * nb) * g;
 }
-// CTAs actually used for W positions: at most P, at least min_tokens positions each, and for
-// a paged cache at least bs positions each (so rounded cuts never collide).
-__host__ __device__ inline int64_t plan_ctas(int64_t W, int64_t P, int min_tokens, int bs) {
+// CTAs actually used: at most P, at least min_tokens positions each, at least one unit each.
+__host__ __device__ inline int64_t plan_ctas(int64_t W, int64_t U, int64_t P, int min_tokens) {
     int64_t want = (W + min_tokens - 1) / min_tokens;
-    if (bs > 1) {
-        const int64_t cap = W / bs > 1 ? W / bs : 1;
-        if (cap < want) want = cap;
-    }
+    if (U < want) want = U;
     return want < P ? want : P;
-}
-// First CTA holding stream tokens [ustart, ustart + L) under the rounded cuts.
-__host__ __device__ inline int64_t cta_first_of_stream(int64_t ustart, int64_t L, int64_t W,
-                                                       int64_t P, int bs) {
-    const int64_t reach = bs > 1 ? (L < bs ? L : (int64_t)bs) : 1;
-    return cta_of(ustart + reach - 1, W, P);
 }
 
 // ------------------------------------------------------------------ launch parameters
@@ -84,6 +92,7 @@ struct DecodeParams {
     int B, H_kv, T_max;
     int P;                // CTAs of the partition (grid size)
     int min_tokens;       // fewer CTAs when W / P would drop below this (1 = never)
+    int grain;            // partition unit in tokens (partition_grain of the query group)
     int combine_mode;     // 0: the last CTA of a split stream merges it; 1: combine kernel
     float qscale;         // log2(e) / sqrt(D), folded into q
     int overlap;          // 1: lens and history rows may be read before the preceding grid ends

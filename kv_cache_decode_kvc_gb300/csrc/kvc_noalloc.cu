@@ -77,7 +77,8 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     const bool d_ok = dtype == KVC_BF16 ? (D == 64 || D == 128 || D == 256)
                                         : (D == 4 || D == 64 || D == 128 || D == 256);
     if (!g_ok || !d_ok) return KVC_EUNSUPPORTED;
-    if ((double)B * H_kv * (double)T_max >= 1125899906842624.0) return KVC_ERANGE;
+    // the kernels keep prefix sums of the sequence lengths in 32 bits
+    if ((int64_t)B * T_max >= (int64_t(1) << 31)) return KVC_ERANGE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ECUDA;
@@ -131,6 +132,7 @@ extern "C" int kvc_decode_attn_noalloc(const void* K, const void* V, int B, int 
     p.T_q = 1;
     const long long nseg = ((long long)sms + (long long)U - 1) / (long long)U + 1;
     p.combine_mode = (nseg * G * D * 4 > 65536) ? 1 : 0;
+    p.grain = kvc::partition_grain(G, p.combine_mode, 1);
     p.qscale = (float)(1.4426950408889634 / sqrt((double)D));
 
     int smem = 0, e;

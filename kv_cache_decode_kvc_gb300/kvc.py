@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
         "kvc_get_launch_overlap": (I, [P]),
         "kvc_get_shape": (I, [P] + [ctypes.POINTER(I)] * 7),
         "kvc_plan_cta_of": (I, [I64, I64, I]),
+        "kvc_plan_grain": (I, [I, I, I]),
         "kvc_plan_cuts": (I, [P, I, I, I, I, I, I, P]),
         "kvc_plan_stream_ctas": (I, [P, I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "kvc_status_str": (ctypes.c_char_p, [I]),
@@ -315,8 +316,8 @@ def kvc_selftest_wait_timeout(err, info, limit_ns=0, stream=None) -> None:
            "kvc_selftest_wait_timeout")
 
 
-def kvc_plan_cta_of(x, W, P) -> int:
-    return int(load().kvc_plan_cta_of(x, W, P))
+def kvc_plan_cta_of(x, U, P) -> int:
+    return int(load().kvc_plan_cta_of(x, U, P))
 
 
 # ----------------------------------------------------------------------------- owner class

@@ -47,42 +47,42 @@ def test_bytes_formula_rejects_overflow_and_negatives(lib):
     assert kvc.kvc_bytes_formula(2**40, 2**40, 1, 1, 1, 2) == 0
 
 
-def test_partition_covers_every_position_once(lib):
+def test_partition_covers_every_unit_once(lib):
     rng = random.Random(5)
     for _ in range(200):
-        W = rng.randint(1, 10**7)
+        U = rng.randint(1, 10**7)
         P = rng.randint(1, 600)
-        # CTA i owns [floor(i W / P), floor((i+1) W / P)); owner of x is recovered exactly
+        # CTA i owns units [floor(i U / P), floor((i+1) U / P)); owner of x is recovered exactly
         for i in rng.sample(range(P), min(P, 8)):
-            a, b = i * W // P, (i + 1) * W // P
+            a, b = i * U // P, (i + 1) * U // P
             for x in {a, b - 1, (a + b) // 2}:
                 if a <= x < b:
-                    assert kvc.kvc_plan_cta_of(x, W, P) == i
-        assert kvc.kvc_plan_cta_of(0, W, P) == 0 or (W * 1) // P == 0
-        assert kvc.kvc_plan_cta_of(W - 1, W, P) == P - 1
+                    assert kvc.kvc_plan_cta_of(x, U, P) == i
+        assert kvc.kvc_plan_cta_of(0, U, P) == 0 or (U * 1) // P == 0
+        assert kvc.kvc_plan_cta_of(U - 1, U, P) == P - 1
     assert kvc.kvc_plan_cta_of(5, 5, 3) == -1
 
 
 def test_split_slots_are_unique(lib):
     # the kernel writes the partial state of (CTA i, stream u) to slot i + u: injective over
-    # the pairs whose ranges meet (checked by brute force on ragged stream lengths)
+    # the pairs whose unit ranges meet (checked by brute force on ragged stream lengths)
     rng = random.Random(9)
     for _ in range(50):
-        lens = [rng.randint(0, 40) for _ in range(rng.randint(1, 12))]
+        lens = [rng.randint(0, 700) for _ in range(rng.randint(1, 12))]
         H = rng.randint(1, 4)
-        streams = [L for L in lens for _ in range(H)]
-        W = sum(streams)
-        if W == 0:
+        units = [-(-L // 128) for L in lens for _ in range(H)]
+        U = sum(units)
+        if U == 0:
             continue
         P = rng.randint(1, 40)
         seen = {}
         start = 0
-        for u, L in enumerate(streams):
-            if L:
-                for i in range(kvc.kvc_plan_cta_of(start, W, P), kvc.kvc_plan_cta_of(start + L - 1, W, P) + 1):
+        for u, n in enumerate(units):
+            if n:
+                for i in range(kvc.kvc_plan_cta_of(start, U, P), kvc.kvc_plan_cta_of(start + n - 1, U, P) + 1):
                     assert (i + u) not in seen, (seen[(i + u)], (i, u))
                     seen[i + u] = (i, u)
-            start += L
+            start += n
 
 
 def test_status_strings(lib):
