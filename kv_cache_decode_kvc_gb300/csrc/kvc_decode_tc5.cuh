@@ -544,10 +544,17 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     NewRow<ROLL> nrow;    // producer: where the stream's new row is
     int ent = 0;          // paged: this lane's block of the tile at pref
     int npre = 0;         // tiles whose K/V copies started before the grid dependency wait
+    // How many: copies in flight at the grid wait delay its release (measured with a plain
+    // kernel chain: 0.9 us with none, 2.2 us with 192 KB per CTA in flight), while the early
+    // tiles save their load latency.  Small layers gain from one (Llama-2-7B MHA, ~7 tiles per
+    // CTA: 17.0 against 17.7 us per layer with a full ring), long ones from a full ring (8B GQA,
+    // ~48 tiles per CTA: 71.4 against 72.6 with one): a quarter of the CTA's tiles, 1 to NST.
+    const int64_t tiles_per_cta = P > 0 ? (U / P) * p.grain / TT : 0;
+    const int emax = tiles_per_cta / 4 < 1 ? 1 : (tiles_per_cta / 4 > NST ? NST : (int)(tiles_per_cta / 4));
     if (work && (PAGED ? warp == 0 : tid == 0)) {
         pref.init(prefix, B, H_kv, r0, r1);
         if (early)
-            while (pref.valid && npre < NST && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
+            while (pref.valid && npre < emax && !nrow.in_tile(p, pref.it.b, pref.it.L, pref.t, pref.n())) {
                 if constexpr (PAGED) ent = tile_block<TT>(p, pref, lane);
                 if constexpr (C::SPLIT) {
                     issued[npre] += 1;
