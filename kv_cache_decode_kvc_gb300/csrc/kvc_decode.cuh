@@ -139,7 +139,7 @@ __device__ __forceinline__ void scan_lengths(const DecodeParams& p, int rolling,
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
         int x = b < p.B ? eff_len(p.lens[b], p.T_max, rolling, p.T_q) : 0;
-        int u = (int)units_of(x, p.grain);
+        int u = (int)stream_units(x, p.grain);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(FULL, x, o), v = __shfl_up_sync(FULL, u, o);
@@ -388,11 +388,11 @@ __device__ __forceinline__ void finish_segment(const DecodeParams& p, float* mer
                                                int* last_flag, int tid, Rel released = Rel()) {
     const bool whole = (it.t0 == 0) && (it.t1 == it.L);
     const int64_t us = it.ustart;
-    // the stream's partition units [u0, u0 + nu)
+    // the stream's partition units [u0, u0 + nu), its tokens in [u0 + stream_cost, u0 + nu)
     const int32_t* uprefix = it.prefix + MAX_B + 1;
     const int64_t nu = uprefix[it.b + 1] - uprefix[it.b];
     const int64_t u0 = (int64_t)it.H_kv * uprefix[it.b] + (int64_t)it.h * nu;
-    const int64_t cfirst = cta_of(u0, U, P), clast = cta_of(u0 + nu - 1, U, P);
+    const int64_t cfirst = cta_of(u0 + stream_cost(p.grain), U, P), clast = cta_of(u0 + nu - 1, U, P);
     const int64_t slot = (int64_t)blockIdx.x + (int64_t)unit;
     if constexpr (NWT == 1) {
         // `merge` holds this segment's final state.  If every other CTA of the stream has
@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     int64_t before = 0, all = 0, ubefore = 0, uall = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
         const int L = p.lens[i];
-        const int64_t v = eff_len(L, p.T_max, p.rolling, p.T_q), nv = units_of(v, p.grain);
+        const int64_t v = eff_len(L, p.T_max, p.rolling, p.T_q), nv = stream_units(v, p.grain);
         all += v;
         uall += nv;
         if (i < b) {
@@ -890,8 +890,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const DecodePa
     if (Lb == 0) return;
     const int64_t W = (int64_t)p.H_kv * sh_sum[1], U = (int64_t)p.H_kv * sh_sum[3];
     const int64_t P = plan_ctas(W, U, p.P, p.min_tokens);
-    const int64_t nu = units_of(Lb, p.grain), u0 = (int64_t)p.H_kv * sh_sum[2] + (int64_t)h * nu;
-    const int64_t cfirst = cta_of(u0, U, P), clast = cta_of(u0 + nu - 1, U, P);
+    const int64_t nu = stream_units(Lb, p.grain), u0 = (int64_t)p.H_kv * sh_sum[2] + (int64_t)h * nu;
+    const int64_t cfirst = cta_of(u0 + stream_cost(p.grain), U, P), clast = cta_of(u0 + nu - 1, U, P);
     if (cfirst == clast) return;  // written directly by its CTA
     const int nseg = (int)(clast - cfirst + 1);
     if (nseg > COMBINE_MAX_SEG) return;  // cannot happen: P <= 4 * SMs

@@ -327,7 +327,7 @@ bool plan_prefix(const int32_t* lens, int B, int T_max, int grain, std::vector<i
     for (int b = 0; b < B; ++b) {
         const int L = (lens[b] >= 1 && lens[b] <= T_max) ? lens[b] : 0;
         prefix[b + 1] = prefix[b] + L;
-        uprefix[b + 1] = uprefix[b] + (int32_t)kvc::units_of(L, grain);
+        uprefix[b + 1] = uprefix[b] + (int32_t)kvc::stream_units(L, grain);
     }
     return true;
 }
@@ -360,7 +360,7 @@ int kvc_plan_stream_ctas(const int32_t* lens_host, int B, int H_kv, int T_max, i
     if (W == 0 || nu == 0) return KVC_EINVAL;
     const int64_t Pu = kvc::plan_ctas(W, U, P, min_tokens);
     const int64_t u0 = (int64_t)H_kv * uprefix[b] + (int64_t)h * nu;
-    *first = (int)kvc::cta_of(u0, U, Pu);
+    *first = (int)kvc::cta_of(u0 + kvc::stream_cost(grain), U, Pu);
     *last = (int)kvc::cta_of(u0 + nu - 1, U, Pu);
     return KVC_OK;
 }

@@ -4,12 +4,12 @@ paged cache's host-side argument checks.
 
 Each stream is cut into units of g tokens (g = 128, one tcgen05 tile; g = 1, the plain token
 split, or a paged block, for groups of 16 or 32 heads merged inside the kernel; the last unit of
-a stream may be partial) and CTA i of Pu takes units [floor(i U / Pu), floor((i+1) U / Pu)).  Checked here by
-brute force over the cuts: cuts increase strictly (no empty CTA) and sit on unit boundaries of
-their stream (so on block boundaries of a paged pool with blocks of up to 128 tokens), every CTA
-holds floor(U / Pu) or ceil(U / Pu) units (the tiles a CTA streams), the first / last CTA of
-every stream match the formula the merge uses, and the partial-state slot (CTA + stream) is
-injective.
+a stream may be partial); with g = 128 a stream is charged one more unit for its start, placed
+before its first token unit.  CTA i of Pu takes units [floor(i U / Pu), floor((i+1) U / Pu)).
+Checked here: the cuts equal those of a separate Python statement of that rule, never decrease
+and sit on unit boundaries of their stream (so on block boundaries of a paged pool with blocks
+of up to 128 tokens); the first / last CTA of every stream match a brute-force search over the
+cuts; the partial-state slot (CTA + stream) is injective.
 """
 import ctypes
 
@@ -57,6 +57,23 @@ def _units_in(streams, a, b, g=UNIT):
     return n
 
 
+def _model_cuts(lens, H_kv, T_max, P, min_tokens, g):
+    """The partition rule, restated: stream costs, unit cuts, token positions."""
+    streams, W = _streams(lens, H_kv, T_max)
+    c = 1 if g == UNIT else 0
+    costs = [(L + g - 1) // g + c for *_, L in streams]
+    cs = np.concatenate([[0], np.cumsum(costs)])
+    U = int(cs[-1])
+    Pu = min(P, -(-W // min_tokens), U)
+
+    def pos(x):
+        k = int(np.searchsorted(cs, x, side="right") - 1)
+        j = x - cs[k]
+        return streams[k][2] + max(0, j - c) * g
+
+    return Pu, [pos(i * U // Pu) for i in range(Pu)] + [W]
+
+
 CASES = [  # lens, H_kv, T_max, P, min_tokens
     ([3001, 4500, 5999, 3000, 4200], 8, 6016, 152, 256),
     ([4097] * 4, 8, 4224, 152, 1),               # every stream ends in a one-token unit
@@ -74,17 +91,19 @@ CASES = [  # lens, H_kv, T_max, P, min_tokens
 def test_cuts_fall_on_unit_boundaries_and_balance_the_units(lib, lens, H_kv, T_max, P, min_tokens, grain):
     Pu, cuts = _plan(lib, lens, H_kv, T_max, P, min_tokens, grain)
     streams, W = _streams(lens, H_kv, T_max)
-    U = sum((L + grain - 1) // grain for *_, L in streams)
-    assert Pu == min(P, -(-W // min_tokens), U)
+    mPu, mcuts = _model_cuts(lens, H_kv, T_max, P, min_tokens, grain)
+    assert Pu == mPu and list(cuts) == mcuts
     assert cuts[0] == 0 and cuts[-1] == W
-    assert np.all(np.diff(cuts) > 0), "an empty CTA range"
+    assert np.all(np.diff(cuts) >= 0)
     for c in cuts[1:-1]:
+        if c == W:
+            continue
         owner = next(s for (_, _, s, L) in streams if s <= c < s + L)
         assert (c - owner) % grain == 0, f"cut {c} inside a unit"
+    # token units per CTA: the unit counts differ by at most one plus the stream starts held
     per_cta = [_units_in(streams, cuts[i], cuts[i + 1], grain) for i in range(Pu)]
-    assert sum(per_cta) == U
-    assert per_cta == [(i + 1) * U // Pu - i * U // Pu for i in range(Pu)]
-    assert max(per_cta) - min(per_cta) <= 1
+    U_tok = sum((L + grain - 1) // grain for *_, L in streams)
+    assert sum(per_cta) == U_tok
 
 
 @pytest.mark.parametrize("grain", [UNIT, 1])
@@ -115,6 +134,17 @@ def test_paged_blocks_are_never_split(lib, bs):
     for c in cuts[1:-1]:
         owner = next(s for (_, _, s, L) in streams if s <= c < s + L)
         assert (c - owner) % bs == 0
+
+
+def test_stream_starts_are_charged_a_unit(lib):
+    # 4 streams of 4 units each, 2 CTAs: costs 5 + 5 + 5 + 5, so each CTA takes two streams
+    lens, H_kv = [512, 512], 2
+    Pu, cuts = _plan(lib, lens, H_kv, 512, 2, 1)
+    assert Pu == 2 and list(cuts) == [0, 1024, 2048]
+    # 3 CTAs over costs 5 + 5 + 5 + 5 = 20: cuts at cost 6 (stream 1, first token unit) and 13
+    # (stream 2, its third unit: token 2 * 128)
+    Pu, cuts = _plan(lib, lens, H_kv, 512, 3, 1)
+    assert Pu == 3 and list(cuts) == [0, 512, 1024 + 256, 2048]
 
 
 def test_block_size_one_grain_is_the_plain_token_split(lib):
