@@ -1215,8 +1215,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 if (fused && t == c.it.L - 1) {
                     const __nv_bfloat16* kr = static_cast<const __nv_bfloat16*>(p.k_new) + unit * D;
                     const __nv_bfloat16* vr = static_cast<const __nv_bfloat16*>(p.v_new) + unit * D;
-                    a = FP8 ? f8_row_scale(kr) : q8_row_scale(kr);
-                    b = FP8 ? f8_row_scale(vr) : q8_row_scale(vr);
+                    const float2 sc = new_row_scales(kr, vr, FP8 ? 1 : 0);
+                    a = sc.x;
+                    b = sc.y;
                 } else {
                     a = __ldcg(p.Ksc + unit * p.T_max + t);
                     b = __ldcg(p.Vsc + unit * p.T_max + t);

@@ -435,6 +435,13 @@ __device__ __forceinline__ float f8_row_scale(const __nv_bfloat16* x) {
     }
     return __fdiv_rn(amax, 448.f);
 }
+// The K and V row scales of a fused step's new row, computed from k_new / v_new as its append
+// computes them (fp8 != 0: E4M3 scales, else int8).  Out of line: it runs once per stream, and
+// inlined at each call site of the tile loops it would crowd their instruction cache.
+static __device__ __noinline__ float2 new_row_scales(const __nv_bfloat16* kr, const __nv_bfloat16* vr, int fp8);
+static __device__ __noinline__ float2 new_row_scales(const __nv_bfloat16* kr, const __nv_bfloat16* vr, int fp8) {
+    return fp8 ? make_float2(f8_row_scale(kr), f8_row_scale(vr)) : make_float2(q8_row_scale(kr), q8_row_scale(vr));
+}
 // Warp-cooperative: lane l encodes elements 4l .. 4l+3 of a D = 128 row; lane 0 stores the scale.
 __device__ __forceinline__ void f8_store_row(const __nv_bfloat16* x, uint8_t* codes, float* scale, int lane) {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(x) + lane);
