@@ -1065,35 +1065,10 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // For each segment of this CTA, in order: wait for the softmax warps' final state in
         // `merge`, write the output or the partial state, merge the stream if this CTA is the
         // last to finish it, release `merge`.  Runs beside the next segment's tiles.
-        const int et = tid - (2 + C::NW) * 32;
-        SegIter it;
-        it.init(prefix, B, H_kv, r0, r1);
-        bool ok = true;
-        for (int sg = 0; it.valid; ++sg) {
-            ok = ok && mbar_wait(m_full, (uint32_t)(sg & 1), abort_flag, p.err);
-            SegIter nx = it;
-            nx.next();
-            if (!nx.valid) {
-                final_segment(ok, it, et);
-                break;
-            }
-            // the merge buffer goes back to the softmax warps as soon as it has been read; the
-            // partial state's fence, arrival count and any merge of the stream follow
-            if (ok)
-                finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
-                                                              U, P, last_flag, et,
-                                                              [&]() { mbar_arrive(m_empty); });
-            else
-                mbar_arrive(m_empty);
-            it = nx;
-        }
-    } else {
-        // ======================================================= softmax + accumulate
-        // zero the padded q rows and the P rows of padded heads (they stay zero), and write the
-        // fused append's new rows; then meet the MMA warp (named barrier 2) for the TMEM base
-        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += C::NW * 32)
-            reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (warp == 2 && fused) {
+        // The fused append's new rows, written by the first epilogue warp, idle until the first
+        // segment ends: the producer waits for them only at the tile that holds them, and no warp
+        // on the way to the first tile waits for their k_new / v_new loads.
+        if (warp == 2 + C::NW && fused) {
             SegIter it;
             it.init(prefix, B, H_kv, r0, r1);
             while (it.valid) {
@@ -1159,6 +1134,34 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(append_bar);
         }
+        const int et = tid - (2 + C::NW) * 32;
+        SegIter it;
+        it.init(prefix, B, H_kv, r0, r1);
+        bool ok = true;
+        for (int sg = 0; it.valid; ++sg) {
+            ok = ok && mbar_wait(m_full, (uint32_t)(sg & 1), abort_flag, p.err);
+            SegIter nx = it;
+            nx.next();
+            if (!nx.valid) {
+                final_segment(ok, it, et);
+                break;
+            }
+            // the merge buffer goes back to the softmax warps as soon as it has been read; the
+            // partial state's fence, arrival count and any merge of the stream follow
+            if (ok)
+                finish_segment<T, G, D, C::HS, 1, C::NEPI, 3>(p, merge, it, (size_t)it.b * H_kv + it.h,
+                                                              U, P, last_flag, et,
+                                                              [&]() { mbar_arrive(m_empty); });
+            else
+                mbar_arrive(m_empty);
+            it = nx;
+        }
+    } else {
+        // ======================================================= softmax + accumulate
+        // zero the padded q rows and the P rows of padded heads (they stay zero); then meet the
+        // MMA warp (named barrier 2) for the TMEM base
+        for (int i = tid - 64; i < (C::OPB_BYTES + 2 * C::PBUF) / 16; i += C::NW * 32)
+            reinterpret_cast<uint4*>(qsw)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_async_smem();
         tc5_fence_before();
         named_bar_sync(2, 32 + C::NW * 32);
