@@ -1003,12 +1003,16 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         }
     } else if (QUANT && warp >= 2 + C::NW + C::NEPI) {
         // ======================================================= int8 -> bf16 converters
-        // Per stage, in tile order: wait for the copies, widen the K and V tiles in place
-        // (int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of
-        // column blocks 0 and 1), publish to the tensor cores, arrive.  Column block 0 is
-        // written first (it does not overlap the int8 rows); after a barrier of the converter
-        // warps, each thread widens whole rows' second halves in place.
+        // Per stage, in tile order: wait for the copies, widen the K and then the V tile in place
+        // (int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of column
+        // blocks 0 and 1), publish to the tensor cores, arrive.  Unit u = (row u >> 3, 16-code
+        // group u & 7): a quarter warp reads one whole 128-byte int8 row (no bank conflicts).
+        // Every thread loads all its units of the tensor before any thread writes (the bf16
+        // rows of column block 1 overwrite the int8 rows), then widens them, storing the two
+        // 16-byte halves of a unit in an order that keeps a quarter warp's stores on distinct
+        // banks (groups 0-3 land in column block 0, 4-7 in block 1, at the same chunk offsets).
         const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
+        constexpr int PER = TT * 8 / (C::NCONV * 32);     // units per thread and tensor (8)
         Cur cc;
         cc.init(prefix, B, H_kv, r0, r1);
         int s = 0;
@@ -1017,43 +1021,35 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         while (cc.valid) {
             ok = ok && mbar_wait(&full_bar[s], ph, abort_flag, p.err);
             unsigned char* st = ring + s * C::STAGE_BYTES;
-            // (the barriers run whatever ok is: a thread that gave up must not strand the others)
-            if (ok) {
-                // column block 0: unit = (tensor, row, 16-byte group g of columns 16g .. 16g+15)
-#pragma unroll 4
-                for (int u = ct; u < 2 * TT * 4; u += C::NCONV * 32) {
-                    unsigned char* tb = st + (u >> 9) * C::TILE_BYTES;
-                    const int r = (u >> 2) & (TT - 1), g = u & 3;
-                    const uint4 v = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + r * C::D + g * 16);
-                    uint4 o0, o1;
-                    widen_i8x16(v, o0, o1);
-                    unsigned char* row = tb + r * 128;
-                    *reinterpret_cast<uint4*>(row + (((2 * g) ^ (r & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ (r & 7)) << 4)) = o1;
-                }
-            }
-            named_bar_sync(4, C::NCONV * 32);
-            // column block 1, in place: a thread owns whole rows (it reads a row's last 64 bytes
-            // before writing the row's 128); the read order rotates with the row so that the
-            // threads of a quarter warp hit different banks
-            if (ok) {
-#pragma unroll 2
-                for (int u = ct; u < 2 * TT; u += C::NCONV * 32) {
-                    const int r = u & (TT - 1);
-                    unsigned char* row = st + (u >> 7) * C::TILE_BYTES + C::HALF_BYTES + r * 128;
-                    uint4 v[4];  // v[i] holds column group (i + r) mod 4
+#pragma unroll 1
+            for (int tsr = 0; tsr < 2; ++tsr) {  // K, then V
+                unsigned char* tb = st + tsr * C::TILE_BYTES;
+                uint4 v[PER];
+                if (ok)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        v[i] = *reinterpret_cast<const uint4*>(row + 64 + ((i + r) & 3) * 16);
+                    for (int i = 0; i < PER; ++i) {
+                        const int u = ct + i * C::NCONV * 32;
+                        v[i] = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + (u >> 3) * C::D + (u & 7) * 16);
+                    }
+                // (the barrier runs whatever ok is: a thread that gave up must not strand the others)
+                named_bar_sync(4, C::NCONV * 32);
+                if (ok)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int g = (i + r) & 3;
+                    for (int i = 0; i < PER; ++i) {
+                        const int u = ct + i * C::NCONV * 32;
+                        const int r = u >> 3, g = u & 7;
                         uint4 o0, o1;
                         widen_i8x16(v[i], o0, o1);
-                        *reinterpret_cast<uint4*>(row + (((2 * g) ^ (r & 7)) << 4)) = o0;
-                        *reinterpret_cast<uint4*>(row + (((2 * g + 1) ^ (r & 7)) << 4)) = o1;
+                        unsigned char* row = tb + (g >> 2) * C::HALF_BYTES + r * 128;
+                        const int c0 = 2 * (g & 3);
+                        if (g & 4) {
+                            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+                            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
+                        } else {
+                            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
+                            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+                        }
                     }
-                }
             }
             fence_async_smem();  // generic-proxy writes before the tensor cores read them
             mbar_arrive(&conv_full[s]);
