@@ -44,7 +44,7 @@ struct Tc5Cfg {
     static constexpr int NW = 4 * HSPLIT;
     static constexpr int NEPI = 2;                      // segment-epilogue warps
     static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
-    static constexpr int NCONV = 4;                     // converter warps (int8 and fp8 caches)
+    static constexpr int NCONV = MODE_ == 3 && G_ <= 4 ? 8 : 4;  // converter warps (int8 and fp8 caches)
     static constexpr int TT = 128;                      // tokens per tile = MMA M
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
     static constexpr int HALF_BYTES = TT * 128;         // one column block of a 16-bit K or V tile
