@@ -1005,12 +1005,12 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         // ======================================================= int8 -> bf16 converters
         // Per stage, in tile order: wait for the copies, widen the K and then the V tile in place
         // (int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of column
-        // blocks 0 and 1), publish to the tensor cores, arrive.  Unit u = (row u >> 3, 16-code
-        // group u & 7): a quarter warp reads one whole 128-byte int8 row (no bank conflicts).
-        // Every thread loads all its units of the tensor before any thread writes (the bf16
-        // rows of column block 1 overwrite the int8 rows), then widens them, storing the two
-        // 16-byte halves of a unit in an order that keeps a quarter warp's stores on distinct
-        // banks (groups 0-3 land in column block 0, 4-7 in block 1, at the same chunk offsets).
+        // blocks 0 and 1), publish to the tensor cores, arrive.  Every thread loads all its units
+        // of the tensor before any thread writes (the bf16 rows of column block 1 overwrite the
+        // int8 rows), then widens them.  A unit is 16 codes (group g) of one row; a quarter warp
+        // takes rows 2p and 2p + 1, groups 0-3 of one and 4-7 of the other, so its 16-byte loads
+        // cover the 8 bank groups once, and so do its stores (row 2p + 1's chunks are row 2p's
+        // XOR 1 under the swizzle): no bank conflicts and no divergent stores.
         const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
         constexpr int PER = TT * 8 / (C::NCONV * 32);     // units per thread and tensor (8)
         Cur cc;
@@ -1029,7 +1029,9 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
                     for (int i = 0; i < PER; ++i) {
                         const int u = ct + i * C::NCONV * 32;
-                        v[i] = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + (u >> 3) * C::D + (u & 7) * 16);
+                        const int rs = (u >> 2) & 1;
+                        const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
+                        v[i] = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + r * C::D + g * 16);
                     }
                 // (the barrier runs whatever ok is: a thread that gave up must not strand the others)
                 named_bar_sync(4, C::NCONV * 32);
@@ -1037,18 +1039,14 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
 #pragma unroll
                     for (int i = 0; i < PER; ++i) {
                         const int u = ct + i * C::NCONV * 32;
-                        const int r = u >> 3, g = u & 7;
+                        const int rs = (u >> 2) & 1;
+                        const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
                         uint4 o0, o1;
                         widen_i8x16(v[i], o0, o1);
                         unsigned char* row = tb + (g >> 2) * C::HALF_BYTES + r * 128;
                         const int c0 = 2 * (g & 3);
-                        if (g & 4) {
-                            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
-                            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
-                        } else {
-                            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
-                            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
-                        }
+                        *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
                     }
             }
             fence_async_smem();  // generic-proxy writes before the tensor cores read them
