@@ -42,18 +42,23 @@ struct Tc5Cfg {
     static constexpr int HSPLIT = G >= 16 ? 2 : 1;
     static constexpr int GH = G / HSPLIT;
     static constexpr int NW = 4 * HSPLIT;
-    static constexpr int NEPI = 2;                      // segment-epilogue warps
+    // segment-epilogue warps (int8 cache with groups of up to 4 heads: one, which leaves room
+    // for the MMA2 warp within 16 warps)
+    static constexpr int NEPI = MODE_ == 3 && G_ <= 4 ? 1 : 2;
     static constexpr int NTHREADS = (2 + NW + NEPI) * 32;
     static constexpr int NCONV = MODE_ == 3 && G_ <= 4 ? 8 : 4;  // converter warps (int8 and fp8 caches)
     static constexpr int TT = 128;                      // tokens per tile = MMA M
     static constexpr int BOX_ROWS = TC_BOX_ROWS;
     static constexpr int HALF_BYTES = TT * 128;         // one column block of a 16-bit K or V tile
     static constexpr int TILE_BYTES = TT * ROWB;        // a 16-bit tile
-    // a ring stage holds one tile of K and one of V as they land: 16-bit tiles, or for an fp8
+    // a ring stage holds one tile of K and one of V as they land: 16-bit tiles; for an fp8
     // cache 8-bit ones (TT rows of D bytes, 128-byte swizzled), whose V is widened into one of
-    // two f16 working tiles (VW)
-    static constexpr int LAND_BYTES = FP8 ? TT * D : TILE_BYTES;
-    static constexpr int STAGE_BYTES = 2 * LAND_BYTES;
+    // two f16 working tiles (VW); for an int8 cache the K codes (128-byte swizzled, widened into
+    // tensor memory) and a 16-bit V tile area whose back column block the V codes land in
+    static constexpr bool Q8 = MODE_ == 3;
+    static constexpr int KLAND = (FP8 || Q8) ? TT * D : TILE_BYTES;  // K area of a stage
+    static constexpr int VAREA = FP8 ? TT * D : TILE_BYTES;          // V area of a stage
+    static constexpr int STAGE_BYTES = KLAND + VAREA;
     static constexpr int VW_BYTES = FP8 ? 2 * TILE_BYTES : 0;
     static constexpr int OPB_BLOCK = N * 128;           // one column block of a K-major [N][128 B] operand
     static constexpr int OPB_BYTES = (FP8 ? 1 : HALVES) * OPB_BLOCK;
@@ -89,7 +94,10 @@ struct Tc5Cfg {
     static constexpr int RING_BYTES = SPLIT ? (NST + NV) * TILE_BYTES : NST * STAGE_BYTES;
     static constexpr int SMEM = RING_BYTES + FIXED;
     // S^T buffers [0, N) and [N, 2N); O^T buffers (hi and lo columns) [2N, 2N + N2), [2N + N2, 2N + 2 N2)
-    static constexpr int TMEM_NEED = 2 * N + 2 * N2;
+    // int8 cache: two bf16 K tiles, MMA1's A operand (lane = token, 64 columns of 2 dims each),
+    // at columns [KA_COL, KA_COL + 128)
+    static constexpr int KA_COL = 128;
+    static constexpr int TMEM_NEED = Q8 ? KA_COL + 128 : 2 * N + 2 * N2;
     static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : 256));
     static_assert(NST >= 2, "ring too shallow");
     static_assert(!SPLIT || NST >= 3, "split rings: at least 3 K slots");
@@ -97,6 +105,7 @@ struct Tc5Cfg {
     static_assert(HSPLIT == 1 || GH % 8 == 0, "head slices start on a swizzle row group");
     static_assert(!PMN || NP <= 32, "P_hi and P_lo share one 64-column row");
     static_assert(!FP8 || G <= 8, "fp8 cache: up to 8 query heads per KV head");
+    static_assert(!Q8 || 2 * N + 2 * N2 <= KA_COL, "int8 cache: S^T and O^T below the K tiles");
     static_assert(OPB_BLOCK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms aligned");
 };
 
@@ -112,12 +121,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= (uint64_t)2u << 61;
     return d;
 }
-// fp8 cache with groups of up to 4 heads: one more warp, which issues MMA2 alone (the MMA warp then
-// issues only MMA1; each tcgen05.mma holds its issuing thread ~90 cycles, and the two contractions
-// plus their waits exceeded an fp8 tile's time on one thread)
+// 8-bit caches with groups of up to 4 heads: one more warp, which issues MMA2 alone (the MMA warp
+// then issues only MMA1; each tcgen05.mma holds its issuing thread ~90-110 cycles, and the two
+// contractions plus their waits exceeded an 8-bit tile's time on one thread; from the producer
+// thread, MMA2 delayed the next tile's copies)
 template <int G, int MODE>
 __host__ __device__ constexpr bool tc5_mma2_warp() {
-    return MODE == 4 && G <= 4;
+    return (MODE == 3 || MODE == 4) && G <= 4;
 }
 // Threads of the kernel instantiation: a quantized cache adds the converter warps.
 template <int G, int MODE>
@@ -160,6 +170,29 @@ __device__ __forceinline__ void tc5_mma(uint32_t d_tmem, uint64_t a, uint64_t b,
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+// A (M = 128 rows, K-major 16-bit) from tensor memory: row m in lane m, two K elements per column.
+__device__ __forceinline__ void tc5_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane (completion: tc5_wait_st).
+__device__ __forceinline__ void tc5_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tc5_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ void tc5_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -262,7 +295,7 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
     const int n = c.n();
     const size_t unit = (size_t)c.it.b * p.H_kv + c.it.h;
     const uint32_t ks = ring + stage * C::STAGE_BYTES;
-    const uint32_t vs = ks + C::LAND_BYTES;
+    const uint32_t vs = ks + C::KLAND;
     constexpr bool PAGED = MODE == 1, QUANT = MODE == 3, FP8 = MODE == 4;
     constexpr bool paged = PAGED;
     const bool full = n == TT && !paged;
@@ -301,14 +334,16 @@ __device__ __forceinline__ void issue_tile_tc5(const DecodeParams& p, const Tile
             tma_load_2d(vs + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
         }
     } else if (QUANT) {
-        // int8 rows (128 bytes) into the back column block of the tile area, widened in place later
+        // int8 rows (128 bytes): K's 128-byte swizzled into the K area (widened into tensor
+        // memory later), V's unswizzled into the back column block of the V tile area (widened
+        // in place later)
         const int row0 = (int)(unit * p.T_max + c.t);
         const CUtensorMap* mk = full ? tmKf : tmK;
         const CUtensorMap* mv = full ? tmVf : tmV;
         for (int bx = 0; bx < nbox; ++bx) {
-            const uint32_t off = C::HALF_BYTES + bx * C::BOX_ROWS * C::D;
+            const uint32_t off = bx * C::BOX_ROWS * C::D;
             tma_load_2d(ks + off, mk, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
-            tma_load_2d(vs + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
+            tma_load_2d(vs + C::HALF_BYTES + off, mv, 0, row0 + bx * C::BOX_ROWS, &full_bar[stage], pol);
         }
     } else {
         const int row0 = (int)(unit * p.T_max + c.t);
@@ -477,6 +512,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     uint64_t* sv_full = vw_empty + 2;      // [NV] split rings: V slot landed
     uint64_t* sv_empty = sv_full + 2;      // [NV] split rings: V slot read by MMA2
     int* vissued = reinterpret_cast<int*>(sv_empty + 2);  // [NV] V copies issued per slot (abort drain)
+    uint64_t* ka_empty = reinterpret_cast<uint64_t*>(vissued + 2);  // [2] int8: K tile read (MMA1 commit)
 
     // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its
     // CTAs take SMs as ours exit) but waits in griddepcontrol.wait until this grid is complete.
@@ -498,8 +534,10 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         mbar_init(m_full, C::NW * 32);
         mbar_init(m_empty, C::NEPI * 32);
         mbar_init(append_bar, 1);
-        if constexpr (QUANT)
+        if constexpr (QUANT) {
             for (int s = 0; s < NST; ++s) mbar_init(&conv_full[s], C::NCONV * 32);
+            for (int i = 0; i < 2; ++i) mbar_init(&ka_empty[i], 1);
+        }
         if constexpr (FP8)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&vw_full[i], C::NCONV * 32);
@@ -603,7 +641,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     // (fp8: the MMA warp issues MMA2 as well, one tile behind MMA1; a stage is free once MMA1
     // has read K and the converters V, and the producer thread only refills the ring: a tensor
     // copy can hold its issuing thread for hundreds of cycles, so no MMA waits behind one)
-    const bool m2p = !FP8 && (!PAGED || p.m2p != 0);
+    const bool m2p = !FP8 && !DED2 && (!PAGED || p.m2p != 0);
     // V read MN-major x P; an fp8 cache's widened V and its weights are f16
     constexpr uint32_t IDESC2 = FP8 ? instr_desc_f16(128, C::N2, 1, C::PMN ? 1 : 0)
                                     : instr_desc_bf16(128, C::N2, 1, C::PMN ? 1 : 0);
@@ -611,7 +649,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
     const uint32_t vw_s = smem_addr(vw);
     auto issue_mma2 = [&](int k, int st, uint32_t tm) {
         // V: the stage's tile, or (fp8) the f16 working tile k & 1
-        const uint64_t dV0 = smem_desc_sw128(FP8 ? vw_s : (C::SPLIT ? smem_addr(vring) : ring_s + C::TILE_BYTES),
+        const uint64_t dV0 = smem_desc_sw128(FP8 ? vw_s : (C::SPLIT ? smem_addr(vring) : ring_s + C::KLAND),
                                              LY::HSTR, LY::GSTR);
         // P: K-major rows of 64 tokens, or MN-major token rows (one 64-column pattern; the
         // leading offset is never stepped over)
@@ -783,6 +821,11 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                      "r"(C::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (QUANT) {
+            // the converter warps write K tiles into tensor memory: the allocation is theirs to read
+            tc5_fence_before();
+            named_bar_arrive(6, 32 + C::NCONV * 32);
+        }
         // Each segment's q rows (G rows of D bf16 at row unit * G of q) go into the swizzled
         // operand from registers, loaded one segment ahead and stored once the previous
         // segment's last MMA1 has read the operand.
@@ -859,7 +902,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             __syncwarp();
         };
         for (int k = 0;; ++k) {
-            if (!m2p && !FP8) {
+            if (!m2p && !FP8 && !DED2) {
                 // MMA2 of the previous tile here, first (it frees a ring stage as soon as the
                 // weights are written)
                 if (k > 0 && alive) mma2_here(k - 1);
@@ -871,7 +914,8 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             }
             if (!cur.valid || !alive) break;
             // ---- MMA1(k): S^T[k&1] = K(stage s) . Q^T
-            // int8 cache: wait until the converter warps have widened the stage to bf16
+            // int8 cache: wait until the converter warps have widened K into tensor memory and V
+            // in place
             alive = mbar_wait(QUANT ? &conv_full[s] : &full_bar[s], ph, abort_flag, p.err);
             // (fp8: the K codes are read as they landed)
             if (alive && cur.first()) {
@@ -894,6 +938,11 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                         // one 128-byte column block: k-steps of 32 codes
                         const uint32_t off = (uint32_t)(s * C::STAGE_BYTES + kk * 32);
                         tc5_mma_f8(tS, dK0 + (off >> 4), dQ0 + ((uint32_t)(kk * 32) >> 4), IDESC1, kk > 0 ? 1u : 0u);
+                    } else if constexpr (QUANT) {
+                        // K tile k & 1 in tensor memory: k-step kk is columns 8 kk .. 8 kk + 7
+                        const uint32_t qoff = (uint32_t)((kk >> 2) * C::OPB_BLOCK + (kk & 3) * 32);
+                        tc5_mma_ta(tS, tmem + (uint32_t)(C::KA_COL + (k & 1) * 64 + kk * 8), dQ0 + (qoff >> 4),
+                                   IDESC1, kk > 0 ? 1u : 0u);
                     } else {
                         // (split rings: K slots of one tile each)
                         const uint32_t off = (uint32_t)(s * (C::SPLIT ? C::TILE_BYTES : C::STAGE_BYTES) +
@@ -904,6 +953,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
                 }
                 tc5_commit(&s_full[k & 1]);
                 if constexpr (FP8) tc5_commit(&empty_bar[s]);  // K read (the converters arrive for V)
+                if constexpr (QUANT) tc5_commit(&ka_empty[k & 1]);  // the K tile in tensor memory is read
                 if constexpr (C::SPLIT) tc5_commit(&empty_bar[s]);  // split rings: the K slot is free
                 *mma1_issued += 1;
             }
@@ -916,26 +966,29 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             if (++s == NST) { s = 0; ph ^= 1u; }
         }
     } else if (DED2 && warp == 2 + C::NW + C::NEPI + C::NCONV) {
-        // ======================================================= MMA2 issue (fp8, groups <= 4)
-        // MMA2 of each tile once its weights, its O^T buffer and its f16 V working tile are ready
-        // (lane 0 issues; the warp follows its verdict)
+        // ======================================================= MMA2 issue (8-bit caches, groups <= 4)
+        // MMA2 of each tile once its weights and its O^T buffer are ready, and for fp8 its f16 V
+        // working tile (int8: the stage's V was widened before MMA1 of the tile; lane 0 issues,
+        // the warp follows its verdict)
         Cur mc;
         mc.init(prefix, B, H_kv, r0, r1);
         bool ok = true;
+        int s2 = 0;
         for (int k = 0; ok && mc.valid; ++k) {
             if (lane == 0) {
                 ok = mbar_wait(&p_full[k & 1], (k >> 1) & 1, abort_flag, p.err) &&
                      mbar_wait(&o_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err) &&
-                     mbar_wait(&vw_full[k & 1], (k >> 1) & 1, abort_flag, p.err);
+                     (!FP8 || mbar_wait(&vw_full[k & 1], (k >> 1) & 1, abort_flag, p.err));
                 if (ok) {
                     tc5_fence_after();
                     // written by warp 1's allocation before the weights of tile 0 existed
                     if (k == 0) tmem = *tmem_slot;
-                    issue_mma2(k, 0, tmem);
+                    issue_mma2(k, s2, tmem);
                 }
             }
             ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
             mc.advance();
+            if (++s2 == NST) s2 = 0;
         }
     } else if (FP8 && warp >= 2 + C::NW + C::NEPI) {
         // ======================================================= E4M3 V -> f16 converters
@@ -958,7 +1011,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             if (ok) {
                 const int n = cc.n();
                 const int loaded = n == TT ? TT : ((n + C::BOX_ROWS - 1) / C::BOX_ROWS) * C::BOX_ROWS;
-                const unsigned char* vl = ring + s * C::STAGE_BYTES + C::LAND_BYTES;
+                const unsigned char* vl = ring + s * C::STAGE_BYTES + C::KLAND;
                 unsigned char* vt = vw + w * C::TILE_BYTES;
                 // unit = (row r, 16-code column group c) -> 32 bytes of f16 (two 16-byte chunks).
                 // The 8 lanes of a quarter warp take one c and 8 consecutive rows, so their loads
@@ -1003,52 +1056,81 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
         }
     } else if (QUANT && warp >= 2 + C::NW + C::NEPI) {
         // ======================================================= int8 -> bf16 converters
-        // Per stage, in tile order: wait for the copies, widen the K and then the V tile in place
-        // (int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of column
-        // blocks 0 and 1), publish to the tensor cores, arrive.  Every thread loads all its units
-        // of the tensor before any thread writes (the bf16 rows of column block 1 overwrite the
-        // int8 rows), then widens them.  A unit is 16 codes (group g) of one row; a quarter warp
-        // takes rows 2p and 2p + 1, groups 0-3 of one and 4-7 of the other, so its 16-byte loads
-        // cover the 8 bank groups once, and so do its stores (row 2p + 1's chunks are row 2p's
-        // XOR 1 under the swizzle): no bank conflicts and no divergent stores.
+        // Per stage, in tile order: wait for the copies, widen the K codes into tensor memory and
+        // the V codes in place, publish to the tensor cores, arrive.
+        //  K: MMA1's A operand in tensor memory (buffer k & 1, free once MMA1 of tile k - 2 has
+        //   read it): a thread widens its own row (lane 32 (warp % 4) + lane, the quadrant this
+        //   warp may access; the warps of a quadrant split the row) 32 codes at a time; the codes
+        //   landed 128-byte swizzled, so the 8 rows of a quarter warp read 8 different bank groups.
+        //  V: int8 rows at column block 1 -> bf16 rows in the 128-byte-swizzled layout of column
+        //   blocks 0 and 1.  Every thread loads all its units before any thread writes (the bf16
+        //   rows of column block 1 overwrite the int8 rows), then widens them.  A unit is 16 codes
+        //   (group g) of one row; a quarter warp takes rows 2p and 2p + 1, groups 0-3 of one and
+        //   4-7 of the other, so its 16-byte loads cover the 8 bank groups once, and so do its
+        //   stores (row 2p + 1's chunks are row 2p's XOR 1 under the swizzle).
         const int ct = tid - (2 + C::NW + C::NEPI) * 32;  // 0 .. NCONV * 32 - 1
-        constexpr int PER = TT * 8 / (C::NCONV * 32);     // units per thread and tensor (8)
+        const int cw = ct >> 5;                           // converter warp
+        constexpr int PER = TT * 8 / (C::NCONV * 32);     // V units per thread (4 or 8)
+        const int kr = 32 * (warp & 3) + lane;            // K row = tensor-memory lane
+        constexpr int KP = 16 / C::NCONV;                 // 32-code pieces of that row per warp
         Cur cc;
         cc.init(prefix, B, H_kv, r0, r1);
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        while (cc.valid) {
+        named_bar_sync(6, 32 + C::NCONV * 32);  // the MMA warp has allocated tensor memory
+        tc5_fence_after();
+        const uint32_t tka = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)C::KA_COL;
+        for (int k = 0; cc.valid; ++k) {
             ok = ok && mbar_wait(&full_bar[s], ph, abort_flag, p.err);
+            ok = ok && mbar_wait(&ka_empty[k & 1], ((k >> 1) & 1) ^ 1u, abort_flag, p.err);
+            ok = __all_sync(FULL, ok);  // the tensor-memory store below is warp-wide
+            tc5_fence_after();
             unsigned char* st = ring + s * C::STAGE_BYTES;
+            if (ok)
 #pragma unroll 1
-            for (int tsr = 0; tsr < 2; ++tsr) {  // K, then V
-                unsigned char* tb = st + tsr * C::TILE_BYTES;
-                uint4 v[PER];
-                if (ok)
+                for (int q = (cw >> 2) * KP; q < (cw >> 2) * KP + KP; ++q) {  // 32 codes (16 columns) a pass
+                    uint4 c2[2];
 #pragma unroll
-                    for (int i = 0; i < PER; ++i) {
-                        const int u = ct + i * C::NCONV * 32;
-                        const int rs = (u >> 2) & 1;
-                        const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
-                        v[i] = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + r * C::D + g * 16);
-                    }
-                // (the barrier runs whatever ok is: a thread that gave up must not strand the others)
-                named_bar_sync(4, C::NCONV * 32);
-                if (ok)
+                    for (int j = 0; j < 2; ++j)
+                        c2[j] = *reinterpret_cast<const uint4*>(st + kr * 128 + (((2 * q + j) ^ (kr & 7)) << 4));
+                    uint32_t w[16];
 #pragma unroll
-                    for (int i = 0; i < PER; ++i) {
-                        const int u = ct + i * C::NCONV * 32;
-                        const int rs = (u >> 2) & 1;
-                        const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
+                    for (int j = 0; j < 2; ++j) {
                         uint4 o0, o1;
-                        widen_i8x16(v[i], o0, o1);
-                        unsigned char* row = tb + (g >> 2) * C::HALF_BYTES + r * 128;
-                        const int c0 = 2 * (g & 3);
-                        *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
-                        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+                        widen_i8x16(c2[j], o0, o1);
+                        w[8 * j + 0] = o0.x; w[8 * j + 1] = o0.y; w[8 * j + 2] = o0.z; w[8 * j + 3] = o0.w;
+                        w[8 * j + 4] = o1.x; w[8 * j + 5] = o1.y; w[8 * j + 6] = o1.z; w[8 * j + 7] = o1.w;
                     }
-            }
+                    tc5_st16(tka + (uint32_t)((k & 1) * 64 + q * 16), w);
+                }
+            unsigned char* tb = st + C::KLAND;
+            uint4 v[PER];
+            if (ok)
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int u = ct + i * C::NCONV * 32;
+                    const int rs = (u >> 2) & 1;
+                    const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
+                    v[i] = *reinterpret_cast<const uint4*>(tb + C::HALF_BYTES + r * C::D + g * 16);
+                }
+            // (the barrier runs whatever ok is: a thread that gave up must not strand the others)
+            named_bar_sync(4, C::NCONV * 32);
+            if (ok)
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int u = ct + i * C::NCONV * 32;
+                    const int rs = (u >> 2) & 1;
+                    const int r = ((u >> 4) << 1) | rs, g = ((rs ^ (u >> 3)) & 1) << 2 | (u & 3);
+                    uint4 o0, o1;
+                    widen_i8x16(v[i], o0, o1);
+                    unsigned char* row = tb + (g >> 2) * C::HALF_BYTES + r * 128;
+                    const int c0 = 2 * (g & 3);
+                    *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+                }
+            tc5_wait_st();
+            tc5_fence_before();  // tensor-memory stores before the MMA warp's wait
             fence_async_smem();  // generic-proxy writes before the tensor cores read them
             mbar_arrive(&conv_full[s]);
             cc.advance();
@@ -1401,7 +1483,7 @@ __global__ void __launch_bounds__(tc5_threads<G, MODE>(), 1)
             const int loaded = ((n + br - 1) / br) * br;
             if (!FP8 && h0 == 0 && row >= loaded) {
                 using LY = Tc5Layout<C, PAGED>;
-                unsigned char* vt = (C::SPLIT ? vring + (k % C::NV) * C::TILE_BYTES : ring + s * C::STAGE_BYTES + C::TILE_BYTES) +
+                unsigned char* vt = (C::SPLIT ? vring + (k % C::NV) * C::TILE_BYTES : ring + s * C::STAGE_BYTES + C::KLAND) +
                                     (row >> 3) * LY::GSTR + (row & 7) * 128;
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf)

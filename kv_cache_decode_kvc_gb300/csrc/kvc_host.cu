@@ -137,8 +137,9 @@ bool make_q8_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_row
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over an fp8 cache with D = 128 (rows of 128 E4M3 codes): boxes of 128 bytes x box_rows
-// rows, 128-byte swizzle (the K tile is MMA1's operand as it lands).
+// 2-D map over an 8-bit cache with D = 128 (rows of 128 codes): boxes of 128 bytes x box_rows
+// rows, 128-byte swizzle (an fp8 K tile is MMA1's operand as it lands; an int8 K tile is read a
+// row per thread).
 bool make_f8_tensor_map(CUtensorMap* map, void* base, uint64_t rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
@@ -465,10 +466,11 @@ static int create_common(kvc_t* out, int layers, int B, int H_q, int H_kv, int D
                      make_f8_tensor_map(&m4[1], vb, rows, box_small) &&
                      make_f8_tensor_map(&m4[2], kb, rows, box_full) &&
                      make_f8_tensor_map(&m4[3], vb, rows, box_full);
-            else if (quant)  // int8 rows of 128 bytes, unswizzled (widened to bf16 in the kernel)
-                ok = make_q8_tensor_map(&m4[0], kb, rows, box_small) &&
+            else if (quant)  // int8 rows of 128 bytes: K 128-byte swizzled (each converter thread
+                             // widens a whole row), V unswizzled (widened in place)
+                ok = make_f8_tensor_map(&m4[0], kb, rows, box_small) &&
                      make_q8_tensor_map(&m4[1], vb, rows, box_small) &&
-                     make_q8_tensor_map(&m4[2], kb, rows, box_full) &&
+                     make_f8_tensor_map(&m4[2], kb, rows, box_full) &&
                      make_q8_tensor_map(&m4[3], vb, rows, box_full);
             else if (paged)  // the tcgen05 kernel's paged variant (D = 128) reads 4-D boxes
                 ok = make_paged_tensor_map(&m4[0], kb, rows, box_small) &&
