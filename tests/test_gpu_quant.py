@@ -96,6 +96,21 @@ def test_quant_split_t_any_split_matches(ctas, mode):
     check_close(out, ref, torch.bfloat16, f"int8 ctas={ctas} mode={mode}", abs_att=_abs_att(case, qc))
 
 
+@pytest.mark.parametrize("G", [1, 8])
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_quant_long_segments_per_cta(G, ctas):
+    """One or two CTAs, so each streams dozens of tiles through every ring stage and both
+    tensor-memory K buffers many times over (G = 8 runs the four-converter layout, G = 1 the
+    eight-converter one with its own MMA2 warp); one stream ends in a partial tile."""
+    case = Case(1020 + G, 3, 2 * G, 2, 128, [2000, 1333, 129], "bf16")
+    T_max = 2048
+    out, views = _run(case, T_max, ctas=ctas)
+    qc = _oracle(case, T_max)
+    _check_cache(views, qc)
+    ref = qc.decode_attn(host_bits(case.q), case.lens.numpy())
+    check_close(out, ref, torch.bfloat16, f"int8 long G={G} ctas={ctas}", abs_att=_abs_att(case, qc))
+
+
 @pytest.mark.parametrize("overlap", [0, 1])
 def test_quant_layer_loop_with_overlap(overlap):
     """Several layers back to back (each with its own seeded data), repeated steps."""
