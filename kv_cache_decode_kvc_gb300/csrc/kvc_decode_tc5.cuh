@@ -422,11 +422,12 @@ __device__ __forceinline__ bool group_any(bool pred) {
 }
 
 // Warp roles: warp 0 issues the tensor copies (producer) and MMA2 (for a paged pool with
-// m2p = 0, warp 1 does), warp 1 issues MMA1 and loads q, warps 2 .. 2+NW-1 run the softmax,
-// write P and accumulate O (thread <-> tensor-memory lane 32*(warp%4) + lane), the next two
-// warps finish segments (output or partial state, and the merge of a stream whose last segment
-// this CTA completes) while the next segment streams; the CTA's last segment is finished by the
-// epilogue and softmax warps together.
+// m2p = 0, warp 1 does; for an 8-bit cache with G <= 4, a warp of its own), warp 1 issues MMA1
+// and loads q, warps 2 .. 2+NW-1 run the softmax, write P and accumulate O (thread <->
+// tensor-memory lane 32*(warp%4) + lane), the next NEPI warps finish segments (output or
+// partial state, and the merge of a stream whose last segment this CTA completes) while the
+// next segment streams; the CTA's last segment is finished by the epilogue and softmax warps
+// together.  8-bit caches add NCONV converter warps after those, then the MMA2 warp if any.
 // Double buffers: S^T and O^T in tensor memory, P in shared memory; MMA1 of tile k+1 runs while
 // the softmax warps work on tile k, and O^T(k-1) is folded in after the softmax of tile k.
 // Slot of a stream's new row in the fused step (the row a preceding append may just have
