@@ -117,7 +117,9 @@ int kvc_layer_ptrs(kvc_t h, int layer, void** K, void** V);
 int kvc_last_error(kvc_t h, void* stream, uint32_t* detail);
 
 /* Number of CTAs the attention kernel splits the work over (0 restores the default: one per
- * SM).  1 <= ctas <= 4 * SMs.  Changes only the split, never the result beyond rounding. */
+ * SM, or four fifths of the SMs when the combine kernel merges the streams, see
+ * kvc_set_combine_mode).  1 <= ctas <= 4 * SMs.  Changes only the split, never the result beyond
+ * rounding.  kvc_get_ctas returns the setting (the SM count while it is 0). */
 int kvc_set_ctas(kvc_t h, int ctas);
 int kvc_get_ctas(kvc_t h);
 

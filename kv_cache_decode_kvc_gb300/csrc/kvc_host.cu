@@ -266,6 +266,12 @@ int attn_common(kvc_t h, int layer, const void* q, const void* k_new, const void
         mode = (nseg * h->G * T_q * h->D * 4 > 65536) ? 1 : 0;
     }
     p.combine_mode = mode;
+    // Few long streams merged by the combine kernel (a segment per CTA): a decode grid of four
+    // fifths of the SMs measured faster on MQA B = 1, T = 131072, G = 32 (us per layer with
+    // 104 / 120 / 136 / 152 CTAs: 26.8 / 26.5 / 29.8 / 29.2; this rule's 121 on one box: 28.2-28.5
+    // against 26.2-26.4 with 120 and 29.2 with 152, a step not understood).  Grids merged in-kernel
+    // keep one CTA per SM (MQA B = 64 with 120 CTAs: 44.7 against 37.5).
+    if (mode == 1 && h->ctas <= 0) p.P = h->sms * 4 / 5;
     p.grain = kvc::partition_grain(h->G, mode, p.bs);
     p.qscale = (float)(1.4426950408889634 / sqrt((double)h->D));
     p.overlap = h->overlap;
